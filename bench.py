@@ -1,0 +1,481 @@
+#!/usr/bin/env python3
+"""Benchmark: paged decode attention over a chunked-slab KV pool on GB300.
+
+One step = one decode pass over every layer of the workload (one
+pkv_paged_decode_attention launch per layer) with K/V, block tables and q already
+resident in HBM.  Default workload: Qwen3-0.6B-shaped decode (28 layers, Hq 16 / Hkv 8
+/ D 128, bf16, 8 sequences x 4096 tokens, fragmented slab-crossing block tables).
+
+Prints one JSON line (rank 0).  `value` is achieved HBM bandwidth in GB/s of
+algorithmic bytes (K/V payload + metadata + q/out + block-table entries used +
+context lengths) summed over ranks; `kv_tokens_per_s` is the other half of the metric.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+                  [--workload NAME]
+
+`--impl reference` times the oracle (plain FP64 C on the host cores) on a bounded
+sample of the same workload.  Multi-GPU runs (torchrun) are independent replicas:
+every rank processes its own batch, with no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_cache_split_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of peak), KV tokens read/s"
+FMT_ROW_BYTES = {wl.FMT_BF16: (2.0, 2.0, 0), wl.FMT_K4V4: (0.5, 0.5, 1), wl.FMT_K8V4: (1.0, 0.5, 1),
+                 wl.FMT_K8V8: (1.0, 1.0, 1)}
+
+
+def token_head_bytes(fmt: int, D: int) -> int:
+    kb, vb, packed = FMT_ROW_BYTES[fmt]
+    return int(kb * D + vb * D + packed * 2 * (D // 32) * 8)
+
+
+def algorithmic_bytes(fmt, D, Hkv, Hq, lens) -> int:
+    """K/V payload + metadata of tokens < L, q and out, block-table entries used, ctx."""
+    B = len(lens)
+    kv = sum(lens) * Hkv * token_head_bytes(fmt, D)
+    qo = 2 * B * Hq * D * 2
+    bt = sum(wl.nblocks(L) for L in lens) * 4
+    return kv + qo + bt + 4 * B
+
+
+def workload_for(name: str):
+    if name == "qwen3-0.6b":
+        return wl.qwen3_0_6b()
+    if name == "tiny":
+        return wl.tiny()
+    if name == "qwen3-1.7b-k4v4":
+        return wl.qwen3_1_7b_k4v4()
+    if name == "llama-3.2-1b-k8v4":
+        return wl.llama_1b(wl.FMT_K8V4)
+    if name == "llama-3.2-1b-k8v8":
+        return wl.llama_1b(wl.FMT_K8V8)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def describe(w) -> str:
+    L = sorted(set(w.lens))
+    lens = f"{w.B} x {L[0]}" if len(L) == 1 else f"{w.B} x [{min(w.lens)}..{max(w.lens)}]"
+    return (f"{w.name}-shaped decode: {w.n_layers} layer(s), Hq {w.Hq} / Hkv {w.Hkv} / D {w.D}, "
+            f"{wl.FMT_NAMES[w.fmt]}, {lens} tokens, 32-token blocks, 32-block slabs")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+
+def dist_init(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def dist_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks (nvidia-smi sampled in the background during the timed region)
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            ident = str(device_index)
+        self.cmd = ["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "50"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.12)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return None
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------
+# measured peaks, ncu traffic record
+# ---------------------------------------------------------------------------
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured copy bandwidth (MEASURED_PEAKS.json)"
+    except Exception:
+        return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_split_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("decode") or f in ("pkv_internal.cuh", "plan.cu"):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source (else null)."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        e = rec.get(workload)
+        if e and e.get("kernel_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline (the oracle)
+# ---------------------------------------------------------------------------
+
+class OracleRun:
+    """The oracle on one layer of the workload (sequences 0..n-1), using every core of
+    this process's affinity."""
+
+    def __init__(self, w, max_seqs=None):
+        import oracle
+        self.cores = len(os.sched_getaffinity(0))
+        self.seqs = list(range(w.B if max_seqs is None else min(max_seqs, w.B)))
+        o = oracle.OraclePool(1, w.Hkv, w.D, w.fmt, seed=w.hadamard_seed)
+        o.reserve_rows(w.rows_used)
+        for b in self.seqs:
+            k, v = w.kv(0, b)
+            r, s = w.token_placement(b)
+            o.write_block(0, r, s, k, v)
+        self.o, self.w = o, w
+        self.q = w.q(0)[self.seqs]
+        self.bt = w.block_table()[self.seqs]
+        self.ctx = w.ctx()[self.seqs]
+        self.lens = [w.lens[b] for b in self.seqs]
+        self.nbytes = algorithmic_bytes(w.fmt, w.D, w.Hkv, w.Hq, self.lens)
+
+    def run(self) -> float:
+        t0 = time.perf_counter()
+        self.o.decode_attention(0, self.q, self.bt, self.ctx, self.w.scale, n_threads=self.cores)
+        return time.perf_counter() - t0
+
+    def sample_text(self, runs: int) -> str:
+        w = self.w
+        return (f"1 of {w.n_layers} layer(s), {len(self.seqs)} of {w.B} sequences ({sum(self.lens)} tokens), "
+                f"all {w.Hq} query heads; median of {runs} runs")
+
+
+def oracle_sample(w, budget_s: float = 10.0, max_seqs=None):
+    """Time the oracle until `budget_s` of CPU work (at least one run)."""
+    r = OracleRun(w, max_seqs)
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while True:
+        times.append(r.run())
+        if time.perf_counter() > t_end or len(times) >= 50:
+            break
+    t = statistics.median(times)
+    return {"value": r.nbytes / t / 1e9, "unit": "GB/s", "cores": r.cores, "kind": "oracle",
+            "sample": r.sample_text(len(times)), "seconds_per_sample": t, "kv_tokens_per_s": sum(r.lens) / t}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, rank, world, local):
+    import torch
+    import paged_kv_cache_split_gb300 as pkv
+
+    torch.cuda.set_device(local)
+    w = workload_for(args.workload)
+    dev = torch.device("cuda", local)
+    pool = pkv.Pool(w.n_layers, w.Hkv, w.D, pkv.FORMAT_NAMES[w.fmt], hadamard_seed=w.hadamard_seed,
+                    max_slabs=(w.rows_used + 31) // 32 + 8)
+    pool.reserve_rows(w.rows_used)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + w.seed * 100 + rank)
+    rows = np.concatenate([w.token_placement(b)[0] for b in range(w.B)])
+    slots = np.concatenate([w.token_placement(b)[1] for b in range(w.B)])
+    rows_d = torch.from_numpy(rows).to(dev)
+    slots_d = torch.from_numpy(slots).to(dev)
+    ntok = rows.size
+    for layer in range(w.n_layers):
+        k = torch.randn((ntok, w.Hkv, w.D), generator=gen, device=dev).to(torch.bfloat16)
+        v = torch.randn((ntok, w.Hkv, w.D), generator=gen, device=dev).to(torch.bfloat16)
+        pool.write_block(layer, rows_d, slots_d, k, v)
+        del k, v
+    q = torch.randn((w.n_layers, w.B, w.Hq, w.D), generator=gen, device=dev).to(torch.bfloat16)
+    bt = torch.from_numpy(w.block_table()).to(dev)
+    ctx = torch.from_numpy(w.ctx()).to(dev)
+    out = torch.empty_like(q)
+    ws = pool.workspace(w.B, w.Hq, dev)
+    max_ctx = max(w.lens)
+
+    def step():
+        for layer in range(w.n_layers):
+            pool.paged_decode_attention(layer, q[layer], bt, ctx, w.scale, max_ctx=max_ctx, out=out[layer],
+                                        workspace=ws)
+
+    # Eager pass: per-launch CUDA events on the launching stream.
+    stream = torch.cuda.current_stream()
+    step()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * w.n_layers)]
+    for layer in range(w.n_layers):
+        ev[2 * layer].record(stream)
+        pool.paged_decode_attention(layer, q[layer], bt, ctx, w.scale, max_ctx=max_ctx, out=out[layer], workspace=ws)
+        ev[2 * layer + 1].record(stream)
+    torch.cuda.synchronize()
+    eager_launch_us = statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3 for i in range(w.n_layers))
+    if pool.check_errors():
+        raise SystemExit("device error word set during setup")
+
+    # CUDA graph of one step (all layers) for the timed region.
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+    run = graph.replay if graph is not None else step
+
+    # End-to-end arm: pinned host inputs copied in and the result copied out every step.
+    q_h = q.cpu().pin_memory()
+    bt_h = bt.cpu().pin_memory()
+    ctx_h = ctx.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    q_e = torch.empty_like(q)
+    bt_e = torch.empty_like(bt)
+    ctx_e = torch.empty_like(ctx)
+    out_e = torch.empty_like(out)
+
+    def e2e_step():
+        q_e.copy_(q_h, non_blocking=True)
+        bt_e.copy_(bt_h, non_blocking=True)
+        ctx_e.copy_(ctx_h, non_blocking=True)
+        for layer in range(w.n_layers):
+            pool.paged_decode_attention(layer, q_e[layer], bt_e, ctx_e, w.scale, max_ctx=max_ctx, out=out_e[layer],
+                                        workspace=ws)
+        out_h.copy_(out_e, non_blocking=True)
+
+    sampler = ClockSampler(local)
+    with sampler:
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            run()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        ms_step = t0.elapsed_time(t1) / args.steps
+        # end-to-end, through the public API with host buffers
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        ms_e2e = e0.elapsed_time(e1) / args.steps
+    if pool.check_errors():
+        raise SystemExit("device error word set during the timed region")
+    if not torch.equal(out_e, out):
+        raise SystemExit("end-to-end result differs from the device-resident result")
+
+    ms_step = dist_max(ms_step, world)
+    ms_e2e = dist_max(ms_e2e, world)
+    bytes_layer = algorithmic_bytes(w.fmt, w.D, w.Hkv, w.Hq, w.lens)
+    bytes_step = bytes_layer * w.n_layers
+    tokens_step = sum(w.lens) * w.n_layers
+    value = bytes_step * world / (ms_step * 1e-3) / 1e9
+    launch_us = ms_step * 1e3 / w.n_layers
+    achieved = bytes_layer / (launch_us * 1e-6) / 1e9
+    peak, peak_src = measured_peak()
+    h2d = q.numel() * 2 + bt.numel() * 4 + ctx.numel() * 4
+    d2h = out.numel() * 2
+    res = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) bf16 K/V and q; no model weights)",
+        "config": {"workload": describe(w), "global_batch": w.B * world, "seq_len": max(w.lens),
+                   "layers": w.n_layers, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB read per step vs 129 MB L2)",
+                   "cuda_graph": graph is not None},
+        "kv_tokens_per_s": round(tokens_step * world / (ms_step * 1e-3), 1),
+        "pct_of_nominal_8tbs": round(100 * value / world / 8000.0, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
+                     "per_launch_bytes": bytes_layer, "avg_launch_us": round(launch_us, 3),
+                     "eager_launch_us": round(eager_launch_us, 3), "peak_source": peak_src,
+                     "kernel": "decode_kernel (split-K flash decoding, fused combine)"},
+        "e2e": {"value": round(bytes_step * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": w.n_layers * args.steps,
+        "clocks": sampler.summary(),
+    }
+    return res, w
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default="qwen3-0.6b")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_init(args.gpus)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = workload_for(args.workload)
+        import oracle
+        oracle.build()
+        cores = len(os.sched_getaffinity(0))
+        r = OracleRun(w, max_seqs=2)
+        times = []
+        for i in range(args.warmup + args.steps):
+            dt = r.run()
+            if i >= args.warmup:
+                times.append(dt)
+        t = statistics.median(times) if times else r.run()
+        lens = r.lens
+        nbytes = r.nbytes
+        v = nbytes / t / 1e9
+        cores = r.cores
+        base = {"sample": r.sample_text(len(times))}
+        res = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": 1,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+               "data": "synthetic (seeded N(0,1) bf16 K/V and q; no model weights)",
+               "config": {"workload": describe(w), "global_batch": w.B, "seq_len": max(w.lens),
+                          "layers": w.n_layers, "parallelism": "host cores"},
+               "kv_tokens_per_s": round(sum(lens) / t, 1),
+               "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": base["sample"]},
+               "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(res), flush=True)
+        return
+
+    res, w = run_gpu(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            cb = oracle_sample(w, budget_s=10.0, max_seqs=w.B)
+            res["cpu_baseline"] = {k: (round(v, 5) if isinstance(v, float) else v) for k, v in cb.items()}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,224 @@
+/*
+ * pkv.h — C ABI of the GB300 paged-KV decode-attention library (libpkv.so).
+ *
+ * A pool stores the K/V cache of every layer in chunked slab storage: for each
+ * layer and stored tensor, a vector of fixed-size slabs shaped
+ *   [slab_blocks, block_size, n_kv_heads, row]
+ * (row = head_dim bf16 values, or packed codes, or (scale, offset) pairs).  A
+ * physical row (one block of block_size tokens) maps to slab = row / slab_blocks,
+ * row_in_slab = row % slab_blocks.  Growth appends fresh zeroed slabs and never
+ * copies or frees an existing one.
+ *   [mlxcel issue #235, "chunked slab storage for the paged pool", Proposed
+ *    solution: bullets 1-3]
+ *
+ * Stored formats: native bf16, or packed K4/V4, K8/V4, K8/V8 with token-local
+ * affine groups of group_size values and an FP32 (scale, offset) pair per group;
+ * K (and Q at attention time) is expressed in a fixed signed Hadamard basis.
+ *   [mlx-swift-lm PR #142, "packed paged KV formats with bounded workspace
+ *    admission", Summary]
+ *
+ * Conventions for every call
+ *  - All pointers named *_dev are device pointers; *_host are host pointers.
+ *    Device buffers passed in are owned by the caller and must stay valid until
+ *    the work enqueued on `stream` has finished.
+ *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *    stream.  Every call that touches device memory is asynchronous on that
+ *    stream unless stated otherwise; none synchronises the device except
+ *    pkv_pool_check_errors and pkv_pool_destroy.
+ *  - Host-checkable errors (NULL pointers, sizes out of range, a layer index out
+ *    of range, workspace too small, allocation failure) are returned
+ *    synchronously, before any state changes or work is enqueued.
+ *  - Device-detected range errors (a block-table row beyond the pool's rows, a
+ *    context length beyond max_blocks*block_size, a slot beyond block_size) set
+ *    the pool's device error word; the offending block/token is skipped (the
+ *    result is then undefined but no memory outside the pool is touched).  Read
+ *    and clear it with pkv_pool_check_errors.
+ *  - A pool is not thread-safe; callers serialise calls on one pool.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pkv_pool pkv_pool; /* opaque; owns slabs, pointer tables, row allocator */
+
+typedef enum {
+  PKV_FMT_BF16 = 0, /* native: K and V rows are head_dim bf16 values            */
+  PKV_FMT_K4V4 = 1, /* K 4-bit codes (Hadamard basis), V 4-bit codes           */
+  PKV_FMT_K8V4 = 2, /* K 8-bit codes (Hadamard basis), V 4-bit codes           */
+  PKV_FMT_K8V8 = 3  /* K 8-bit codes (Hadamard basis), V 8-bit codes           */
+} pkv_format;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID = -1, /* bad argument (NULL, size, layer, alignment)          */
+  PKV_ERR_OOM = -2,     /* the allocator returned NULL; the pool is unchanged    */
+  PKV_ERR_CUDA = -3,    /* a CUDA runtime call failed (message: pkv_last_error)  */
+  PKV_ERR_FORMAT = -4,  /* storage identity does not match the request           */
+  PKV_ERR_RANGE = -5,   /* a host-visible index is out of range                  */
+  PKV_ERR_DEVICE = -6   /* the device error word was set (pkv_pool_check_errors) */
+} pkv_status;
+
+/* Tensor kinds stored per layer. */
+enum { PKV_KIND_K = 0, PKV_KIND_V = 1, PKV_KIND_KMETA = 2, PKV_KIND_VMETA = 3 };
+
+typedef struct {
+  int32_t n_layers;      /* >= 1                                                */
+  int32_t n_kv_heads;    /* 1..8 (one decode consumer warp per kv head)         */
+  int32_t head_dim;      /* 64, 128 or 256                                      */
+  int32_t block_size;    /* tokens per block; must be 32                        */
+  int32_t slab_blocks;   /* blocks per slab (POOL_SLAB_BLOCKS); 1..4096, 32 is the default */
+  int32_t group_size;    /* values per affine group; must be 32 (ignored for bf16) */
+  int32_t format;        /* pkv_format                                          */
+  int32_t max_slabs;     /* capacity of the slab pointer table (>= 1)           */
+  uint64_t hadamard_seed;/* signs s_i = -1 iff top bit of splitmix64(seed + i)  */
+} pkv_pool_config;
+
+/* Stream-ordered allocator used for slabs.  alloc returns NULL on failure.  With
+ * a NULL allocator the pool uses cudaMallocAsync / cudaFreeAsync on the stream. */
+typedef struct {
+  void* (*alloc)(void* ctx, size_t bytes, void* stream);
+  void (*release)(void* ctx, void* ptr, void* stream);
+  void* ctx;
+} pkv_allocator;
+
+typedef struct {
+  int32_t n_slabs;            /* slabs per (layer, tensor) currently held          */
+  int32_t n_kinds;            /* 2 (bf16) or 4 (packed: K, V, K meta, V meta)      */
+  int64_t slab_append_events; /* slabs appended since create (never a copy)        */
+  int64_t rows_capacity;      /* n_slabs * slab_blocks                             */
+  int64_t rows_in_use;        /* rows with a nonzero reference count               */
+  int64_t bytes_reserved;     /* sum over every slab of every layer and tensor     */
+  int64_t row_bytes[4];       /* bytes of one (token, head) row per tensor kind    */
+} pkv_stats;
+
+/* Create a pool with no slabs.  The allocator struct is copied.  Errors:
+ * PKV_ERR_INVALID for an unsupported configuration, PKV_ERR_CUDA if the device
+ * cannot be used.  Synchronous. */
+pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_allocator* alloc, void* stream,
+                           pkv_pool** out);
+
+/* Synchronise `stream` of the last call, release every slab and the pool. */
+void pkv_pool_destroy(pkv_pool* pool);
+
+/* Append n_slabs fresh zeroed slabs to every layer and tensor, in one step
+ * (presize_for_span).  Existing slabs are neither copied nor freed; their base
+ * addresses stay valid.  All-or-nothing: on PKV_ERR_OOM the pool is unchanged.
+ *   [mlxcel #235, Proposed solution, bullet 2] */
+pkv_status pkv_append_slab(pkv_pool* pool, int n_slabs, void* stream);
+
+/* Take n rows from the free list (LIFO reuse of released rows, then rows of
+ * appended slabs in ascending order), appending slabs when it is empty.  Each
+ * returned row has reference count 1.  rows_host: n int32.
+ *   [mlxcel #235, Behavioral invariants: block ids, refcounts, free-row reuse] */
+pkv_status pkv_alloc_rows(pkv_pool* pool, int n, int32_t* rows_host, void* stream);
+
+/* Reference counting of rows (host bookkeeping only).  retain requires a live
+ * row; release returns a row to the free list when its count reaches 0.
+ * PKV_ERR_RANGE for a row outside the pool or not live. */
+pkv_status pkv_retain_row(pkv_pool* pool, int32_t row);
+pkv_status pkv_release_row(pkv_pool* pool, int32_t row);
+
+/* Maximal same-slab runs of a block-table row list, in logical order: writes the
+ * starting index of each run to run_start_host (capacity n) and returns the number
+ * of runs (0 for n <= 0, -1 for bad arguments).  Host only; no pool needed.
+ *   [mlxcel #235, touch point 3, gather_visible] */
+int pkv_slab_runs(const int32_t* rows_host, int n, int slab_blocks, int32_t* run_start_host);
+
+/* write_block: token i of k/v goes to (rows_dev[i], slots_dev[i]) of `layer`.
+ * k_bf16_dev, v_bf16_dev: [n_tokens, n_kv_heads, head_dim] bf16, row-major.
+ * Packed formats quantise here, once: K is rotated into the Hadamard basis,
+ * then every group of group_size values gets scale = (max-min)/(2^bits-1),
+ * offset = min, code = round-half-even((x-min)/scale) (0 when scale is 0).
+ *   [mlxcel #235, touch point 1; mlx-swift-lm #142, After: "quantize fresh K/V
+ *    once"] */
+pkv_status pkv_write_block(pkv_pool* pool, int layer, int n_tokens, const int32_t* rows_dev,
+                           const int32_t* slots_dev, const void* k_bf16_dev, const void* v_bf16_dev,
+                           void* stream);
+
+/* copy_on_write_block: copy every byte of block src_rows_dev[i] to block
+ * dst_rows_dev[i], for every layer and stored tensor.  Pairs must not overlap.
+ *   [mlxcel #235, touch point 2] */
+pkv_status pkv_copy_on_write_block(pkv_pool* pool, int n, const int32_t* src_rows_dev,
+                                   const int32_t* dst_rows_dev, void* stream);
+
+/* gather_visible: the visible context of one sequence (tokens [0, ctx_len)) as
+ * dense arrays in logical order, equal to concatenating the maximal same-slab
+ * runs of its block-table row.  bt_row_dev: ceil(ctx_len/block_size) rows.
+ * Outputs (device): k_out, v_out [n_kv_heads, ctx_len, row_bytes(kind)];
+ * kmeta_out, vmeta_out [n_kv_heads, ctx_len, head_dim/group_size, 2] float32,
+ * which must be NULL for bf16 and non-NULL for packed (else PKV_ERR_FORMAT);
+ * with ctx_len 0 nothing is written and every output may be NULL.
+ *   [mlxcel #235, touch point 3] */
+pkv_status pkv_gather_visible(pkv_pool* pool, int layer, const int32_t* bt_row_dev, int ctx_len,
+                              void* k_out_dev, void* v_out_dev, void* kmeta_out_dev,
+                              void* vmeta_out_dev, void* stream);
+
+/* Workspace bytes needed by pkv_paged_decode_attention for batches of up to B
+ * sequences with Hq query heads (max_ctx is the caller's bound on any context
+ * length; it is accepted for interface stability and does not change the size).
+ * The workspace holds the split-K partials and per-sequence arrival counters; it
+ * must be zero-filled once before its first use (the kernel leaves it reusable). */
+pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int Hq, int max_ctx,
+                                      size_t* bytes);
+
+/* Batched single-token decode attention with GQA (query head h reads KV head
+ * h / (Hq / n_kv_heads)), no mask, over tokens [0, ctx_lens[b]) of each
+ * sequence:  out[b,h] = softmax(scale * q[b,h] . K_b^T) V_b.
+ * For packed formats q is rotated into K's Hadamard basis inside the kernel and
+ * K/V are dequantised in registers (no dequantised history is materialised).
+ *   q_bf16_dev:      [B, Hq, head_dim] bf16 (un-rotated)
+ *   block_table_dev: [B, max_blocks] int32 rows
+ *   ctx_lens_dev:    [B] int32; 0 gives a zero output row
+ *   max_ctx:         host bound on ctx_lens (used only to size the launch)
+ *   out_bf16_dev:    [B, Hq, head_dim] bf16
+ *   workspace_dev:   ws_bytes >= pkv_decode_workspace_bytes(B, Hq), zeroed once
+ * Deterministic: bitwise identical results for identical inputs on one device.
+ *   [mlxcel issue #2171, "one KV storage abstraction": Proposed Solution
+ *    (KVCache::attend -> paged_batch_decode_attention) and Edge cases (single
+ *    token, no mask); mlx-swift-lm #142: "direct attention consumes packed pages
+ *    without expanding the history"] */
+pkv_status pkv_paged_decode_attention(pkv_pool* pool, int layer, int B, int Hq,
+                                      const void* q_bf16_dev, const int32_t* block_table_dev,
+                                      int max_blocks, const int32_t* ctx_lens_dev, int max_ctx,
+                                      float scale, void* out_bf16_dev, void* workspace_dev,
+                                      size_t ws_bytes, void* stream);
+
+/* Number of CTAs a decode launch uses (0 = one per SM, the default).  Changing it
+ * changes the split-K partition (results agree to rounding) and the workspace
+ * size.  PKV_ERR_INVALID for n < 0. */
+pkv_status pkv_decode_set_ctas(pkv_pool* pool, int n_ctas);
+
+/* Pool statistics (host bookkeeping; no device access). */
+pkv_status pkv_pool_stats(const pkv_pool* pool, pkv_stats* out);
+
+/* Device base address of slab `slab` of (layer, kind); PKV_ERR_RANGE if absent. */
+pkv_status pkv_slab_address(const pkv_pool* pool, int layer, int kind, int slab, void** addr);
+
+/* Storage identity check: PKV_OK if cfg describes the same stored layout as the
+ * pool (format, head_dim, n_kv_heads, block_size, slab_blocks, group_size and,
+ * for packed formats, hadamard_seed), else PKV_ERR_FORMAT.  Used to reject an
+ * incompatible storage identity before any allocation or copy.
+ *   [mlx-swift-lm #142, Summary: reject incompatible storage identities] */
+pkv_status pkv_pool_check_identity(const pkv_pool* pool, const pkv_pool_config* cfg);
+
+/* Synchronise `stream`, read and clear the device error word.  PKV_ERR_DEVICE if it
+ * was set (bits: 1 row out of range, 2 context too long, 4 slot out of range,
+ * 8 wait limit reached); *word_out (optional) receives the bits. */
+pkv_status pkv_pool_check_errors(pkv_pool* pool, void* stream, int32_t* word_out);
+
+/* Static description of a status code, and the last CUDA error message seen by
+ * this thread (empty if none). */
+const char* pkv_status_string(pkv_status status);
+const char* pkv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

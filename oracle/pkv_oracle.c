@@ -84,11 +84,7 @@ void oracle_hadamard_signs(uint64_t seed, int D, double* s) {
   for (int i = 0; i < D; ++i) s[i] = (oracle_splitmix64(seed + (uint64_t)i) >> 63) ? -1.0 : 1.0;
 }
 
-static int popcount32(uint32_t v) {
-  int c = 0;
-  while (v) { c += (int)(v & 1u); v >>= 1; }
-  return c;
-}
+static int popcount32(uint32_t v) { return __builtin_popcount(v); }
 
 /* Entry (i, j) of the orthonormal Sylvester Hadamard matrix of order D. */
 double oracle_hadamard_entry(int i, int j, int D) {
@@ -114,6 +110,31 @@ static int exponent_of(double x) {
  * Returns 1 when the FP64 sum is exact for every i (every nonzero input is a
  * multiple of 2^(Emin-7) and |sum| < D*2^(Emax+1), so the sum is exact when
  * Emax - Emin <= 45 - log2(D)); 0 otherwise (the result is still produced). */
+/* The same rotation with the +-1 entries of sqrt(D) * H_D taken from a table
+ * (hs[i * D + j] = (-1)^popcount(i&j)); used by the pool image for speed. */
+static int rotate_k_table(const uint16_t* k_bf16, int D, const double* signs, const double* hs, float* out) {
+  int emin = 100000, emax = -100000;
+  double x[512];
+  for (int j = 0; j < D; ++j) {
+    double v = bf16_to_double(k_bf16[j]);
+    x[j] = signs[j] * v;
+    if (v != 0.0) {
+      int e = exponent_of(v);
+      if (e < emin) emin = e;
+      if (e > emax) emax = e;
+    }
+  }
+  int exact = (emax < emin) || (emax - emin <= 45 - ilog2(D));
+  const double inv = 1.0 / sqrt((double)D);
+  for (int i = 0; i < D; ++i) {
+    double acc = 0.0;
+    for (int j = 0; j < D; ++j) acc += hs[(size_t)i * D + j] * x[j];
+    double prod = acc * inv;
+    out[i] = (float)prod;
+  }
+  return exact;
+}
+
 int oracle_rotate_k(const uint16_t* k_bf16, int D, const double* signs, float* out) {
   int emin = 100000, emax = -100000;
   for (int j = 0; j < D; ++j) {
@@ -220,6 +241,7 @@ typedef struct oracle_pool {
   int n_kinds;        /* 2 (K, V) or 4 (K, V, K meta, V meta) */
   size_t row_bytes[4];
   double* signs;
+  double* hs; /* [D * D] entries of sqrt(D) * H_D */
   int n_slabs, cap_slabs;
   uint8_t** slab; /* slab[(s * n_layers + layer) * n_kinds + kind] */
   long inexact_rotations;
@@ -264,6 +286,11 @@ oracle_pool* oracle_pool_new(int n_layers, int n_kv_heads, int head_dim, int for
   p->signs = (double*)malloc(sizeof(double) * (size_t)head_dim);
   if (!p->signs) { free(p); return NULL; }
   oracle_hadamard_signs(seed, head_dim, p->signs);
+  p->hs = (double*)malloc(sizeof(double) * (size_t)head_dim * (size_t)head_dim);
+  if (!p->hs) { free(p->signs); free(p); return NULL; }
+  for (int i = 0; i < head_dim; ++i)
+    for (int j = 0; j < head_dim; ++j)
+      p->hs[(size_t)i * head_dim + j] = (popcount32((uint32_t)(i & j)) & 1) ? -1.0 : 1.0;
   return p;
 }
 
@@ -272,6 +299,7 @@ void oracle_pool_free(oracle_pool* p) {
   for (long i = 0; i < (long)p->n_slabs * p->n_layers * p->n_kinds; ++i) free(p->slab[i]);
   free(p->slab);
   free(p->signs);
+  free(p->hs);
   free(p);
 }
 
@@ -325,11 +353,17 @@ int oracle_write_block(oracle_pool* p, int layer, int n, const int32_t* rows, co
                        const uint16_t* k, const uint16_t* v) {
   if (layer < 0 || layer >= p->n_layers || n < 0) return OR_ERR_ARG;
   const int D = p->head_dim, H = p->n_kv_heads;
-  float* xr = (float*)malloc(sizeof(float) * (size_t)D);
-  if (!xr) return OR_ERR_MEM;
   int rc = OR_OK;
+  long inexact = 0;
+  /* Tokens are independent; rows written by two tokens of one call must differ. */
+#pragma omp parallel for schedule(static) reduction(+ : inexact)
   for (int i = 0; i < n; ++i) {
-    if (!row_ok(p, rows[i]) || slots[i] < 0 || slots[i] >= p->block_size) { rc = OR_ERR_RANGE; continue; }
+    float xr[512];
+    if (!row_ok(p, rows[i]) || slots[i] < 0 || slots[i] >= p->block_size) {
+#pragma omp atomic write
+      rc = OR_ERR_RANGE;
+      continue;
+    }
     for (int h = 0; h < H; ++h) {
       const uint16_t* kr = k + ((size_t)i * H + h) * D;
       const uint16_t* vr = v + ((size_t)i * H + h) * D;
@@ -338,7 +372,7 @@ int oracle_write_block(oracle_pool* p, int layer, int n, const int32_t* rows, co
         memcpy(addr(p, layer, 1, rows[i], slots[i], h), vr, p->row_bytes[1]);
         continue;
       }
-      if (!oracle_rotate_k(kr, D, p->signs, xr)) p->inexact_rotations++;
+      if (!rotate_k_table(kr, D, p->signs, p->hs, xr)) inexact++;
       oracle_quantize(xr, D, p->k_bits, p->group_size, addr(p, layer, 0, rows[i], slots[i], h),
                       (float*)addr(p, layer, 2, rows[i], slots[i], h));
       for (int d = 0; d < D; ++d) xr[d] = bf16_to_float(vr[d]);
@@ -346,7 +380,7 @@ int oracle_write_block(oracle_pool* p, int layer, int n, const int32_t* rows, co
                       (float*)addr(p, layer, 3, rows[i], slots[i], h));
     }
   }
-  free(xr);
+  p->inexact_rotations += inexact;
   return rc;
 }
 

@@ -1,0 +1,39 @@
+// plan.cu — shared-memory plan of the decode kernel (host side).
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+// The kernel keeps NS stages of T tokens x all kv heads in shared memory.  Pick
+// the largest T in {32, 16, 8} that still allows at least 4 stages (at most 8),
+// leaving room for the barriers, the per-sequence unit prefix and, for packed
+// formats, the per-warp q scratch used by the Hadamard rotation.
+bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
+  const FormatBits fb = format_bits(fmt);
+  if (fb.k == 0 || hkv < 1 || hkv > 8 || B < 1 || B > 4096) return false;
+  const bool packed = fmt != PKV_FMT_BF16;
+  const size_t meta = packed ? (size_t)(D / kGroup) * 8 : 0;
+  const size_t per_token = (size_t)hkv * ((size_t)(fb.k + fb.v) * D / 8 + 2 * meta);
+  const size_t budget = 232448;  // 227 KB opt-in shared memory per block on sm_100-class parts
+  size_t fixed = (size_t)(2 * B + 1 + 4) * 4 + 16 + 128;
+  if (packed) fixed += (size_t)hkv * G * D * 4;
+  if (fixed >= budget) return false;
+  const int cand[3] = {32, 16, 8};
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int T : cand) {
+      const size_t stage = (size_t)T * per_token;
+      size_t ns = (budget - fixed) / (stage + 16);
+      if (ns > 8) ns = 8;
+      if ((pass == 0 && ns >= 4) || (pass == 1 && ns >= 2)) {
+        plan->tokens_per_stage = T;
+        plan->n_stages = (int)ns;
+        plan->stage_bytes = stage;
+        plan->smem_bytes = ns * stage + ns * 16 + fixed;
+        plan->threads = (hkv + 1) * 32;
+        return true;
+      }
+    }
+  }
+  return false;
+}
+
+}  // namespace pkv

@@ -407,3 +407,25 @@ def test_gqa_mapping_uses_floor_division():
     p.write_block(0, rows[t // 32], (t % 32).astype(np.int32), k, v)
     out = p.decode_attention(0, wl.bf16_normal(rng, (1, H * G, D)), rows[None], [40], 0.125)
     assert np.allclose(out[0, :, 0], np.arange(H * G) // G)
+
+
+@pytest.mark.parametrize("fmt,kb,vb", [(FMT_K4V4, 4, 4), (FMT_K8V4, 8, 4), (FMT_K8V8, 8, 8)])
+def test_pool_write_equals_rotate_then_quantize(fmt, kb, vb):
+    """The pool image's packed write path equals the pinned primitives composed."""
+    H, D = 2, 128
+    p = OraclePool(1, H, D, fmt, seed=0x5EED)
+    p.reserve_rows(32)
+    rng = wl.rng_for(61)
+    k, v = wl.bf16_normal(rng, (5, H, D), 0.01), wl.bf16_normal(rng, (5, H, D), 0.01)
+    p.write_block(0, np.full(5, 3, np.int32), np.arange(5, dtype=np.int32), k, v)
+    kc, vc, km, vm = p.gather_visible(0, np.array([3], np.int32), 5)
+    s = oracle.hadamard_signs(0x5EED, D)
+    for t in range(5):
+        for h in range(H):
+            rk, exact = oracle.rotate_k(k[t, h], s)
+            assert exact
+            c, m = oracle.quantize(rk, kb)
+            assert np.array_equal(kc[h, t], c) and np.array_equal(km[h, t].view(np.float32), m.reshape(-1))
+            c, m = oracle.quantize(wl.bf16_bits_to_f32(v[t, h]), vb)
+            assert np.array_equal(vc[h, t], c) and np.array_equal(vm[h, t].view(np.float32), m.reshape(-1))
+    assert p.inexact_rotations == 0
