@@ -189,6 +189,33 @@ pkv_status pkv_paged_decode_attention(pkv_pool* pool, int layer, int B, int Hq,
                                       float scale, void* out_bf16_dev, void* workspace_dev,
                                       size_t ws_bytes, void* stream);
 
+/* Size of the fixed device scratch array used by pkv_paged_decode_attention_noalloc. */
+#define PKV_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/* Decode attention without any device allocation by the caller or the library.
+ * The source pages have no counterpart to this call.  It exists for callers that
+ * cannot call cudaMalloc or borrow an allocator: for example a serving loop that
+ * reserved all of its device memory at start-up and may not allocate during a
+ * decode step, or a plugin whose host framework owns the device allocator.
+ * Arguments and results are those of pkv_paged_decode_attention, minus the
+ * workspace: the split-K partials and arrival counters live instead in a fixed
+ * array of PKV_STATIC_SCRATCH_BYTES (8 MiB) compiled into the library, which every
+ * GPU that loads the library holds until the process exits.
+ *  - The first call on each device looks up that device's copy of the array
+ *    (cudaGetSymbolAddress, with the device current); make that first call before
+ *    any stream capture.
+ *  - Each call clears the arrival counters on `stream` (a cudaMemsetAsync, not an
+ *    allocation), then launches the same kernel as pkv_paged_decode_attention.
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents: calls whose GPU work overlaps (different streams, or different
+ *    pools) race on it and give undefined results; serialise them.
+ *  - PKV_ERR_RANGE, with a message from pkv_last_error, when (B, Hq, head_dim)
+ *    need more scratch than the array holds (pkv_decode_workspace_bytes tells). */
+pkv_status pkv_paged_decode_attention_noalloc(pkv_pool* pool, int layer, int B, int Hq,
+                                              const void* q_bf16_dev, const int32_t* block_table_dev,
+                                              int max_blocks, const int32_t* ctx_lens_dev, int max_ctx,
+                                              float scale, void* out_bf16_dev, void* stream);
+
 /* Number of CTAs a decode launch uses (0 = one per SM, the default).  Changing it
  * changes the split-K partition (results agree to rounding) and the workspace
  * size.  PKV_ERR_INVALID for n < 0. */

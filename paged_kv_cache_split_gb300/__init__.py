@@ -80,6 +80,7 @@ SIGNATURES = {
     "pkv_gather_visible": ([_P, _I, _P, _I, _P, _P, _P, _P, _P], _I),
     "pkv_decode_workspace_bytes": ([_P, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
     "pkv_paged_decode_attention": ([_P, _I, _I, _I, _P, _P, _I, _P, _I, _F, _P, _P, _SZ, _P], _I),
+    "pkv_paged_decode_attention_noalloc": ([_P, _I, _I, _I, _P, _P, _I, _P, _I, _F, _P, _P], _I),
     "pkv_decode_set_ctas": ([_P, _I], _I),
     "pkv_pool_stats": ([_P, ctypes.POINTER(Stats)], _I),
     "pkv_slab_address": ([_P, _I, _I, _I, ctypes.POINTER(_P)], _I),
@@ -286,6 +287,20 @@ class Pool:
             int(block_table.shape[1]), _dev(ctx_lens, torch.int32, "ctx_lens", (B,)), int(max_ctx), float(scale),
             _dev(out, torch.bfloat16, "out", (B, Hq, D)), workspace.data_ptr(), int(workspace.numel()),
             _stream(stream)), "paged_decode_attention")
+        return out
+
+    def paged_decode_attention_noalloc(self, layer: int, q, block_table, ctx_lens, scale: float,
+                                       max_ctx: int = 0, out=None, stream=None):
+        """Decode attention with no workspace argument: the library's fixed device
+        scratch array is used instead (see pkv_paged_decode_attention_noalloc)."""
+        torch = _torch()
+        B, Hq, D = q.shape
+        if out is None:
+            out = torch.empty_like(q)
+        _check(self._lib.pkv_paged_decode_attention_noalloc(
+            self._h, layer, B, Hq, _dev(q, torch.bfloat16, "q"), _dev(block_table, torch.int32, "block_table"),
+            int(block_table.shape[1]), _dev(ctx_lens, torch.int32, "ctx_lens", (B,)), int(max_ctx), float(scale),
+            _dev(out, torch.bfloat16, "out", (B, Hq, D)), _stream(stream)), "paged_decode_attention_noalloc")
         return out
 
     # -- introspection -------------------------------------------------------

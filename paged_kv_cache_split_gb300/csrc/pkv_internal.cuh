@@ -181,4 +181,7 @@ cudaError_t launch_copy_blocks(const uint8_t* const* table, int n_layers, int n_
 cudaError_t launch_gather(const LayerView& lv, const int32_t* bt_row, int ctx, uint8_t* const* outs,
                           cudaStream_t s);
 
+// Message returned by pkv_last_error() on this thread.
+void set_last_error(const char* msg);
+
 }  // namespace pkv

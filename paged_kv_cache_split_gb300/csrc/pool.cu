@@ -52,6 +52,10 @@ struct pkv_pool {
 
 static thread_local std::string g_last_error;
 
+namespace pkv {
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+}  // namespace pkv
+
 static pkv_status cuda_fail(cudaError_t e, const char* where) {
   g_last_error = std::string(where) + ": " + cudaGetErrorString(e);
   return PKV_ERR_CUDA;
