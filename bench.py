@@ -268,6 +268,8 @@ def run_gpu(args, rank, world, local):
 
     torch.cuda.set_device(local)
     w = workload_for(args.workload)
+    if args.layers:
+        w = wl.scaled(w, w.name, n_layers=args.layers)
     dev = torch.device("cuda", local)
     pool = pkv.Pool(w.n_layers, w.Hkv, w.D, pkv.FORMAT_NAMES[w.fmt], hadamard_seed=w.hadamard_seed,
                     max_slabs=(w.rows_used + 31) // 32 + 8)
@@ -431,6 +433,8 @@ def main():
     ap.add_argument("--workload", default="qwen3-0.6b")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling aid: override the workload's layer count (not for reported numbers)")
     args = ap.parse_args()
     rank, world, local = dist_init(args.gpus)
 

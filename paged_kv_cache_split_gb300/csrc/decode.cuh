@@ -32,7 +32,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include "pkv_internal.cuh"
+#include "decode_common.cuh"
 
 namespace pkv {
 
@@ -61,26 +61,6 @@ struct DecodeTraits {
   static_assert(KP * KEPP == DPL && VP * VEPP == DPL, "piece geometry");
   static_assert(!PACKED || (KEPP <= kGroup && VEPP <= kGroup), "a piece stays inside one group");
 };
-
-struct DecodeParams {
-  LayerView lv;
-  int B, Hq, max_blocks;
-  const uint16_t* q;
-  const int32_t* bt;
-  const int32_t* ctx;
-  float scale_log2;
-  float inv_sqrt_d;
-  const float* signs;
-  uint16_t* out;
-  int32_t* counters;
-  float* partials;
-  int T;            // tokens per unit / stage
-  int NS;           // stages in the ring
-  int stage_bytes;  // T * Hkv * (KB + VB + 2 MB)
-};
-
-constexpr int kMaxConsumerWarps = 8;
-constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
 
 // ---- conversions of one loaded piece (w[] = LU/4 words) to floats ------------
 template <int BITS, int LU>
@@ -121,22 +101,6 @@ __device__ __forceinline__ void load_piece(const uint8_t* p, uint32_t (&w)[LU / 
   }
 }
 
-__device__ __forceinline__ uint16_t f2bf(float x) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
-}
-
-// Unit u -> sequence: the largest b with UP[b] <= u and UP[b+1] > u.
-__device__ __forceinline__ int find_seq(const int32_t* UP, int B, int32_t u) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (UP[mid] <= u) lo = mid; else hi = mid - 1;
-  }
-  // skip empty sequences sharing the same start
-  while (lo + 1 <= B - 1 && UP[lo + 1] <= u) ++lo;
-  return lo;
-}
-
 template <int FMT, int D, int G>
 __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodeParams P) {
   using Tr = DecodeTraits<FMT, D, G>;
@@ -155,49 +119,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
   int32_t* flag = LS + B;                                 // [4]
   float* qscr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(flag + 4) + 15) & ~uintptr_t(15));
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NC);
-    }
-    fence_mbar_init();
-  }
-  // Unit prefix over sequences (warp 0): unit = T tokens of one sequence.
-  if (warp == 0) {
-    const int lim = P.max_blocks * kBlockTokens;
-    int32_t carry = 0;
-    for (int base = 0; base < B; base += 32) {
-      const int b = base + lane;
-      int32_t n = 0;
-      if (b < B) {
-        int32_t L = P.ctx[b];
-        if (L < 0 || L > lim) {
-          atomicOr(err, ERR_CTX);
-          L = L < 0 ? 0 : lim;
-        }
-        LS[b] = L;
-        n = (L + T - 1) / T;
-      }
-      int32_t inc = n;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += y;
-      }
-      if (b < B) UP[b] = carry + inc - n;
-      carry += __shfl_sync(0xffffffffu, inc, 31);
-    }
-    if (lane == 0) UP[B] = carry;
-  }
+  decode_prologue(P, full, empty, NC, UP, LS);
   __syncthreads();
 
   const int32_t U = UP[B];
   const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
-  // Empty sequences: their (zero) rows are written by CTA b % grid.
-  for (int b = blockIdx.x; b < B; b += gridDim.x) {
-    if (LS[b] != 0) continue;
-    for (int i = threadIdx.x; i < P.Hq * D; i += blockDim.x) P.out[(size_t)b * P.Hq * D + i] = 0;
-  }
+  zero_empty_sequences<D>(P, LS);
   if (C == 0) return;
   const int32_t u0 = (int32_t)blockIdx.x * C;
   const int32_t u1 = min(U, u0 + C);
@@ -502,40 +429,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
             }
           }
         }
-        __threadfence();
-        named_barrier_sync(1, NC * 32);
-        if (warp == 0 && lane == 0) {
-          const int32_t ticket = atomicAdd(&P.counters[b], 1);
-          const bool last = ticket == (c_hi - c_lo);
-          if (last) P.counters[b] = 0;  // leave the workspace ready for the next launch
-          flag[0] = last ? 1 : 0;
-        }
-        named_barrier_sync(1, NC * 32);
-        if (flag[0]) {
-          __threadfence();
-          // Merge the partials of every CTA that held part of sequence b, in CTA order.
-#pragma unroll 1
-          for (int g = 0; g < G; ++g) {
-            const size_t head = (size_t)h * G + g;
-            float M = -INFINITY;
-            for (int32_t c = c_lo; c <= c_hi; ++c)
-              M = fmaxf(M, __ldcg(P.partials + (((size_t)c + b) * P.Hq + head) * (D + 2)));
-            float den = 0.f;
-            for (int32_t c = c_lo; c <= c_hi; ++c) {
-              const float* pp = P.partials + (((size_t)c + b) * P.Hq + head) * (D + 2);
-              den += exp2f(__ldcg(pp) - M) * __ldcg(pp + 1);
-            }
-            const float inv = 1.0f / den;
-            for (int d = lane; d < D; d += 32) {
-              float num = 0.f;
-              for (int32_t c = c_lo; c <= c_hi; ++c) {
-                const float* pp = P.partials + (((size_t)c + b) * P.Hq + head) * (D + 2);
-                num += exp2f(__ldcg(pp) - M) * __ldcg(pp + 2 + d);
-              }
-              P.out[((size_t)b * P.Hq + head) * D + d] = f2bf(num * inv);
-            }
-          }
-        }
+        finish_split_sequence<D, G>(P, b, c_lo, c_hi, NC, h, flag);
       }
     }
   }

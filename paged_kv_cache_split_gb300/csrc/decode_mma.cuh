@@ -1,0 +1,339 @@
+// decode_mma.cuh — native-bf16 paged decode attention on tensor-core tiles.
+//
+// Same contract and work partition as decode.cuh (units of T tokens x all kv heads
+// split evenly over one CTA per SM, producer warp + one consumer warp per kv head,
+// split-K partials merged by the last CTA of a sequence), with two changes that
+// cut the consumer's issue slots by several times for bf16 K/V:
+//
+//  * Staging: the producer copies each token's row (all kv heads, contiguous in
+//    the slab) with its own 1-D bulk copy into a padded shared-memory row whose
+//    stride is 16 bytes more than the payload.  Eight consecutive tokens then sit
+//    in eight different 16-byte bank groups, so ldmatrix reads of 8 tokens x 16
+//    bytes are conflict-free.
+//  * Math on mma.sync.m16n8k16 (bf16 in, fp32 accumulate):
+//      S  = Q K^T  with M = the G query heads of the kv head (padded to 16),
+//                  N = 8 tokens, K = 16 dims; Q is an A fragment held in registers
+//                  for the whole sequence, K comes from ldmatrix;
+//      O^T = V^T P^T with M = 16 output dims, N = the query heads, K = 16 tokens;
+//                  V^T comes from ldmatrix.trans, and P^T's B fragment is exactly
+//                  the accumulator fragment of S for those 16 tokens, so the
+//                  probabilities never leave registers.
+//    Logits are scaled by scale*log2(e) in fp32 after the QK product; the online
+//    softmax runs in base 2 on the accumulator fragments; P is rounded to bf16 for
+//    the PV product while the denominator sums the fp32 probabilities.
+#pragma once
+
+#include "decode_common.cuh"
+
+namespace pkv {
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D += A B for one m16n8k16 bf16 tile (A row-major 16x16, B col-major 16x8).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const DecodeParams P) {
+  static_assert(G >= 1 && G <= 8 && D % 16 == 0, "geometry");
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int hkv = P.lv.hkv;
+  const int NC = hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = P.T, NS = P.NS, B = P.B;
+  int32_t* err = P.lv.err;
+  const int ROW = hkv * D * 2;  // one token, all kv heads, in the slab
+  const int PROW = ROW + 16;    // padded shared-memory row
+
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * P.stage_bytes);
+  uint64_t* empty = full + NS;
+  int32_t* UP = reinterpret_cast<int32_t*>(empty + NS);
+  int32_t* LS = UP + (B + 1);
+  int32_t* flag = LS + B;
+
+  decode_prologue(P, full, empty, NC, UP, LS);
+  __syncthreads();
+  const int32_t U = UP[B];
+  const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
+  zero_empty_sequences<D>(P, LS);
+  if (C == 0) return;
+  const int32_t u0 = (int32_t)blockIdx.x * C;
+  const int32_t u1 = min(U, u0 + C);
+  if (u0 >= u1) return;
+  const int offV = T * PROW;
+
+  if (warp == NC) {
+    // ----------------------------- producer ---------------------------------
+    int issued = 0;
+    bool dead = false;
+    for (int32_t ub = u0; ub < u1 && !dead; ub += 32) {
+      const int32_t u = ub + lane;
+      const uint8_t* kbase = nullptr;
+      const uint8_t* vbase = nullptr;
+      int ok = 0;
+      if (u < u1) {
+        const int b = find_seq(UP, B, u);
+        const int32_t tok0 = (u - UP[b]) * T;
+        const int j = tok0 / kBlockTokens, slot0 = tok0 % kBlockTokens;
+        const int32_t row = P.bt[(size_t)b * P.max_blocks + j];
+        if (row >= 0 && (int64_t)row < P.lv.rows_capacity) {
+          const int32_t slab = row / P.lv.slab_blocks;
+          const int32_t r = row - slab * P.lv.slab_blocks;
+          const uint8_t* const* ent = P.lv.tab.base + (size_t)slab * P.lv.tab.stride;
+          const size_t first = (size_t)(r * kBlockTokens + slot0) * ROW;
+          kbase = ent[0] + first;
+          vbase = ent[1] + first;
+          ok = 1;
+        } else {
+          atomicOr(err, ERR_ROW);
+        }
+      }
+      const int cnt = min(32, u1 - ub);
+      for (int i = 0; i < cnt; ++i) {
+        const uint8_t* kb = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)kbase, i);
+        const uint8_t* vb = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)vbase, i);
+        const int oki = __shfl_sync(0xffffffffu, ok, i);
+        const int s = issued % NS;
+        if (lane == 0) {
+          if (issued >= NS && !mbar_wait_bounded(&empty[s], ((issued / NS) & 1) ^ 1, err)) dead = true;
+          // A whole unit is always copied (T tokens stay inside the block); tokens
+          // past the context are masked by a zero probability.
+          if (!dead) mbar_arrive_expect_tx(&full[s], oki ? (uint32_t)(2 * T * ROW) : 0u);
+        }
+        dead = __shfl_sync(0xffffffffu, dead, 0);
+        if (dead) break;
+        __syncwarp();
+        if (oki) {
+          uint8_t* st = stages + (size_t)s * P.stage_bytes;
+          for (int c = lane; c < 2 * T; c += 32) {
+            const int kind = c / T, tok = c - kind * T;
+            bulk_g2s(st + kind * offV + tok * PROW, (kind ? vb : kb) + (size_t)tok * ROW, (uint32_t)ROW, &full[s]);
+          }
+        }
+        ++issued;
+      }
+    }
+    if (lane == 0) {
+      const int first = issued > NS ? issued - NS : 0;
+      for (int n = first; n < issued; ++n) mbar_wait_bounded(&full[n % NS], (n / NS) & 1, err);
+    }
+    return;
+  }
+
+  // ------------------------------ consumers ---------------------------------
+  const int h = warp;
+  const int g = lane >> 2, t = lane & 3;
+  // ldmatrix row owned by this lane: matrix mi = lane/8, row ri = lane%8 covers
+  // token 8*(mi/2)+ri and dims 8*(mi%2) .. +7 of the current 16-token x 16-dim tile.
+  const int ld_tok = 8 * ((lane >> 3) >> 1) + (lane & 7);
+  const int ld_dim = 8 * ((lane >> 3) & 1);
+  uint32_t qa[D / 16][2];
+  float o[D / 16][4];
+  float m_run = -INFINITY, l_run = 0.f;
+  bool dead = false;
+  const uint32_t smem_base = smem_u32(stages);
+
+  int b = find_seq(UP, B, u0);
+  int n = 0;
+  for (int32_t u = u0; u < u1; ++u, ++n) {
+    while (u >= UP[b + 1]) ++b;
+    const bool seg_start = (u == u0) || (u == UP[b]);
+    const bool seg_end = (u == u1 - 1) || (u == UP[b + 1] - 1);
+    if (seg_start) {
+      // A fragments of Q (rows = query heads of kv head h; rows >= G are zero).
+      const uint32_t* qrow =
+          reinterpret_cast<const uint32_t*>(P.q + ((size_t)b * P.Hq + (size_t)h * G + (g < G ? g : 0)) * D);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        qa[kk][0] = g < G ? qrow[(16 * kk + 2 * t) / 2] : 0u;
+        qa[kk][1] = g < G ? qrow[(16 * kk + 2 * t + 8) / 2] : 0u;
+      }
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+
+    const int32_t tok0 = (u - UP[b]) * T;
+    const int nv = min(T, LS[b] - tok0);
+    const int s = n % NS;
+    if (!dead && !mbar_wait_bounded(&full[s], (n / NS) & 1, err)) dead = true;
+    dead = __shfl_sync(0xffffffffu, dead, 0);
+    if (!dead) {
+      const uint32_t kst = smem_base + (uint32_t)(s * P.stage_bytes);
+      const uint32_t vst = kst + (uint32_t)offV;
+      for (int kc = 0; kc * 16 < nv; ++kc) {
+        // ---- S = Q K^T for 16 tokens (two n-tiles of 8) ----
+        float sacc[2][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sacc[0][i] = sacc[1][i] = 0.f;
+        const uint32_t kaddr = kst + (uint32_t)((kc * 16 + ld_tok) * PROW + h * D * 2 + ld_dim * 2);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(kaddr + kk * 32, r0, r1, r2, r3);
+          mma_bf16_16816(sacc[0], qa[kk][0], 0u, qa[kk][1], 0u, r0, r1);
+          mma_bf16_16816(sacc[1], qa[kk][0], 0u, qa[kk][1], 0u, r2, r3);
+        }
+        // ---- online softmax for head g (row g), tokens 2t, 2t+1, 8+2t, 9+2t ----
+        const int tb = kc * 16 + 2 * t;
+        float x0 = tb < nv ? sacc[0][0] * P.scale_log2 : -INFINITY;
+        float x1 = tb + 1 < nv ? sacc[0][1] * P.scale_log2 : -INFINITY;
+        float x2 = tb + 8 < nv ? sacc[1][0] * P.scale_log2 : -INFINITY;
+        float x3 = tb + 9 < nv ? sacc[1][1] * P.scale_log2 : -INFINITY;
+        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const bool grow = mx > m_run;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float alpha = grow ? exp2f(m_run - mx) : 1.0f;
+          if (grow) m_run = mx;
+          l_run *= alpha;
+          // O^T columns of this lane are heads 2t and 2t+1, whose statistics live in
+          // lanes 8t and 8t+4.
+          const float ae = __shfl_sync(0xffffffffu, alpha, 8 * t);
+          const float ao = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            o[mt][0] *= ae;
+            o[mt][2] *= ae;
+            o[mt][1] *= ao;
+            o[mt][3] *= ao;
+          }
+        }
+        const float p0 = exp2f(x0 - m_run), p1 = exp2f(x1 - m_run);
+        const float p2 = exp2f(x2 - m_run), p3 = exp2f(x3 - m_run);
+        l_run += (p0 + p1) + (p2 + p3);
+        const uint32_t pb0 = pack_bf16x2(p0, p1), pb1 = pack_bf16x2(p2, p3);
+        // ---- O^T += V^T P^T over these 16 tokens ----
+        const uint32_t vaddr = vst + (uint32_t)((kc * 16 + ld_tok) * PROW + h * D * 2 + ld_dim * 2);
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vaddr + mt * 32, a0, a1, a2, a3);
+          mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    if (seg_end) {
+      l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+      l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+      const float me = __shfl_sync(0xffffffffu, m_run, 8 * t), mo = __shfl_sync(0xffffffffu, m_run, 8 * t + 4);
+      const float le = __shfl_sync(0xffffffffu, l_run, 8 * t), lo = __shfl_sync(0xffffffffu, l_run, 8 * t + 4);
+      const int he = 2 * t, ho = 2 * t + 1;
+      const int32_t c_lo = UP[b] / C, c_hi = (UP[b + 1] - 1) / C;
+      if (c_lo == c_hi) {
+        const float ie = 1.0f / le, io = 1.0f / lo;
+        uint16_t* oe = P.out + ((size_t)b * P.Hq + (size_t)h * G + he) * D;
+        uint16_t* oo = P.out + ((size_t)b * P.Hq + (size_t)h * G + ho) * D;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          if (he < G) {
+            oe[16 * mt + g] = f2bf(o[mt][0] * ie);
+            oe[16 * mt + g + 8] = f2bf(o[mt][2] * ie);
+          }
+          if (ho < G) {
+            oo[16 * mt + g] = f2bf(o[mt][1] * io);
+            oo[16 * mt + g + 8] = f2bf(o[mt][3] * io);
+          }
+        }
+      } else {
+        const size_t slot = (size_t)blockIdx.x + (size_t)b;
+        float* pe = P.partials + (slot * P.Hq + (size_t)h * G + he) * (D + 2);
+        float* po = P.partials + (slot * P.Hq + (size_t)h * G + ho) * (D + 2);
+        if (he < G) {
+          if (g == 0) {
+            pe[0] = me;
+            pe[1] = le;
+          }
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            pe[2 + 16 * mt + g] = o[mt][0];
+            pe[2 + 16 * mt + g + 8] = o[mt][2];
+          }
+        }
+        if (ho < G) {
+          if (g == 0) {
+            po[0] = mo;
+            po[1] = lo;
+          }
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            po[2 + 16 * mt + g] = o[mt][1];
+            po[2 + 16 * mt + g + 8] = o[mt][3];
+          }
+        }
+        finish_split_sequence<D, G>(P, b, c_lo, c_hi, NC, h, flag);
+      }
+    }
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
+  DecodeParams P;
+  P.lv = a.lv;
+  P.B = a.B;
+  P.Hq = a.Hq;
+  P.max_blocks = a.max_blocks;
+  P.q = a.q;
+  P.bt = a.bt;
+  P.ctx = a.ctx;
+  P.scale_log2 = a.scale_log2;
+  P.inv_sqrt_d = a.inv_sqrt_d;
+  P.signs = a.signs;
+  P.out = a.out;
+  P.counters = a.counters;
+  P.partials = a.partials;
+  P.T = a.tokens_per_stage;
+  P.NS = a.n_stages;
+  P.stage_bytes = 2 * P.T * (a.lv.hkv * D * 2 + 16);
+  auto kern = decode_bf16_mma_kernel<D, G>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<a.grid, (a.lv.hkv + 1) * 32, a.smem_bytes, a.stream>>>(P);
+  return cudaGetLastError();
+}
+
+inline cudaError_t launch_decode_bf16_mma(const DecodeArgs& a) {
+#define PKV_CASE(DD, GG) \
+  if (a.D == DD && a.G == GG) return launch_decode_bf16_mma_t<DD, GG>(a);
+  PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
+  PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
+  PKV_CASE(256, 1) PKV_CASE(256, 2) PKV_CASE(256, 4) PKV_CASE(256, 8)
+#undef PKV_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

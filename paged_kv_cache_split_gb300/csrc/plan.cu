@@ -17,6 +17,29 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
   size_t fixed = (size_t)(2 * B + 1 + 4) * 4 + 16 + 128;
   if (packed) fixed += (size_t)hkv * G * D * 4;
   if (fixed >= budget) return false;
+  if (!packed) {
+    // Native bf16 (tensor-core kernel): each token's row of all kv heads is copied
+    // into a padded row (payload + 16 bytes) for K and for V; T is 32 or 16 (the
+    // PV product consumes 16 tokens at a time).  Prefer T = 32 with >= 3 stages.
+    const size_t prow = (size_t)hkv * D * 2 + 16;
+    const int cand_bf16[2] = {32, 16};
+    for (int pass = 0; pass < 2; ++pass) {
+      for (int T : cand_bf16) {
+        const size_t stage = 2 * (size_t)T * prow;
+        size_t ns = (budget - fixed) / (stage + 16);
+        if (ns > 8) ns = 8;
+        if ((pass == 0 && ns >= 3) || (pass == 1 && ns >= 2)) {
+          plan->tokens_per_stage = T;
+          plan->n_stages = (int)ns;
+          plan->stage_bytes = stage;
+          plan->smem_bytes = ns * stage + ns * 16 + fixed;
+          plan->threads = (hkv + 1) * 32;
+          return true;
+        }
+      }
+    }
+    return false;
+  }
   const int cand[3] = {32, 16, 8};
   for (int pass = 0; pass < 2; ++pass) {
     for (int T : cand) {
