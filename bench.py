@@ -39,6 +39,7 @@ if ROOT not in sys.path:
 from paged_kv_cache_split_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "paged decode attention: achieved HBM GB/s (% of peak), KV tokens read/s"
+LAUNCHES_PER_CALL = 2  # attention kernel + split-K combine kernel
 FMT_ROW_BYTES = {wl.FMT_BF16: (2.0, 2.0, 0), wl.FMT_K4V4: (0.5, 0.5, 1), wl.FMT_K8V4: (1.0, 0.5, 1),
                  wl.FMT_K8V8: (1.0, 1.0, 1)}
 
@@ -415,10 +416,10 @@ def run_gpu(args, rank, world, local):
                      "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
                      "per_launch_bytes": bytes_layer, "avg_launch_us": round(launch_us, 3),
                      "eager_launch_us": round(eager_launch_us, 3), "peak_source": peak_src,
-                     "kernel": "decode_kernel (split-K flash decoding, fused combine)"},
+                     "kernel": "decode attention kernel + split-K combine kernel (per-launch time is their sum)"},
         "e2e": {"value": round(bytes_step * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": w.n_layers * args.steps,
+        "gpu_launches": LAUNCHES_PER_CALL * w.n_layers * args.steps,
         "clocks": sampler.summary(),
     }
     return res, w

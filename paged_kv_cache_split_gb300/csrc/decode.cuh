@@ -114,12 +114,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * P.stage_bytes);
   uint64_t* empty = full + NS;
-  int32_t* UP = reinterpret_cast<int32_t*>(empty + NS);  // [B + 1] unit prefix
+  const uint8_t** tab = reinterpret_cast<const uint8_t**>(empty + NS);  // [kSmemTableEntries]
+  int32_t* UP = reinterpret_cast<int32_t*>(tab + kSmemTableEntries);  // [B + 1] unit prefix
   int32_t* LS = UP + (B + 1);                             // [B] clamped lengths
   int32_t* flag = LS + B;                                 // [4]
   float* qscr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(flag + 4) + 15) & ~uintptr_t(15));
 
-  decode_prologue(P, full, empty, NC, UP, LS);
+  decode_prologue(P, full, empty, NC, UP, LS, tab);
   __syncthreads();
 
   const int32_t U = UP[B];
@@ -137,6 +138,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
 
   if (warp == NC) {
     // ----------------------------- producer ---------------------------------
+    const bool use_stab = smem_table_entries(P) > 0;
+    const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once
     int issued = 0;
     bool dead = false;
     for (int32_t ub = u0; ub < u1 && !dead; ub += 32) {
@@ -152,7 +155,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
         if (row >= 0 && (int64_t)row < P.lv.rows_capacity) {
           const int32_t slab = row / P.lv.slab_blocks;
           const int32_t r = row - slab * P.lv.slab_blocks;
-          const uint8_t* const* ent = P.lv.tab.base + (size_t)slab * P.lv.tab.stride;
+          const uint8_t* const* ent = use_stab ? tab + (size_t)slab * P.lv.n_kinds
+                                                : P.lv.tab.base + (size_t)slab * P.lv.tab.stride;
           const size_t first = (size_t)(r * kBlockTokens + slot0) * hkv;
           src[0] = ent[0] + first * KBt;
           src[1] = ent[1] + first * VBt;
@@ -181,11 +185,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
             mbar_arrive_expect_tx(&full[s], kbytes + vbytes + 2 * mbytes);
             uint8_t* st = stages + (size_t)s * P.stage_bytes;
             if (nv > 0) {
-              bulk_g2s(st, s0, kbytes, &full[s]);
-              bulk_g2s(st + off_v, s1, vbytes, &full[s]);
+              bulk_g2s_hint(st, s0, kbytes, &full[s], kv_policy);
+              bulk_g2s_hint(st + off_v, s1, vbytes, &full[s], kv_policy);
               if (Tr::PACKED) {
-                bulk_g2s(st + off_km, s2, mbytes, &full[s]);
-                bulk_g2s(st + off_vm, s3, mbytes, &full[s]);
+                bulk_g2s_hint(st + off_km, s2, mbytes, &full[s], kv_policy);
+                bulk_g2s_hint(st + off_vm, s3, mbytes, &full[s], kv_policy);
               }
             }
           }
@@ -412,11 +416,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
           }
         }
       } else {
-        const size_t slot = (size_t)blockIdx.x + (size_t)b;
         if (tsub == 0) {
 #pragma unroll
           for (int g = 0; g < G; ++g) {
-            float* pp = P.partials + (slot * P.Hq + (size_t)h * G + g) * (D + 2);
+            float* pp = partial_ptr(P, D, (size_t)blockIdx.x, b, (size_t)h * G + g);
             if (cg == 0) {
               pp[0] = m[g];
               pp[1] = lsum[g];
@@ -425,11 +428,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
             for (int p = 0; p < Tr::VP; ++p) {
               const int d0 = (p * Tr::NCG + cg) * Tr::VEPP;
 #pragma unroll
-              for (int e = 0; e < Tr::VEPP; ++e) pp[2 + d0 + e] = acc[g][p * Tr::VEPP + e];
+              for (int e = 0; e < Tr::VEPP; ++e) pp[kPartialHeader + d0 + e] = acc[g][p * Tr::VEPP + e];
             }
           }
         }
-        finish_split_sequence<D, G>(P, b, c_lo, c_hi, NC, h, flag);
       }
     }
   }
@@ -465,8 +467,9 @@ cudaError_t launch_decode_t(const DecodeArgs& a) {
     if (e != cudaSuccess) return e;
     smem_set = 232448;
   }
-  kern<<<a.grid, (a.lv.hkv + 1) * 32, a.smem_bytes, a.stream>>>(P);
-  return cudaGetLastError();
+  cudaError_t e = launch_with_pdl(kern, a.grid, (a.lv.hkv + 1) * 32, a.smem_bytes, a.stream, P);
+  if (e != cudaSuccess) return e;
+  return launch_combine<D>(P, a.grid, a.stream);
 }
 
 template <int FMT>

@@ -47,9 +47,38 @@ __device__ __forceinline__ int find_seq(const int32_t* UP, int B, int32_t u) {
 // warp) and warp 0 builds the unit prefix UP[0..B] over sequences (unit = T tokens
 // of one sequence) and LS[b], the context length clamped to the block table.  The
 // caller runs __syncthreads() afterwards.
+//
+// Programmatic dependent launch: the kernel waits for the previous kernel of the
+// stream to complete and publish its memory (wait) before it reads any input or
+// writes any output, and only then lets the next kernel of the stream be scheduled
+// (launch_dependents).  So when a dependent kernel starts, everything that preceded
+// this kernel on the stream has completed: the combine kernel relies on that to
+// read the context lengths before its own wait.
+//
+// Before the wait the kernel touches only what no kernel writes: it copies this
+// layer's slab base pointers into shared memory (`tab`, when they fit; the table
+// changes only through stream-ordered copies issued by append_slab) and issues L2
+// prefetch hints for the context lengths and the block table.
+constexpr int kSmemTableEntries = 1024;
+
+__device__ __forceinline__ int smem_table_entries(const DecodeParams& P) {
+  const int64_t n = (P.lv.rows_capacity / P.lv.slab_blocks) * P.lv.n_kinds;
+  return n <= kSmemTableEntries ? (int)n : 0;
+}
+
 __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t* full, uint64_t* empty, int NC,
-                                                int32_t* UP, int32_t* LS) {
+                                                int32_t* UP, int32_t* LS, const uint8_t** tab) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = smem_table_entries(P);
+  for (int i = threadIdx.x; i < nt; i += blockDim.x) {
+    const int slab = i / P.lv.n_kinds, kind = i - slab * P.lv.n_kinds;
+    tab[i] = P.lv.tab.base[(size_t)slab * P.lv.tab.stride + kind];
+  }
+  for (int i = threadIdx.x * 32; i < P.B; i += blockDim.x * 32) prefetch_l2(P.ctx + i);
+  for (int64_t i = (int64_t)threadIdx.x * 32; i < (int64_t)P.B * P.max_blocks; i += (int64_t)blockDim.x * 32)
+    prefetch_l2(P.bt + i);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.NS; ++s) {
       mbar_init(&full[s], 1);
@@ -94,65 +123,172 @@ __device__ __forceinline__ void zero_empty_sequences(const DecodeParams& P, cons
   }
 }
 
-// Split-K epilogue, run by every consumer warp of the CTA (warp h owns query heads
-// h*G .. h*G+G-1) after it has written its partial (m, l, acc[D]) of sequence b to
-// slot blockIdx.x + b.  The CTA takes an arrival ticket on the sequence's counter;
-// the CTA whose ticket completes the count merges the partials of CTAs c_lo..c_hi
-// in CTA order (so the result does not depend on arrival order), writes the bf16
-// output and resets the counter for the next launch.
-template <int D, int G>
-__device__ __forceinline__ void finish_split_sequence(const DecodeParams& P, int b, int32_t c_lo, int32_t c_hi,
-                                                      int NC, int h, int32_t* flag) {
+// Partial record of one (CTA, sequence, query head), 16-byte aligned:
+//   [m (running max, base 2), l (sum of probabilities), 0, 0, acc[D]]
+// in slot (CTA + sequence); CTAs c and c+1 of one sequence use consecutive slots.
+constexpr int kPartialHeader = 4;
+
+__host__ __device__ constexpr int partial_floats(int D) { return D + kPartialHeader; }
+
+__device__ __forceinline__ float* partial_ptr(const DecodeParams& P, int D, size_t cta, int b, size_t head) {
+  return P.partials + (((cta + (size_t)b) * P.Hq) + head) * (size_t)partial_floats(D);
+}
+
+template <int V>
+struct VecF;
+template <>
+struct VecF<2> {
+  using T = float2;
+};
+template <>
+struct VecF<4> {
+  using T = float4;
+};
+
+// Split-K merge, a separate kernel chained after the attention kernel: one warp
+// per (sequence, query head) of every sequence that more than one CTA worked on.
+// Parts are merged one after another in CTA order with the online-softmax rule
+// (running max, rescaled denominator and numerator), so the result does not
+// depend on which CTA finished first.  Each lane owns D/32 consecutive dims; the
+// loads of up to CH parts (their (m, l) and the lane's dims; CH = 32 for D <= 128,
+// 16 for D = 256) are issued before any is used, so a sequence split into <= CH
+// parts costs one L2 round trip.
+//
+// The attention kernel signals its dependents only after its own wait, so the
+// context lengths (inputs of the attention call, never written by it) are final
+// when this kernel starts: the unit prefix is built before waiting for the
+// partials.
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const DecodeParams P, int main_grid) {
+  extern __shared__ int32_t cup[];  // unit prefix UP[0..B]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __threadfence();
-  named_barrier_sync(1, NC * 32);
-  if (warp == 0 && lane == 0) {
-    const int32_t ticket = atomicAdd(&P.counters[b], 1);
-    const bool last = ticket == (c_hi - c_lo);
-    if (last) P.counters[b] = 0;
-    flag[0] = last ? 1 : 0;
-  }
-  named_barrier_sync(1, NC * 32);
-  if (!flag[0]) return;
-  __threadfence();
-  // Lanes own parts for the max and the denominator, and dims for the numerator,
-  // so that the L2 round trips overlap instead of chaining.
-  const int nparts = c_hi - c_lo + 1;
-  const size_t pstride = (size_t)P.Hq * (D + 2);  // CTAs c, c+1 use slots c+b, c+1+b
-#pragma unroll 1
-  for (int g = 0; g < G; ++g) {
-    const size_t head = (size_t)h * G + g;
-    const float* base = P.partials + (((size_t)c_lo + b) * P.Hq + head) * (D + 2);
-    float M = -INFINITY;
-    for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(base + (size_t)i * pstride));
+  if (warp == 0) {
+    const int lim = P.max_blocks * kBlockTokens;
+    int32_t carry = 0;
+    for (int base = 0; base < P.B; base += 32) {
+      const int b = base + lane;
+      int32_t n = 0;
+      if (b < P.B) {
+        int32_t L = P.ctx[b];
+        L = L < 0 ? 0 : (L > lim ? lim : L);
+        n = (L + P.T - 1) / P.T;
+      }
+      int32_t inc = n;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float den = 0.f;
-    for (int i = lane; i < nparts; i += 32) {
-      const float* pp = base + (size_t)i * pstride;
-      den += exp2f(__ldcg(pp) - M) * __ldcg(pp + 1);
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += y;
+      }
+      if (b < P.B) cup[b] = carry + inc - n;
+      carry += __shfl_sync(0xffffffffu, inc, 31);
     }
+    if (lane == 0) cup[P.B] = carry;
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int32_t U = cup[P.B];
+  const int32_t C = (U + main_grid - 1) / main_grid;
+  if (C == 0) return;
+  constexpr int V = D / 32;                // dims per lane: 2, 4 or 8
+  constexpr int NV = V / 2 > 2 ? 2 : 1;    // vector loads per lane per part
+  constexpr int VW = V / NV;               // floats per vector load: 2 or 4
+  using Vec = typename VecF<VW>::T;
+  constexpr int CH = D <= 128 ? 32 : 16;  // parts in flight per lane
+  const size_t pstride = (size_t)P.Hq * partial_floats(D);
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int pair = blockIdx.x * (blockDim.x >> 5) + warp; pair < P.B * P.Hq; pair += nwarps) {
+    const int b = pair / P.Hq;
+    const size_t head = (size_t)(pair % P.Hq);
+    if (cup[b + 1] == cup[b]) continue;  // empty: zeros written by the attention kernel
+    const int32_t c_lo = cup[b] / C, c_hi = (cup[b + 1] - 1) / C;
+    if (c_lo == c_hi) continue;  // one CTA: output written directly
+    const int nparts = c_hi - c_lo + 1;
+    const float* base = partial_ptr(P, D, (size_t)c_lo, b, head);
+    float M = -INFINITY, den = 0.f, num[V];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    const float inv = 1.0f / den;
-    float num[D / 32];
+    for (int j = 0; j < V; ++j) num[j] = 0.f;
+    for (int i0 = 0; i0 < nparts; i0 += CH) {
+      const int cnt = min(CH, nparts - i0);
+      // Issue every load of the chunk first: lane k's (m, l) of part i0+k, and the
+      // lane's dims of each part.
+      float2 ml = make_float2(-INFINITY, 0.f);
+      if (lane < cnt) ml = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(i0 + lane) * pstride));
+      Vec v[CH][NV];
 #pragma unroll
-    for (int j = 0; j < D / 32; ++j) num[j] = 0.f;
-    for (int i0 = 0; i0 < nparts; i0 += 32) {
-      const int i = i0 + lane;
-      const float wgt = i < nparts ? exp2f(__ldcg(base + (size_t)i * pstride) - M) : 0.f;
-      const int cnt = min(32, nparts - i0);
-#pragma unroll 4
-      for (int k = 0; k < cnt; ++k) {
-        const float wk = __shfl_sync(0xffffffffu, wgt, k);
-        const float* pp = base + (size_t)(i0 + k) * pstride + 2;
+      for (int k = 0; k < CH; ++k) {
+        if (k < cnt) {
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) num[j] = fmaf(wk, __ldcg(pp + lane + 32 * j), num[j]);
+          for (int x = 0; x < NV; ++x)
+            v[k][x] = __ldcg(reinterpret_cast<const Vec*>(base + (size_t)(i0 + k) * pstride + kPartialHeader +
+                                                          lane * V) + x);
+        }
+      }
+      // Lanes = parts: chunk max, weights, denominator.
+      float Mc = ml.x;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, off));
+      Mc = fmaxf(Mc, M);
+      const float a = exp2f(M - Mc);  // rescales earlier chunks (0 on the first)
+      const float wgt = exp2f(ml.x - Mc);
+      float dc = wgt * ml.y;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dc += __shfl_xor_sync(0xffffffffu, dc, off);
+      den = fmaf(den, a, dc);
+#pragma unroll
+      for (int j = 0; j < V; ++j) num[j] *= a;
+      M = Mc;
+      // Lanes = dims: add the chunk's parts in order.
+#pragma unroll
+      for (int k = 0; k < CH; ++k) {
+        if (k < cnt) {
+          const float wk = __shfl_sync(0xffffffffu, wgt, k);
+          const float* vf = reinterpret_cast<const float*>(&v[k][0]);
+#pragma unroll
+          for (int j = 0; j < V; ++j) num[j] = fmaf(wk, vf[j], num[j]);
+        }
       }
     }
+    const float inv = 1.0f / den;
+    uint16_t* o = P.out + ((size_t)b * P.Hq + head) * D + lane * V;
 #pragma unroll
-    for (int j = 0; j < D / 32; ++j) P.out[((size_t)b * P.Hq + head) * D + lane + 32 * j] = f2bf(num[j] * inv);
+    for (int j = 0; j < V; ++j) o[j] = f2bf(num[j] * inv);
   }
+}
+
+// Launch `kern` with programmatic stream serialization enabled (see above).
+template <typename Kern>
+inline cudaError_t launch_with_pdl(Kern kern, int grid, int threads, size_t smem, cudaStream_t stream,
+                                   const DecodeParams& P) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+template <int D>
+inline cudaError_t launch_combine(const DecodeParams& P, int main_grid, cudaStream_t stream) {
+  const int pairs = P.B * P.Hq;
+  int grid = (pairs + 7) / 8;
+  if (grid > 1024) grid = 1024;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = (size_t)(P.B + 1) * sizeof(int32_t);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel<D>, P, main_grid);
 }
 
 }  // namespace pkv

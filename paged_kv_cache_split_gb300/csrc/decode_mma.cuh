@@ -69,11 +69,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * P.stage_bytes);
   uint64_t* empty = full + NS;
-  int32_t* UP = reinterpret_cast<int32_t*>(empty + NS);
+  const uint8_t** tab = reinterpret_cast<const uint8_t**>(empty + NS);  // [kSmemTableEntries]
+  int32_t* UP = reinterpret_cast<int32_t*>(tab + kSmemTableEntries);
   int32_t* LS = UP + (B + 1);
-  int32_t* flag = LS + B;
 
-  decode_prologue(P, full, empty, NC, UP, LS);
+  decode_prologue(P, full, empty, NC, UP, LS, tab);
   __syncthreads();
   const int32_t U = UP[B];
   const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
@@ -83,25 +83,32 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   const int32_t u1 = min(U, u0 + C);
   if (u0 >= u1) return;
   const int offV = T * PROW;
+  const int offQ = 2 * T * PROW;          // q of the sequence, when the unit starts one
+  const int QB = P.Hq * D * 2;
 
   if (warp == NC) {
     // ----------------------------- producer ---------------------------------
+    const bool use_stab = smem_table_entries(P) > 0;
+    const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once
     int issued = 0;
     bool dead = false;
     for (int32_t ub = u0; ub < u1 && !dead; ub += 32) {
       const int32_t u = ub + lane;
       const uint8_t* kbase = nullptr;
       const uint8_t* vbase = nullptr;
+      const uint8_t* qsrc = nullptr;
       int ok = 0;
       if (u < u1) {
         const int b = find_seq(UP, B, u);
+        if (u == u0 || u == UP[b]) qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)b * P.Hq * D);
         const int32_t tok0 = (u - UP[b]) * T;
         const int j = tok0 / kBlockTokens, slot0 = tok0 % kBlockTokens;
         const int32_t row = P.bt[(size_t)b * P.max_blocks + j];
         if (row >= 0 && (int64_t)row < P.lv.rows_capacity) {
           const int32_t slab = row / P.lv.slab_blocks;
           const int32_t r = row - slab * P.lv.slab_blocks;
-          const uint8_t* const* ent = P.lv.tab.base + (size_t)slab * P.lv.tab.stride;
+          const uint8_t* const* ent = use_stab ? tab + (size_t)slab * P.lv.n_kinds
+                                                : P.lv.tab.base + (size_t)slab * P.lv.tab.stride;
           const size_t first = (size_t)(r * kBlockTokens + slot0) * ROW;
           kbase = ent[0] + first;
           vbase = ent[1] + first;
@@ -114,22 +121,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
       for (int i = 0; i < cnt; ++i) {
         const uint8_t* kb = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)kbase, i);
         const uint8_t* vb = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)vbase, i);
+        const uint8_t* qs = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)qsrc, i);
         const int oki = __shfl_sync(0xffffffffu, ok, i);
         const int s = issued % NS;
         if (lane == 0) {
           if (issued >= NS && !mbar_wait_bounded(&empty[s], ((issued / NS) & 1) ^ 1, err)) dead = true;
           // A whole unit is always copied (T tokens stay inside the block); tokens
-          // past the context are masked by a zero probability.
-          if (!dead) mbar_arrive_expect_tx(&full[s], oki ? (uint32_t)(2 * T * ROW) : 0u);
+          // past the context are masked by a zero probability.  A unit that starts
+          // a sequence also brings that sequence's q.
+          if (!dead)
+            mbar_arrive_expect_tx(&full[s], (oki ? (uint32_t)(2 * T * ROW) : 0u) + (qs ? (uint32_t)QB : 0u));
         }
         dead = __shfl_sync(0xffffffffu, dead, 0);
         if (dead) break;
         __syncwarp();
+        uint8_t* st = stages + (size_t)s * P.stage_bytes;
+        if (qs && lane == 31) bulk_g2s(st + offQ, qs, (uint32_t)QB, &full[s]);
         if (oki) {
-          uint8_t* st = stages + (size_t)s * P.stage_bytes;
           for (int c = lane; c < 2 * T; c += 32) {
             const int kind = c / T, tok = c - kind * T;
-            bulk_g2s(st + kind * offV + tok * PROW, (kind ? vb : kb) + (size_t)tok * ROW, (uint32_t)ROW, &full[s]);
+            bulk_g2s_hint(st + kind * offV + tok * PROW, (kind ? vb : kb) + (size_t)tok * ROW, (uint32_t)ROW,
+                          &full[s], kv_policy);
           }
         }
         ++issued;
@@ -162,14 +174,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
     const bool seg_start = (u == u0) || (u == UP[b]);
     const bool seg_end = (u == u1 - 1) || (u == UP[b + 1] - 1);
     if (seg_start) {
-      // A fragments of Q (rows = query heads of kv head h; rows >= G are zero).
-      const uint32_t* qrow =
-          reinterpret_cast<const uint32_t*>(P.q + ((size_t)b * P.Hq + (size_t)h * G + (g < G ? g : 0)) * D);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        qa[kk][0] = g < G ? qrow[(16 * kk + 2 * t) / 2] : 0u;
-        qa[kk][1] = g < G ? qrow[(16 * kk + 2 * t + 8) / 2] : 0u;
-      }
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
@@ -183,6 +187,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
     const int s = n % NS;
     if (!dead && !mbar_wait_bounded(&full[s], (n / NS) & 1, err)) dead = true;
     dead = __shfl_sync(0xffffffffu, dead, 0);
+    if (!dead && seg_start) {
+      // A fragments of Q (rows = query heads of kv head h; rows >= G are zero),
+      // from the copy of q that arrived with this stage.
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(stages + (size_t)s * P.stage_bytes + offQ +
+                                                               ((size_t)h * G + (g < G ? g : 0)) * D * 2);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        qa[kk][0] = g < G ? qrow[(16 * kk + 2 * t) / 2] : 0u;
+        qa[kk][1] = g < G ? qrow[(16 * kk + 2 * t + 8) / 2] : 0u;
+      }
+    }
     if (!dead) {
       const uint32_t kst = smem_base + (uint32_t)(s * P.stage_bytes);
       const uint32_t vst = kst + (uint32_t)offV;
@@ -265,9 +280,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
           }
         }
       } else {
-        const size_t slot = (size_t)blockIdx.x + (size_t)b;
-        float* pe = P.partials + (slot * P.Hq + (size_t)h * G + he) * (D + 2);
-        float* po = P.partials + (slot * P.Hq + (size_t)h * G + ho) * (D + 2);
+        float* pe = partial_ptr(P, D, (size_t)blockIdx.x, b, (size_t)h * G + he);
+        float* po = partial_ptr(P, D, (size_t)blockIdx.x, b, (size_t)h * G + ho);
         if (he < G) {
           if (g == 0) {
             pe[0] = me;
@@ -275,8 +289,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
           }
 #pragma unroll
           for (int mt = 0; mt < D / 16; ++mt) {
-            pe[2 + 16 * mt + g] = o[mt][0];
-            pe[2 + 16 * mt + g + 8] = o[mt][2];
+            pe[kPartialHeader + 16 * mt + g] = o[mt][0];
+            pe[kPartialHeader + 16 * mt + g + 8] = o[mt][2];
           }
         }
         if (ho < G) {
@@ -286,11 +300,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
           }
 #pragma unroll
           for (int mt = 0; mt < D / 16; ++mt) {
-            po[2 + 16 * mt + g] = o[mt][1];
-            po[2 + 16 * mt + g + 8] = o[mt][3];
+            po[kPartialHeader + 16 * mt + g] = o[mt][1];
+            po[kPartialHeader + 16 * mt + g + 8] = o[mt][3];
           }
         }
-        finish_split_sequence<D, G>(P, b, c_lo, c_hi, NC, h, flag);
       }
     }
   }
@@ -314,7 +327,7 @@ cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
   P.partials = a.partials;
   P.T = a.tokens_per_stage;
   P.NS = a.n_stages;
-  P.stage_bytes = 2 * P.T * (a.lv.hkv * D * 2 + 16);
+  P.stage_bytes = 2 * P.T * (a.lv.hkv * D * 2 + 16) + a.Hq * D * 2;
   auto kern = decode_bf16_mma_kernel<D, G>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -322,8 +335,9 @@ cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<a.grid, (a.lv.hkv + 1) * 32, a.smem_bytes, a.stream>>>(P);
-  return cudaGetLastError();
+  cudaError_t e = launch_with_pdl(kern, a.grid, (a.lv.hkv + 1) * 32, a.smem_bytes, a.stream, P);
+  if (e != cudaSuccess) return e;
+  return launch_combine<D>(P, a.grid, a.stream);
 }
 
 inline cudaError_t launch_decode_bf16_mma(const DecodeArgs& a) {

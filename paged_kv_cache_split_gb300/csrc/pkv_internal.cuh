@@ -49,7 +49,7 @@ struct LayerView {
   int n_kinds;
   int hkv;
   int slab_blocks;
-  int64_t rows_capacity;  // rows valid at enqueue time
+  int64_t rows_capacity;  // rows valid at enqueue time (n_slabs * slab_blocks)
   int row_bytes[4];       // per (token, head) row, per kind
   int32_t* err;           // device error word
 };
@@ -119,6 +119,27 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Same copy with an L2 cache policy (e.g. evict-first for data read once).
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// L2 policy: lines fetched under it are the first candidates for eviction.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {

@@ -14,7 +14,7 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
   const size_t meta = packed ? (size_t)(D / kGroup) * 8 : 0;
   const size_t per_token = (size_t)hkv * ((size_t)(fb.k + fb.v) * D / 8 + 2 * meta);
   const size_t budget = 232448;  // 227 KB opt-in shared memory per block on sm_100-class parts
-  size_t fixed = (size_t)(2 * B + 1 + 4) * 4 + 16 + 128;
+  size_t fixed = (size_t)(2 * B + 1 + 4) * 4 + 16 + 128 + 1024 * sizeof(void*);  // + staged slab table (kSmemTableEntries)
   if (packed) fixed += (size_t)hkv * G * D * 4;
   if (fixed >= budget) return false;
   if (!packed) {
@@ -25,7 +25,7 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
     const int cand_bf16[2] = {32, 16};
     for (int pass = 0; pass < 2; ++pass) {
       for (int T : cand_bf16) {
-        const size_t stage = 2 * (size_t)T * prow;
+        const size_t stage = 2 * (size_t)T * prow + (size_t)hkv * G * D * 2;  // + q of one sequence
         size_t ns = (budget - fixed) / (stage + 16);
         if (ns > 8) ns = 8;
         if ((pass == 0 && ns >= 3) || (pass == 1 && ns >= 2)) {

@@ -360,7 +360,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 static size_t workspace_bytes(const pkv_pool* p, int B, int Hq) {
   const int D = p->cfg.head_dim;
   return align_up((size_t)B * sizeof(int32_t), 256) +
-         (size_t)(decode_grid(p) + B) * (size_t)Hq * (size_t)(D + 2) * sizeof(float);
+         (size_t)(decode_grid(p) + B) * (size_t)Hq * (size_t)(D + 4) * sizeof(float);
 }
 
 pkv_status pkv_decode_workspace_bytes(const pkv_pool* p, int B, int Hq, int max_ctx, size_t* bytes) {
