@@ -1,6 +1,6 @@
-// decode_k8v4.cu — decode-attention instantiations for the K8V4 stored format.
-#include "decode.cuh"
+// decode_k8v4.cu — decode attention for the K8V4 packed format (tensor-core tiles).
+#include "decode_packed_mma.cuh"
 
 namespace pkv {
-cudaError_t launch_decode_k8v4(const DecodeArgs& a) { return launch_decode_fmt<PKV_FMT_K8V4>(a); }
+cudaError_t launch_decode_k8v4(const DecodeArgs& a) { return launch_decode_packed_mma<PKV_FMT_K8V4>(a); }
 }  // namespace pkv

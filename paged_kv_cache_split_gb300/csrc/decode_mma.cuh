@@ -1,9 +1,9 @@
 // decode_mma.cuh — native-bf16 paged decode attention on tensor-core tiles.
 //
-// Same contract and work partition as decode.cuh (units of T tokens x all kv heads
-// split evenly over one CTA per SM, producer warp + one consumer warp per kv head,
-// split-K partials merged by the last CTA of a sequence), with two changes that
-// cut the consumer's issue slots by several times for bf16 K/V:
+// Work partition: units of T tokens x all kv heads, split evenly over one CTA per
+// SM; a producer warp plus one consumer warp per kv head; split-K partials merged
+// by the chained combine kernel (decode_common.cuh).  For bf16 K/V two choices cut
+// the consumer's issue slots by several times against CUDA-core dot products:
 //
 //  * Staging: the producer copies each token's row (all kv heads, contiguous in
 //    the slab) with its own 1-D bulk copy into a padded shared-memory row whose

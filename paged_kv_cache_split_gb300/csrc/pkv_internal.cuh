@@ -52,7 +52,26 @@ struct LayerView {
   int64_t rows_capacity;  // rows valid at enqueue time (n_slabs * slab_blocks)
   int row_bytes[4];       // per (token, head) row, per kind
   int32_t* err;           // device error word
+  // Packed formats: TMA tensor maps.  The map of (slab, this layer, kind) lives at
+  // (slab's kind-0 pointer of this layer) + map_delta + kind * 128.
+  int64_t map_delta;
+  int box_bytes[4];       // inner box width (bytes) per kind: 128, 64, 32 or 16
 };
+
+// Bytes of one stage of the packed decode kernel: four 1024-byte-aligned regions
+// of T rows (K codes, V codes, K meta, V meta; all kv heads) and q of one sequence.
+inline int packed_stage_bytes(int T, int krow, int vrow, int mrow, int qbytes) {
+  auto a = [](int x) { return (x + 1023) & ~1023; };
+  return a(T * krow) + a(T * vrow) + 2 * a(T * mrow) + a(qbytes);
+}
+
+// Inner box width for a row of `row_bytes` (all kv heads of one token): the
+// largest of 128/64/32/16 bytes that divides it (its swizzle span).
+inline int tma_box_bytes(int64_t row_bytes) {
+  for (int w = 128; w >= 16; w >>= 1)
+    if (row_bytes % w == 0) return w;
+  return 0;
+}
 
 // ---------------------------------------------------------------------------
 // Inline PTX helpers (sm_90+ mbarrier and bulk-copy forms, used on sm_103a).
@@ -129,6 +148,23 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+// 2-D tensor (TMA) copy of one box into shared memory, completing on `bar`, with an
+// L2 cache policy.  `tmap` is the global address of a CUtensorMap; x (innermost,
+// bytes for a uint8 map) must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar,
+                                           uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Make a tensor map written outside this kernel visible to the tensor-map proxy.
+__device__ __forceinline__ void tensormap_acquire(const void* tmap) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tmap) : "memory");
 }
 
 // L2 policy: lines fetched under it are the first candidates for eviction.

@@ -3,10 +3,10 @@
 
 namespace pkv {
 
-// The kernel keeps NS stages of T tokens x all kv heads in shared memory.  Pick
-// the largest T in {32, 16, 8} that still allows at least 4 stages (at most 8),
-// leaving room for the barriers, the per-sequence unit prefix and, for packed
-// formats, the per-warp q scratch used by the Hadamard rotation.
+// The kernels keep NS stages of T tokens x all kv heads in shared memory (T = 32
+// or 16, NS <= 8), leaving room for the barriers, the staged slab table, the
+// per-sequence unit prefix and, for packed formats, the per-warp q scratch used by
+// the Hadamard rotation.
 bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
   const FormatBits fb = format_bits(fmt);
   if (fb.k == 0 || hkv < 1 || hkv > 8 || B < 1 || B > 4096) return false;
@@ -40,23 +40,32 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
     }
     return false;
   }
-  const int cand[3] = {32, 16, 8};
-  for (int pass = 0; pass < 2; ++pass) {
-    for (int T : cand) {
-      const size_t stage = (size_t)T * per_token;
-      size_t ns = (budget - fixed) / (stage + 16);
-      if (ns > 8) ns = 8;
-      if ((pass == 0 && ns >= 4) || (pass == 1 && ns >= 2)) {
-        plan->tokens_per_stage = T;
-        plan->n_stages = (int)ns;
-        plan->stage_bytes = stage;
-        plan->smem_bytes = ns * stage + ns * 16 + fixed;
-        plan->threads = (hkv + 1) * 32;
-        return true;
+  {
+    // Packed formats (tensor-core kernel): T tokens of K codes, V codes, K meta and
+    // V meta for all kv heads, each in a 1024-byte-aligned region of swizzled TMA
+    // boxes, plus q of one sequence per stage; T = 32 (or 16 when 3 stages would
+    // not fit).
+    const int kr = hkv * D * fb.k / 8, vr = hkv * D * fb.v / 8, mr = hkv * (int)meta;
+    const int cand_p[2] = {32, 16};
+    for (int pass = 0; pass < 2; ++pass) {
+      for (int T : cand_p) {
+        // + 1024: the kernel aligns the first stage to a 1024-byte boundary
+        const size_t stage = (size_t)packed_stage_bytes(T, kr, vr, mr, hkv * G * D * 2);
+        if (fixed + 1024 >= budget) return false;
+        size_t ns = (budget - fixed - 1024) / (stage + 16);
+        if (ns > 8) ns = 8;
+        if ((pass == 0 && ns >= 3) || (pass == 1 && ns >= 2)) {
+          plan->tokens_per_stage = T;
+          plan->n_stages = (int)ns;
+          plan->stage_bytes = stage;
+          plan->smem_bytes = ns * stage + ns * 16 + fixed + 1024;
+          plan->threads = (hkv + 1) * 32;
+          return true;
+        }
       }
     }
+    return false;
   }
-  return false;
 }
 
 }  // namespace pkv

@@ -12,6 +12,7 @@
 // device pointer table still has one entry per (slab, layer, tensor), which is
 // what every kernel reads (touch point 4: per-slab base pointers; touch point 7:
 // one mapping helper).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -36,6 +37,8 @@ struct pkv_pool {
   int64_t row_bytes[4] = {0, 0, 0, 0};
   int64_t slab_bytes[4] = {0, 0, 0, 0};  // one slab of one layer, per kind
   int64_t group_bytes = 0;               // one slab index across layers and kinds
+  int64_t layer_bytes = 0;               // one slab of one layer, all kinds
+  int64_t maps_offset = 0;               // packed: tensor maps at the group's tail
   std::vector<void*> groups;             // allocation per slab index
   uint8_t** table_host = nullptr;        // pinned [max_slabs][n_layers][n_kinds]
   uint8_t** table_dev = nullptr;
@@ -85,7 +88,61 @@ static LayerView layer_view(const pkv_pool* p, int layer) {
   lv.rows_capacity = (int64_t)p->groups.size() * p->cfg.slab_blocks;
   for (int k = 0; k < 4; ++k) lv.row_bytes[k] = (int)p->row_bytes[k];
   lv.err = p->err_dev;
+  lv.map_delta = p->maps_offset - (int64_t)layer * p->layer_bytes + (int64_t)layer * p->n_kinds * 128;
+  for (int k = 0; k < 4; ++k)
+    lv.box_bytes[k] = k < p->n_kinds ? tma_box_bytes(p->row_bytes[k] * p->cfg.n_kv_heads) : 0;
   return lv;
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry point.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// 2-D tensor maps of one slab group (packed formats): for every layer and stored
+// tensor, the slab viewed as [slab_blocks * 32 tokens][Hkv * row] bytes, read in
+// boxes of 16 tokens x box_bytes with the matching shared-memory swizzle.
+static bool encode_group_maps(const pkv_pool* p, uint8_t* group, std::vector<CUtensorMap>& maps) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const int L = p->cfg.n_layers, K = p->n_kinds;
+  maps.resize((size_t)L * K);
+  int64_t off = 0;
+  for (int l = 0; l < L; ++l)
+    for (int k = 0; k < K; ++k) {
+      const int64_t row = p->row_bytes[k] * p->cfg.n_kv_heads;
+      const int box = tma_box_bytes(row);
+      const CUtensorMapSwizzle sw = box == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                    : box == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                    : box == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
+      const cuuint64_t dims[2] = {(cuuint64_t)row, (cuuint64_t)p->cfg.slab_blocks * kBlockTokens};
+      const cuuint64_t strides[1] = {(cuuint64_t)row};
+      const cuuint32_t boxd[2] = {(cuuint32_t)box, 16u};
+      const cuuint32_t estr[2] = {1u, 1u};
+      if (enc(&maps[(size_t)l * K + k], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, group + off, dims, strides, boxd, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+      off += p->slab_bytes[k];
+    }
+  return true;
 }
 
 extern "C" {
@@ -148,10 +205,18 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_allocator* allo
     p->row_bytes[PKV_KIND_VMETA] = p->row_bytes[PKV_KIND_KMETA];
   }
   const int64_t per_row_tokens = (int64_t)cfg->slab_blocks * kBlockTokens * cfg->n_kv_heads;
-  p->group_bytes = 0;
+  p->layer_bytes = 0;
   for (int k = 0; k < p->n_kinds; ++k) {
     p->slab_bytes[k] = per_row_tokens * p->row_bytes[k];
-    p->group_bytes += p->slab_bytes[k] * cfg->n_layers;
+    p->layer_bytes += p->slab_bytes[k];
+  }
+  p->group_bytes = p->layer_bytes * cfg->n_layers;
+  if (p->n_kinds == 4) {
+    // Tensor maps (128 bytes each, 64-byte aligned) after the slab data.
+    p->maps_offset = (p->group_bytes + 127) / 128 * 128;
+    p->group_bytes = p->maps_offset + (int64_t)cfg->n_layers * p->n_kinds * 128;
+    for (int k = 0; k < 4; ++k)
+      if (tma_box_bytes(p->row_bytes[k] * cfg->n_kv_heads) == 0) return fail(PKV_ERR_INVALID);
   }
 
   const size_t table_entries = (size_t)cfg->max_slabs * cfg->n_layers * p->n_kinds;
@@ -227,8 +292,29 @@ pkv_status pkv_append_slab(pkv_pool* p, int n_slabs, void* stream) {
     }
     fresh.push_back(ptr);
   }
+  // Packed formats: tensor maps of the new slabs, encoded before anything is
+  // enqueued so that a failure leaves the pool unchanged.
+  std::vector<std::vector<CUtensorMap>> maps(p->n_kinds == 4 ? fresh.size() : 0);
+  for (size_t i = 0; i < maps.size(); ++i) {
+    if (!encode_group_maps(p, (uint8_t*)fresh[i], maps[i])) {
+      for (void* q : fresh) {
+        if (p->default_alloc)
+          cudaFreeAsync(q, s);
+        else
+          p->alloc.release(p->alloc.ctx, q, stream);
+      }
+      g_last_error = "cuTensorMapEncodeTiled unavailable or rejected a slab";
+      return PKV_ERR_CUDA;
+    }
+  }
   // Zero the new slabs (a fresh zeros slab), then publish their base pointers.
   for (void* ptr : fresh) PKV_CUDA(cudaMemsetAsync(ptr, 0, (size_t)p->group_bytes, s), "cudaMemsetAsync(slab)");
+  // The maps are copied from pageable memory: the call stages the bytes before it
+  // returns, so the vectors may go out of scope at once.
+  for (size_t i = 0; i < maps.size(); ++i)
+    PKV_CUDA(cudaMemcpyAsync((uint8_t*)fresh[i] + p->maps_offset, maps[i].data(),
+                             maps[i].size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice, s),
+             "cudaMemcpyAsync(tensor maps)");
   const int L = p->cfg.n_layers, K = p->n_kinds;
   for (int i = 0; i < n_slabs; ++i) {
     uint8_t* g = (uint8_t*)fresh[(size_t)i];
@@ -437,7 +523,7 @@ pkv_status pkv_pool_stats(const pkv_pool* p, pkv_stats* out) {
   out->slab_append_events = p->append_events;
   out->rows_capacity = (int64_t)p->groups.size() * p->cfg.slab_blocks;
   out->rows_in_use = p->rows_in_use;
-  out->bytes_reserved = (int64_t)p->groups.size() * p->group_bytes;
+  out->bytes_reserved = (int64_t)p->groups.size() * p->layer_bytes * p->cfg.n_layers;  // slab data only
   for (int k = 0; k < 4; ++k) out->row_bytes[k] = p->row_bytes[k];
   return PKV_OK;
 }
