@@ -177,7 +177,9 @@ __device__ __forceinline__ int swz(const SwzRegion& z, int tok, int b) {
 
 __device__ __forceinline__ int ilog2i(int v) { return 31 - __clz(v); }
 
-template <int FMT, int D, int G>
+// W128: every stored tensor's all-heads row is a multiple of 128 bytes, so every box
+// is 128 bytes wide; then all addressing below reduces to per-lane constants.
+template <int FMT, int D, int G, bool W128>
 __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const DecodeParams P) {
   using Tr = PackedTraits<FMT, D>;
   static_assert(G >= 1 && G <= 8 && D % 32 == 0, "geometry");
@@ -375,9 +377,64 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
       __syncwarp();
     }
     if (!dead) {
+      // Fast-path addressing (W128).  A lane touches token rows whose 128-byte
+      // swizzle key is fixed: K code rows 8j+g (key g), meta and V rows 8p+2t+e
+      // (key 2t^e).  base = region + head's box column + first row (+ lane bytes);
+      // key = (head's chunk ^ row key) << 4.  Chunk offsets inside the row are
+      // compile-time and enter through one XOR with the key.
+      const int KBASE = zr[0].off + ((h * Tr::KB) >> 7) * 2048 + g * 128 + 4 * t;
+      const int KKEY = ((((h * Tr::KB) >> 4) & 7) ^ g) << 4;
+      const int MKEY = ((((h * Tr::MB) >> 4) & 7) ^ (2 * t)) << 4;
+      const int KMBASE = zr[2].off + ((h * Tr::MB) >> 7) * 2048 + 2 * t * 128;
+      const int VMBASE = zr[3].off + ((h * Tr::MB) >> 7) * 2048 + 2 * t * 128;
+      const int VBASE = zr[1].off + ((h * Tr::VB) >> 7) * 2048 + 2 * t * 128 +
+                        (Tr::VBITS == 4 ? 4 * (g >> 1) : 4 * (g & 3));
+      const int VKEY = (((((h * Tr::VB) >> 4) & 7) ^ (2 * t)) << 4) ^ (Tr::VBITS == 8 ? 16 * (g >> 2) : 0);
       for (int kc = 0; kc * 16 < nv; ++kc) {
         // ---- logits for 16 tokens: n-tiles 2kc, 2kc+1 ----
         float x[2][2];
+        if constexpr (W128) {
+          const uint8_t* kq = st + KBASE + kc * zr[0].nx * 2048;
+          const uint8_t* km = st + KMBASE + kc * zr[2].nx * 2048;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float sa0 = 0.f, sa1 = 0.f;
+#pragma unroll
+            for (int gp = 0; gp < NG / 2; ++gp) {
+              // (scale, offset) of groups 2gp, 2gp+1 for tokens 8j+2t (e=0) and 8j+2t+1 (e=1)
+              const int moc = 16 * gp;
+              const float4 me0 = *reinterpret_cast<const float4*>(km + 1024 * j + (moc >> 7) * 2048 + (MKEY ^ (moc & 112)));
+              const float4 me1 =
+                  *reinterpret_cast<const float4*>(km + 1024 * j + 128 + (moc >> 7) * 2048 + (MKEY ^ ((moc & 112) ^ 16)));
+#pragma unroll
+              for (int q2 = 0; q2 < 2; ++q2) {
+                const int grp = 2 * gp + q2;
+                const int oc = grp * (kGroup * Tr::KBITS / 8);
+                uint32_t bfr[2][2];
+                if constexpr (Tr::KBITS == 4) {
+                  k_group_frags4(*reinterpret_cast<const uint32_t*>(kq + 1024 * j + (oc >> 7) * 2048 + (KKEY ^ (oc & 112))),
+                                 bfr);
+                } else {
+                  k_group_frags8(
+                      *reinterpret_cast<const uint32_t*>(kq + 1024 * j + (oc >> 7) * 2048 + (KKEY ^ (oc & 112))),
+                      *reinterpret_cast<const uint32_t*>(kq + 1024 * j + ((oc + 16) >> 7) * 2048 +
+                                                         (KKEY ^ ((oc + 16) & 112))),
+                      bfr);
+                }
+                float cacc[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_f16_16816(cacc, qa[grp][0][0], 0u, qa[grp][0][1], 0u, bfr[0][0], bfr[0][1]);
+                mma_f16_16816(cacc, qa[grp][1][0], 0u, qa[grp][1][1], 0u, bfr[1][0], bfr[1][1]);
+                const float s0 = q2 ? me0.z : me0.x, o0 = q2 ? me0.w : me0.y;
+                const float s1 = q2 ? me1.z : me1.x, o1 = q2 ? me1.w : me1.y;
+                sa0 = fmaf(s0, cacc[0] - qbias[grp], fmaf(o0, qsum[grp], sa0));
+                sa1 = fmaf(s1, cacc[1] - qbias[grp], fmaf(o1, qsum[grp], sa1));
+              }
+            }
+            const int tk = kc * 16 + 8 * j + 2 * t;
+            x[j][0] = tk < nv ? sa0 * P.scale_log2 : -INFINITY;
+            x[j][1] = tk + 1 < nv ? sa1 * P.scale_log2 : -INFINITY;
+          }
+        } else {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int tb = kc * 16 + 8 * j;  // first token of the n-tile
@@ -404,6 +461,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
           const int tk = tb + 2 * t;
           x[j][0] = tk < nv ? sa0 * P.scale_log2 : -INFINITY;
           x[j][1] = tk + 1 < nv ? sa1 * P.scale_log2 : -INFINITY;
+        }
         }
         // ---- online softmax for head g ----
         float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
@@ -432,6 +490,50 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
         const uint32_t pb0 = pack_f16x2(p00, p01), pb1 = pack_f16x2(p10, p11);
         // ---- O^T += V^T P^T over these 16 tokens ----
         const int t0 = kc * 16 + 2 * t;
+        if constexpr (W128) {
+          const uint8_t* vq = st + VBASE + kc * zr[1].nx * 2048;
+          const uint8_t* vm = st + VMBASE + kc * zr[3].nx * 2048;
+#pragma unroll
+          for (int gp = 0; gp < NG / 2; ++gp) {
+            // (scale, offset) of groups 2gp, 2gp+1 for tokens 2t+e+8p
+            const int moc = 16 * gp;
+            float4 mv[2][2];
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+              for (int e = 0; e < 2; ++e)
+                mv[pp][e] = *reinterpret_cast<const float4*>(vm + 1024 * pp + 128 * e + (moc >> 7) * 2048 +
+                                                             (MKEY ^ ((moc & 112) ^ (16 * e))));
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+              const int grp = 2 * gp + q2;
+              const int oc = Tr::VBITS == 4 ? 16 * grp : 32 * grp;
+              uint32_t w[2][2];
+#pragma unroll
+              for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                  w[pp][e] = *reinterpret_cast<const uint32_t*>(vq + 1024 * pp + 128 * e + (oc >> 7) * 2048 +
+                                                                (VKEY ^ ((oc & 112) ^ (16 * e))));
+              const float2 s0 = q2 ? make_float2(mv[0][0].z, mv[0][0].w) : make_float2(mv[0][0].x, mv[0][0].y);
+              const float2 s1 = q2 ? make_float2(mv[0][1].z, mv[0][1].w) : make_float2(mv[0][1].x, mv[0][1].y);
+              const float2 s2 = q2 ? make_float2(mv[1][0].z, mv[1][0].w) : make_float2(mv[1][0].x, mv[1][0].y);
+              const float2 s3 = q2 ? make_float2(mv[1][1].z, mv[1][1].w) : make_float2(mv[1][1].x, mv[1][1].y);
+              const uint32_t sc01 = pack_f16x2(s0.x, s1.x), of01 = pack_f16x2(s0.y, s1.y);
+              const uint32_t sc23 = pack_f16x2(s2.x, s3.x), of23 = pack_f16x2(s2.y, s3.y);
+              uint32_t a[2][4];
+              v_group_frags<Tr::VBITS>(w[0][0], w[0][1], w[1][0], w[1][1], g, a);
+#pragma unroll
+              for (int mi = 0; mi < 2; ++mi) {
+                const uint32_t d0 = hfma2_u32(hsub2_u32(a[mi][0], kF16Magic2), sc01, of01);
+                const uint32_t d1 = hfma2_u32(hsub2_u32(a[mi][1], kF16Magic2), sc01, of01);
+                const uint32_t d2 = hfma2_u32(hsub2_u32(a[mi][2], kF16Magic2), sc23, of23);
+                const uint32_t d3 = hfma2_u32(hsub2_u32(a[mi][3], kF16Magic2), sc23, of23);
+                mma_f16_16816(o[grp][mi], d0, d1, d2, d3, pb0, pb1);
+              }
+            }
+          }
+        } else {
 #pragma unroll
         for (int grp = 0; grp < NG; ++grp) {
           const int vb = h * Tr::VB + v_word_offset<Tr::VBITS>(grp, g);
@@ -457,6 +559,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
             const uint32_t d3 = hfma2_u32(hsub2_u32(a[mi][3], kF16Magic2), sc23, of23);
             mma_f16_16816(o[grp][mi], d0, d1, d2, d3, pb0, pb1);
           }
+        }
         }
       }
       __syncwarp();
@@ -518,7 +621,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
   }
 }
 
-template <int FMT, int D, int G>
+template <int FMT, int D, int G, bool W128>
 cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   using Tr = PackedTraits<FMT, D>;
   DecodeParams P;
@@ -539,7 +642,7 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   P.NS = a.n_stages;
   const int hkv = a.lv.hkv;
   P.stage_bytes = packed_stage_bytes(P.T, hkv * Tr::KB, hkv * Tr::VB, hkv * Tr::MB, a.Hq * D * 2);
-  auto kern = decode_packed_mma_kernel<FMT, D, G>;
+  auto kern = decode_packed_mma_kernel<FMT, D, G, W128>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
@@ -553,8 +656,12 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
 
 template <int FMT>
 cudaError_t launch_decode_packed_mma(const DecodeArgs& a) {
-#define PKV_CASE(DD, GG) \
-  if (a.D == DD && a.G == GG) return launch_decode_packed_mma_t<FMT, DD, GG>(a);
+  const bool w128 = a.lv.box_bytes[0] == 128 && a.lv.box_bytes[1] == 128 && a.lv.box_bytes[2] == 128 &&
+                    a.lv.box_bytes[3] == 128;
+#define PKV_CASE(DD, GG)                                                      \
+  if (a.D == DD && a.G == GG)                                                 \
+    return w128 ? launch_decode_packed_mma_t<FMT, DD, GG, true>(a)            \
+                : launch_decode_packed_mma_t<FMT, DD, GG, false>(a);
   PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
   PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
   PKV_CASE(256, 1) PKV_CASE(256, 2) PKV_CASE(256, 4) PKV_CASE(256, 8)
