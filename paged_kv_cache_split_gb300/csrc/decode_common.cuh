@@ -30,6 +30,14 @@ struct DecodeParams {
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
 
+// 2^x with the hardware approximation (relative error below 2^-22; results below
+// 2^-126 flush to zero, which a softmax weight can drop).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint16_t f2bf(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
 // Unit u -> sequence: the largest b with UP[b] <= u (then UP[b+1] > u).

@@ -8,31 +8,34 @@
 // tensor map [tokens][all-heads row bytes]; a stage holds T tokens of each tensor as
 // boxes of 16 tokens x W bytes (W = 128, 64, 32 or 16, the largest dividing the
 // row), written with the W-byte shared-memory swizzle (16-byte chunk c of box row r
-// lands at chunk c ^ f(r)), so reads of one column across 8 tokens are
-// conflict-free.  A 32-token stage of K4/V4 with 8 heads of 128 dims is 24 box
-// copies.  q comes with the first unit of a sequence (one bulk copy).  The packed
-// pages are consumed directly, never expanded in memory (mlx-swift-lm PR #142,
-// Summary: direct attention on packed pages):
+// lands at chunk c ^ f(r)), so 16-byte chunks of 8 consecutive tokens sit in
+// distinct banks and are read with ldmatrix.  q comes with the first unit of a
+// sequence (one bulk copy).  The packed pages are consumed directly, never
+// expanded in memory (mlx-swift-lm PR #142, Summary: direct attention on packed
+// pages):
 //
 //  * q is rotated into K's signed Hadamard basis (q~ = H diag(s) q / sqrt(D), FWHT
 //    in per-warp shared scratch) when a sequence starts and kept as fp16 A
 //    fragments (rows = query heads, rows >= G zero).
-//  * QK, one affine group of 32 dims at a time: a code c becomes the fp16 value
-//    1024 + c by OR-ing it into the mantissa of 1024 (exact; for 4-bit codes in odd
-//    nibble positions the value is 1024 + 16c and the matching q entries are
-//    stored divided by 16).  The group's product C = sum_k A_k (1024 + c_k') gives
-//    q~.c = C - 1024 * sum_k A_k, and the stored (scale s, offset o) of the token
+//  * Codes enter the tensor cores as fp16 subnormals: the bit pattern of a code c
+//    (4 or 8 bits) in the low mantissa bits is the exact value c * 2^-24, so a code
+//    becomes an operand with one AND (4-bit) or one byte permute (8-bit).  A 4-bit
+//    code in the high nibble of its byte is taken as 16c * 2^-24 and the factor 16
+//    is removed on the other operand (q / 16) or on the output (V).
+//  * QK, one affine group of 32 dims at a time: the group's product
+//    C = sum_k q~_k c_k * 2^-24, and the stored (scale s, offset o) of the token
 //    and group fold in on the accumulator fragment:
-//        logit += s (C - bias) + o * sum(q~ over the group).
+//        logit = 2^24 * sum_groups [ s C + o * 2^-24 * sum(q~ over the group) ].
 //    A consistent permutation of the 32 dims of a group is used on both operands
 //    (the dot product does not depend on the order), chosen so that each lane's
-//    B fragment comes from one 32-bit word of codes.
-//  * PV as O^T = V^T P^T: the A operand holds V codes of two tokens per register,
-//    dequantised in fp16 (v = s (c) + o with the tokens' own s and o), the B
-//    operand is P (fp16) straight from the S accumulator fragments.  Each 16-row
-//    M tile covers 16 dims of one group; the order of dims inside a group is
-//    permuted so that a lane's two dims come from one half-word (4-bit) or one byte
-//    pair (8-bit) of a code word, and the output store undoes the permutation.
+//    B fragment comes from one 32-bit word of codes (an ldmatrix row).
+//  * PV as O^T = V^T (P S)^T + (P O_v): the A operand holds raw V codes of two
+//    tokens per register (ldmatrix.trans of the code rows), the B operand is
+//    p_t * s_t (fp16) formed from the S accumulator fragments and the tokens'
+//    scales, and the offsets add sum_t p_t o_t per head and group in fp32.  Each
+//    16-row M tile covers 16 dims of one group; the order of dims inside a group
+//    follows the ldmatrix.trans fragment (a lane's two dims per token come from one
+//    half-word of codes) and the output store undoes the permutation.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -43,11 +46,28 @@ namespace pkv {
 
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -59,19 +79,6 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t r) {
   return __half22float2(*reinterpret_cast<const __half2*>(&r));
 }
 
-__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
-  const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
-                            *reinterpret_cast<const __half2*>(&c));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-constexpr uint32_t kF16Magic2 = 0x64006400u;  // (1024.0h, 1024.0h)
-
 template <int FMT, int D>
 struct PackedTraits {
   static constexpr int KBITS = FMT == PKV_FMT_K4V4 ? 4 : 8;
@@ -80,25 +87,28 @@ struct PackedTraits {
   static constexpr int VB = D * VBITS / 8;
   static constexpr int NG = D / kGroup;      // affine groups per row
   static constexpr int MB = NG * 8;          // (scale, offset) bytes per (token, head)
+  static constexpr int NKC = KB / 16;        // 16-byte chunks per (token, head)
+  static constexpr int NVC = VB / 16;
+  static constexpr int NMC = MB / 16;        // = NG / 2: two groups' (s, o) per chunk
 };
 
-// B fragments of K for one group and one token (this lane's token of the n-tile):
-// k-step ks in {0,1} of the group gets (b[ks][0], b[ks][1]).
+// B fragments of K for one group and one token (this lane's token of the n-tile),
+// as fp16 subnormals: k-step ks in {0,1} of the group gets (b[ks][0], b[ks][1]).
 // 4-bit: word t of the group holds elements 8t..8t+7 (element n in bits 4n..4n+3).
 __device__ __forceinline__ void k_group_frags4(uint32_t w, uint32_t (&b)[2][2]) {
   const uint32_t w8 = w >> 8;
-  b[0][0] = (w & 0x000F000Fu) | kF16Magic2;   // elements 0, 4      : 1024 + c
-  b[0][1] = (w & 0x00F000F0u) | kF16Magic2;   // elements 1, 5      : 1024 + 16 c
-  b[1][0] = (w8 & 0x000F000Fu) | kF16Magic2;  // elements 2, 6
-  b[1][1] = (w8 & 0x00F000F0u) | kF16Magic2;  // elements 3, 7      : 1024 + 16 c
+  b[0][0] = w & 0x000F000Fu;   // elements 0, 4      : c
+  b[0][1] = w & 0x00F000F0u;   // elements 1, 5      : 16 c
+  b[1][0] = w8 & 0x000F000Fu;  // elements 2, 6
+  b[1][1] = w8 & 0x00F000F0u;  // elements 3, 7      : 16 c
 }
 
-// 8-bit: k-step ks uses word 4 ks + t of the group: elements 16 ks + 4t + j.
+// 8-bit: k-step ks uses word t of the group's chunk ks: elements 16 ks + 4t + j.
 __device__ __forceinline__ void k_group_frags8(uint32_t w0, uint32_t w1, uint32_t (&b)[2][2]) {
-  b[0][0] = __byte_perm(w0, 0x64646464u, 0x4140);  // (1024 + c0, 1024 + c1)
-  b[0][1] = __byte_perm(w0, 0x64646464u, 0x4342);  // (1024 + c2, 1024 + c3)
-  b[1][0] = __byte_perm(w1, 0x64646464u, 0x4140);
-  b[1][1] = __byte_perm(w1, 0x64646464u, 0x4342);
+  b[0][0] = __byte_perm(w0, 0u, 0x4140);  // (c0, c1)
+  b[0][1] = __byte_perm(w0, 0u, 0x4342);  // (c2, c3)
+  b[1][0] = __byte_perm(w1, 0u, 0x4140);
+  b[1][1] = __byte_perm(w1, 0u, 0x4342);
 }
 
 // Group-relative dims of the A (q) entries matching k_group_frags4/8, and whether the
@@ -117,46 +127,14 @@ __device__ __forceinline__ int k_dim(int t, int ks, int r, int hh, bool& div16) 
   }
 }
 
-// A fragments of V^T for one group, one 16-token chunk: the four code words of
-// tokens (2t, 2t+1, 2t+8, 2t+9) at this lane's word; returns raw (1024 + c) fp16
-// pairs a[mi][r] for M tile mi in {0,1}, register r in 0..3 (tokens pair 0: r 0,1;
-// pair 1: r 2,3; rows g: r 0,2; rows g+8: r 1,3).
-template <int VBITS>
-__device__ __forceinline__ void v_group_frags(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, int g,
-                                              uint32_t (&a)[2][4]) {
-  if constexpr (VBITS == 4) {
-    const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;  // half-word g&1 of each token's word
-    const uint32_t x01 = __byte_perm(w0, w1, sel);
-    const uint32_t x23 = __byte_perm(w2, w3, sel);
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
-      a[mi][0] = ((x01 >> (8 * mi)) & 0x000F000Fu) | kF16Magic2;      // nibble 2mi   (row g)
-      a[mi][1] = ((x01 >> (8 * mi + 4)) & 0x000F000Fu) | kF16Magic2;  // nibble 2mi+1 (row g+8)
-      a[mi][2] = ((x23 >> (8 * mi)) & 0x000F000Fu) | kF16Magic2;
-      a[mi][3] = ((x23 >> (8 * mi + 4)) & 0x000F000Fu) | kF16Magic2;
-    }
-  } else {
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
-      const int j0 = 2 * mi, j1 = 2 * mi + 1;  // bytes of the word: rows g and g+8
-      a[mi][0] = (__byte_perm(w0, w1, (uint32_t)(j0 | (j0 << 4) | ((4 + j0) << 8) | ((4 + j0) << 12))) & 0x00FF00FFu) | kF16Magic2;
-      a[mi][1] = (__byte_perm(w0, w1, (uint32_t)(j1 | (j1 << 4) | ((4 + j1) << 8) | ((4 + j1) << 12))) & 0x00FF00FFu) | kF16Magic2;
-      a[mi][2] = (__byte_perm(w2, w3, (uint32_t)(j0 | (j0 << 4) | ((4 + j0) << 8) | ((4 + j0) << 12))) & 0x00FF00FFu) | kF16Magic2;
-      a[mi][3] = (__byte_perm(w2, w3, (uint32_t)(j1 | (j1 << 4) | ((4 + j1) << 8) | ((4 + j1) << 12))) & 0x00FF00FFu) | kF16Magic2;
-    }
-  }
-}
-
-// Byte offset, inside one (token, head) V code row, of this lane's word for group grp.
-template <int VBITS>
-__device__ __forceinline__ int v_word_offset(int grp, int g) {
-  return VBITS == 4 ? 16 * grp + 4 * (g >> 1) : 32 * grp + 4 * g;
-}
-
-// Output dim of M tile mi of group grp, row half hh (0: row g, 1: row g+8).
+// Output dim of M tile mi of group grp, row half hh (0: row g, 1: row g+8).  The
+// A fragment of a 4-bit group comes from half-word g of its 16-byte chunk (dims
+// 4g..4g+3 of the group): tile 0 takes the low nibbles of its bytes (dims 4g, 4g+2),
+// tile 1 the high nibbles (dims 4g+1, 4g+3, read as 16c).  An 8-bit group spans two
+// chunks, one per tile; half-word g holds dims 2g and 2g+1 of the chunk.
 template <int VBITS>
 __device__ __forceinline__ int v_out_dim(int grp, int mi, int hh, int g) {
-  return VBITS == 4 ? 32 * grp + 8 * (g >> 1) + 4 * (g & 1) + 2 * mi + hh : 32 * grp + 4 * g + 2 * mi + hh;
+  return VBITS == 4 ? 32 * grp + 4 * g + mi + 2 * hh : 32 * grp + 16 * mi + 2 * g + hh;
 }
 
 // One stored tensor's region of a stage: byte offset, log2 of the box width, boxes
@@ -178,7 +156,8 @@ __device__ __forceinline__ int swz(const SwzRegion& z, int tok, int b) {
 __device__ __forceinline__ int ilog2i(int v) { return 31 - __clz(v); }
 
 // W128: every stored tensor's all-heads row is a multiple of 128 bytes, so every box
-// is 128 bytes wide; then all addressing below reduces to per-lane constants.
+// is 128 bytes wide; then every shared-memory address below is a per-lane constant
+// plus a per-chunk uniform offset plus an immediate.
 template <int FMT, int D, int G, bool W128>
 __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const DecodeParams P) {
   using Tr = PackedTraits<FMT, D>;
@@ -228,85 +207,153 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
 
   if (warp == NC) {
     // ----------------------------- producer ---------------------------------
+    // Lanes hold the info of a batch of 32 units; lane i issues every copy of unit
+    // i of the batch (one 3-D tensor copy per 16 tokens and stored tensor, plus q
+    // when the unit starts a sequence), so the tensor-map acquire fences of a unit
+    // run when its batch is read, ahead of its copies, in the thread that issues them.
     const bool use_stab = smem_table_entries(P) > 0;
     const uint64_t kv_policy = l2_policy_evict_first();
-    const int nboxes = (T / 16) * (zr[0].nx + zr[1].nx + zr[2].nx + zr[3].nx);
     int issued = 0;
     bool dead = false;
     for (int32_t ub = u0; ub < u1 && !dead; ub += 32) {
       const int32_t u = ub + lane;
-      const uint8_t* mapbase = nullptr;
-      const uint8_t* qsrc = nullptr;
-      int y0 = 0, ok = 0;
+      const uint8_t* map = nullptr;  // tensor maps of the unit's slab (kind k at + 128 k)
+      const uint8_t* qsrc = nullptr; // q of its sequence when the unit starts a CTA's segment
+      int y0 = 0, ok = 0;            // first slab row of the unit; row valid
       if (u < u1) {
-        const int b = find_seq(UP, B, u);
-        if (u == u0 || u == UP[b]) qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)b * P.Hq * D);
-        const int32_t tok0 = (u - UP[b]) * T;
-        const int j = tok0 / kBlockTokens, slot0 = tok0 % kBlockTokens;
-        const int32_t row = P.bt[(size_t)b * P.max_blocks + j];
+        const int bb = find_seq(UP, B, u);
+        if (u == u0 || u == UP[bb]) qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)bb * P.Hq * D);
+        const int32_t t0 = (u - UP[bb]) * T;
+        const int j = t0 / kBlockTokens, slot0 = t0 % kBlockTokens;
+        const int32_t row = P.bt[(size_t)bb * P.max_blocks + j];
         if (row >= 0 && (int64_t)row < P.lv.rows_capacity) {
           const int32_t slab = row / P.lv.slab_blocks;
           const int32_t r = row - slab * P.lv.slab_blocks;
-          const uint8_t* ent0 = use_stab ? tab[(size_t)slab * P.lv.n_kinds]
-                                         : P.lv.tab.base[(size_t)slab * P.lv.tab.stride];
-          mapbase = ent0 + P.lv.map_delta;
+          const uint8_t* ent0 =
+              use_stab ? tab[(size_t)slab * P.lv.n_kinds] : P.lv.tab.base[(size_t)slab * P.lv.tab.stride];
+          map = ent0 + P.lv.map_delta;
           y0 = r * kBlockTokens + slot0;
           ok = 1;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tensormap_acquire(map + k * 128);
         } else {
           atomicOr(err, ERR_ROW);
         }
       }
       const int cnt = min(32, u1 - ub);
-      for (int i = 0; i < cnt; ++i) {
-        const uint8_t* mb = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)mapbase, i);
-        const uint8_t* qs = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)qsrc, i);
-        const int yi = __shfl_sync(0xffffffffu, y0, i);
-        const int oki = __shfl_sync(0xffffffffu, ok, i);
-        const int s = issued % NS;
-        if (lane == 0) {
-          if (issued >= NS && !mbar_wait_bounded(&empty[s], ((issued / NS) & 1) ^ 1, err)) dead = true;
-          if (!dead)
-            mbar_arrive_expect_tx(&full[s], (oki ? (uint32_t)(T * (KR + VR + 2 * MR)) : 0u) + (qs ? (uint32_t)QB : 0u));
-        }
-        dead = __shfl_sync(0xffffffffu, dead, 0);
-        if (dead) break;
-        __syncwarp();
-        uint8_t* st = stages + (size_t)s * P.stage_bytes;
-        if (qs && lane == 31) bulk_g2s(st + offQ, qs, (uint32_t)QB, &full[s]);
-        if (oki) {
-          for (int c = lane; c < nboxes; c += 32) {
-            // box c -> (kind, row of boxes cy, column cx)
-            int kind = 0, rem = c;
-            while (rem >= (T / 16) * zr[kind].nx) {
-              rem -= (T / 16) * zr[kind].nx;
-              ++kind;
+      for (int i = 0; i < cnt; ++i, ++issued) {
+        int bad = 0;
+        if (lane == i) {
+          const int s = issued % NS;
+          if (issued >= NS && !mbar_wait_bounded(&empty[s], ((issued / NS) & 1) ^ 1, err)) {
+            bad = 1;
+          } else {
+            mbar_arrive_expect_tx(&full[s], (ok ? (uint32_t)(T * (KR + VR + 2 * MR)) : 0u) + (qsrc ? (uint32_t)QB : 0u));
+            uint8_t* st = stages + (size_t)s * P.stage_bytes;
+            if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, &full[s]);
+            if (ok) {
+              for (int cy = 0; cy < T / 16; ++cy)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  tma_load_3d(st + zr[k].off + ((cy * zr[k].nx) << (zr[k].lg + 4)), map + k * 128, 0, y0 + 16 * cy,
+                              0, &full[s], kv_policy);
             }
-            const int cy = rem / zr[kind].nx, cx = rem - cy * zr[kind].nx;
-            const uint8_t* map = mb + kind * 128;
-            tensormap_acquire(map);
-            tma_load_2d(st + zr[kind].off + ((cy * zr[kind].nx + cx) << (zr[kind].lg + 4)), map,
-                        cx << zr[kind].lg, yi + 16 * cy, &full[s], kv_policy);
           }
         }
-        ++issued;
+        if (__any_sync(0xffffffffu, bad)) {
+          dead = true;
+          break;
+        }
       }
     }
+    // After a timeout, leave no copy in flight into a stage that is no longer waited on.
     if (lane == 0) {
       const int first = issued > NS ? issued - NS : 0;
-      for (int n = first; n < issued; ++n) mbar_wait_bounded(&full[n % NS], (n / NS) & 1, err);
+      for (int k = first; k < issued; ++k) mbar_wait_bounded(&full[k % NS], (k / NS) & 1, err);
     }
     return;
   }
 
   // ------------------------------ consumers ---------------------------------
+  constexpr int NKC = Tr::NKC, NVC = Tr::NVC, NMC = Tr::NMC;
   const int h = warp;
   const int g = lane >> 2, t = lane & 3;
   float* qs = qscr + (size_t)warp * G * D;
   uint32_t qa[NG][2][2];  // A fragments per group, k-step, register (rows g; rows g+8 zero)
-  float qbias[NG], qsum[NG];
-  float o[NG][2][4];      // O^T accumulators: group, M tile, fragment
+  float qsum[NG];         // 2^-24 * sum over the group of the q~ values the MMA sees
+  float o[NG][2][4];      // O^T accumulators, in units of 2^-24: group, M tile, fragment
+  float corr[NG];         // sum_t p_t o_t for head g and each group, this lane's tokens
   float m_run = -INFINITY, l_run = 0.f;
   bool dead = false;
+  const float scale24 = P.scale_log2 * 16777216.0f;
+
+  // Shared-memory addresses.  ldmatrix: lane 8i + r gives row r of matrix i.  K codes
+  // (non-transposed) and V codes (transposed) are read as 8 tokens x one 16-byte
+  // chunk per matrix; a K matrix for (token half j, chunk c) hands lane (g, t) word t
+  // of token 8j + g, a V matrix for (token half p, chunk c) hands it half-word g of
+  // tokens 8p + 2t and 8p + 2t + 1.  With NKC == 2 one x4 load covers both halves
+  // (matrix i = (j = i / 2, c = i % 2)); otherwise x4 load (j, cs) covers chunks
+  // 4cs..4cs+3 of half j.  The (scale, offset) chunks are read 16 bytes per token.
+  const int li = lane >> 3, lr = lane & 7;
+  constexpr int KCS = NKC >= 4 ? NKC / 4 : 1, VCS = NVC >= 4 ? NVC / 4 : 1;
+  constexpr int NMX = NMC >= 2 ? NMC : 2;
+  int kofs[KCS], vofs[VCS], mofs[NMX];
+  int KSTEP = 0, VSTEP = 0, MSTEP = 0;
+  const int VMD = zr[3].off - zr[2].off;
+  if constexpr (W128) {
+    // 128-byte rows: box row r sits at r * 128 and its chunk c at c ^ (r & 7).  A
+    // lane's rows differ only by multiples of 8 (same key), so each load is a
+    // per-lane constant + the chunk's uniform offset + an immediate.  For the
+    // (scale, offset) reads the row key is 2t ^ e and the chunk cm of the head is
+    // hb + cm = hb ^ cm (hb is a multiple of NMC), so the address depends on cm ^ e.
+#pragma unroll
+    for (int cs = 0; cs < KCS; ++cs) {
+      const int c = NKC == 2 ? (li & 1) : 4 * cs + li;
+      const int row = NKC == 2 ? 8 * (li >> 1) + lr : lr;
+      const int byte = h * Tr::KB + 16 * c;
+      kofs[cs] = zr[0].off + (byte >> 7) * 2048 + row * 128 + ((((byte >> 4) & 7) ^ lr) << 4);
+    }
+#pragma unroll
+    for (int cs = 0; cs < VCS; ++cs) {
+      const int c = NVC == 2 ? (li & 1) : 4 * cs + li;
+      const int row = NVC == 2 ? 8 * (li >> 1) + lr : lr;
+      const int byte = h * Tr::VB + 16 * c;
+      vofs[cs] = zr[1].off + (byte >> 7) * 2048 + row * 128 + ((((byte >> 4) & 7) ^ lr) << 4);
+    }
+    const int mb = h * Tr::MB;
+#pragma unroll
+    for (int x = 0; x < NMX; ++x)
+      mofs[x] = zr[2].off + (mb >> 7) * 2048 + 2 * t * 128 + (((((mb >> 4) & 7) ^ (2 * t)) ^ x) << 4);
+    KSTEP = zr[0].nx * 2048;
+    VSTEP = zr[1].nx * 2048;
+    MSTEP = zr[2].nx * 2048;
+  }
+  auto k_addr = [&](uint32_t sb, int kc, int j, int cs) -> uint32_t {
+    if constexpr (W128) {
+      return sb + kc * KSTEP + kofs[cs] + (NKC == 2 ? 0 : 1024 * j);
+    } else {
+      const int c = NKC == 2 ? (li & 1) : 4 * cs + li;
+      const int row = NKC == 2 ? 8 * (li >> 1) + lr : 8 * j + lr;
+      return sb + swz(zr[0], kc * 16 + row, h * Tr::KB + 16 * c);
+    }
+  };
+  auto v_addr = [&](uint32_t sb, int kc, int p, int cs) -> uint32_t {
+    if constexpr (W128) {
+      return sb + kc * VSTEP + vofs[cs] + (NVC == 2 ? 0 : 1024 * p);
+    } else {
+      const int c = NVC == 2 ? (li & 1) : 4 * cs + li;
+      const int row = NVC == 2 ? 8 * (li >> 1) + lr : 8 * p + lr;
+      return sb + swz(zr[1], kc * 16 + row, h * Tr::VB + 16 * c);
+    }
+  };
+  // (scale, offset) of groups 2cm, 2cm+1 for token 16kc + 8j + 2t + e; kind 2 = K, 3 = V
+  auto m_addr = [&](uint32_t sb, int kind, int kc, int j, int e, int cm) -> uint32_t {
+    if constexpr (W128) {
+      return sb + (kind == 3 ? VMD : 0) + kc * MSTEP + mofs[cm ^ e] + 1024 * j + 128 * e;
+    } else {
+      return sb + swz(zr[kind], kc * 16 + 8 * j + 2 * t + e, h * Tr::MB + 16 * cm);
+    }
+  };
 
   int b = find_seq(UP, B, u0);
   int n = 0;
@@ -316,11 +363,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
     const bool seg_end = (u == u1 - 1) || (u == UP[b + 1] - 1);
     if (seg_start) {
 #pragma unroll
-      for (int grp = 0; grp < NG; ++grp)
+      for (int grp = 0; grp < NG; ++grp) {
+        corr[grp] = 0.f;
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
           for (int i = 0; i < 4; ++i) o[grp][mi][i] = 0.f;
+      }
       m_run = -INFINITY;
       l_run = 0.f;
     }
@@ -347,121 +396,79 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
       }
 #pragma unroll
       for (int grp = 0; grp < NG; ++grp) {
-        float bsum = 0.f, tsum = 0.f;
+        float tsum = 0.f;
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             float v[2];
+            bool d16 = false;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-              bool d16;
               const int dd = 32 * grp + k_dim<Tr::KBITS>(t, ks, r, hh, d16);
               const float qv = g < G ? qs[g * D + dd] * P.inv_sqrt_d : 0.f;
               v[hh] = d16 ? qv * 0.0625f : qv;
             }
             qa[grp][ks][r] = pack_f16x2(v[0], v[1]);
             const float2 back = unpack_f16x2(qa[grp][ks][r]);  // the values the MMA sees
-            bsum += back.x + back.y;
-            bool d16;
-            (void)k_dim<Tr::KBITS>(t, ks, r, 0, d16);
             tsum += d16 ? 16.f * (back.x + back.y) : (back.x + back.y);
           }
-        bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
-        bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
         tsum += __shfl_xor_sync(0xffffffffu, tsum, 1);
         tsum += __shfl_xor_sync(0xffffffffu, tsum, 2);
-        qbias[grp] = 1024.f * bsum;
-        qsum[grp] = tsum;
+        qsum[grp] = tsum * 5.9604644775390625e-08f;  // 2^-24
       }
       __syncwarp();
     }
     if (!dead) {
-      // Fast-path addressing (W128).  A lane touches token rows whose 128-byte
-      // swizzle key is fixed: K code rows 8j+g (key g), meta and V rows 8p+2t+e
-      // (key 2t^e).  base = region + head's box column + first row (+ lane bytes);
-      // key = (head's chunk ^ row key) << 4.  Chunk offsets inside the row are
-      // compile-time and enter through one XOR with the key.
-      const int KBASE = zr[0].off + ((h * Tr::KB) >> 7) * 2048 + g * 128 + 4 * t;
-      const int KKEY = ((((h * Tr::KB) >> 4) & 7) ^ g) << 4;
-      const int MKEY = ((((h * Tr::MB) >> 4) & 7) ^ (2 * t)) << 4;
-      const int KMBASE = zr[2].off + ((h * Tr::MB) >> 7) * 2048 + 2 * t * 128;
-      const int VMBASE = zr[3].off + ((h * Tr::MB) >> 7) * 2048 + 2 * t * 128;
-      const int VBASE = zr[1].off + ((h * Tr::VB) >> 7) * 2048 + 2 * t * 128 +
-                        (Tr::VBITS == 4 ? 4 * (g >> 1) : 4 * (g & 3));
-      const int VKEY = (((((h * Tr::VB) >> 4) & 7) ^ (2 * t)) << 4) ^ (Tr::VBITS == 8 ? 16 * (g >> 2) : 0);
+      const uint32_t sb = smem_u32(st);
       for (int kc = 0; kc * 16 < nv; ++kc) {
-        // ---- logits for 16 tokens: n-tiles 2kc, 2kc+1 ----
-        float x[2][2];
-        if constexpr (W128) {
-          const uint8_t* kq = st + KBASE + kc * zr[0].nx * 2048;
-          const uint8_t* km = st + KMBASE + kc * zr[2].nx * 2048;
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            float sa0 = 0.f, sa1 = 0.f;
-#pragma unroll
-            for (int gp = 0; gp < NG / 2; ++gp) {
-              // (scale, offset) of groups 2gp, 2gp+1 for tokens 8j+2t (e=0) and 8j+2t+1 (e=1)
-              const int moc = 16 * gp;
-              const float4 me0 = *reinterpret_cast<const float4*>(km + 1024 * j + (moc >> 7) * 2048 + (MKEY ^ (moc & 112)));
-              const float4 me1 =
-                  *reinterpret_cast<const float4*>(km + 1024 * j + 128 + (moc >> 7) * 2048 + (MKEY ^ ((moc & 112) ^ 16)));
-#pragma unroll
-              for (int q2 = 0; q2 < 2; ++q2) {
-                const int grp = 2 * gp + q2;
-                const int oc = grp * (kGroup * Tr::KBITS / 8);
-                uint32_t bfr[2][2];
-                if constexpr (Tr::KBITS == 4) {
-                  k_group_frags4(*reinterpret_cast<const uint32_t*>(kq + 1024 * j + (oc >> 7) * 2048 + (KKEY ^ (oc & 112))),
-                                 bfr);
-                } else {
-                  k_group_frags8(
-                      *reinterpret_cast<const uint32_t*>(kq + 1024 * j + (oc >> 7) * 2048 + (KKEY ^ (oc & 112))),
-                      *reinterpret_cast<const uint32_t*>(kq + 1024 * j + ((oc + 16) >> 7) * 2048 +
-                                                         (KKEY ^ ((oc + 16) & 112))),
-                      bfr);
-                }
-                float cacc[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_f16_16816(cacc, qa[grp][0][0], 0u, qa[grp][0][1], 0u, bfr[0][0], bfr[0][1]);
-                mma_f16_16816(cacc, qa[grp][1][0], 0u, qa[grp][1][1], 0u, bfr[1][0], bfr[1][1]);
-                const float s0 = q2 ? me0.z : me0.x, o0 = q2 ? me0.w : me0.y;
-                const float s1 = q2 ? me1.z : me1.x, o1 = q2 ? me1.w : me1.y;
-                sa0 = fmaf(s0, cacc[0] - qbias[grp], fmaf(o0, qsum[grp], sa0));
-                sa1 = fmaf(s1, cacc[1] - qbias[grp], fmaf(o1, qsum[grp], sa1));
-              }
-            }
-            const int tk = kc * 16 + 8 * j + 2 * t;
-            x[j][0] = tk < nv ? sa0 * P.scale_log2 : -INFINITY;
-            x[j][1] = tk + 1 < nv ? sa1 * P.scale_log2 : -INFINITY;
-          }
+        // ---- logits for 16 tokens: n-tiles (token halves) j = 0, 1 ----
+        uint32_t kw[2][NKC];  // word t of token 16kc + 8j + g, chunk c
+        if constexpr (NKC == 2) {
+          uint32_t r4[4];
+          ldsm4(k_addr(sb, kc, 0, 0), r4);
+          kw[0][0] = r4[0];
+          kw[0][1] = r4[1];
+          kw[1][0] = r4[2];
+          kw[1][1] = r4[3];
         } else {
 #pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int cs = 0; cs < KCS; ++cs) {
+              uint32_t r4[4];
+              ldsm4(k_addr(sb, kc, j, cs), r4);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) kw[j][4 * cs + m] = r4[m];
+            }
+        }
+        float x[2][2];
+#pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const int tb = kc * 16 + 8 * j;  // first token of the n-tile
           float sa0 = 0.f, sa1 = 0.f;
 #pragma unroll
-          for (int grp = 0; grp < NG; ++grp) {
-            uint32_t bfr[2][2];
-            const int kb = h * Tr::KB + grp * (kGroup * Tr::KBITS / 8) + 4 * t;
-            if constexpr (Tr::KBITS == 4) {
-              k_group_frags4(*reinterpret_cast<const uint32_t*>(st + swz(zr[0], tb + g, kb)), bfr);
-            } else {
-              k_group_frags8(*reinterpret_cast<const uint32_t*>(st + swz(zr[0], tb + g, kb)),
-                             *reinterpret_cast<const uint32_t*>(st + swz(zr[0], tb + g, kb + 16)), bfr);
+          for (int cm = 0; cm < NMC; ++cm) {
+            const float4 m0 = lds128(m_addr(sb, 2, kc, j, 0, cm));  // token 8j + 2t
+            const float4 m1 = lds128(m_addr(sb, 2, kc, j, 1, cm));  // token 8j + 2t + 1
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+              const int grp = 2 * cm + q2;
+              uint32_t bfr[2][2];
+              if constexpr (Tr::KBITS == 4) {
+                k_group_frags4(kw[j][grp], bfr);
+              } else {
+                k_group_frags8(kw[j][2 * grp], kw[j][2 * grp + 1], bfr);
+              }
+              float cacc[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_f16_16816(cacc, qa[grp][0][0], 0u, qa[grp][0][1], 0u, bfr[0][0], bfr[0][1]);
+              mma_f16_16816(cacc, qa[grp][1][0], 0u, qa[grp][1][1], 0u, bfr[1][0], bfr[1][1]);
+              sa0 = fmaf(q2 ? m0.z : m0.x, cacc[0], fmaf(q2 ? m0.w : m0.y, qsum[grp], sa0));
+              sa1 = fmaf(q2 ? m1.z : m1.x, cacc[1], fmaf(q2 ? m1.w : m1.y, qsum[grp], sa1));
             }
-            float cacc[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_f16_16816(cacc, qa[grp][0][0], 0u, qa[grp][0][1], 0u, bfr[0][0], bfr[0][1]);
-            mma_f16_16816(cacc, qa[grp][1][0], 0u, qa[grp][1][1], 0u, bfr[1][0], bfr[1][1]);
-            const int mbo = h * Tr::MB + 8 * grp;
-            const float2 m0 = *reinterpret_cast<const float2*>(st + swz(zr[2], tb + 2 * t, mbo));
-            const float2 m1 = *reinterpret_cast<const float2*>(st + swz(zr[2], tb + 2 * t + 1, mbo));
-            sa0 = fmaf(m0.x, cacc[0] - qbias[grp], fmaf(m0.y, qsum[grp], sa0));
-            sa1 = fmaf(m1.x, cacc[1] - qbias[grp], fmaf(m1.y, qsum[grp], sa1));
           }
-          const int tk = tb + 2 * t;
-          x[j][0] = tk < nv ? sa0 * P.scale_log2 : -INFINITY;
-          x[j][1] = tk + 1 < nv ? sa1 * P.scale_log2 : -INFINITY;
-        }
+          const int tk = kc * 16 + 8 * j + 2 * t;
+          x[j][0] = tk < nv ? sa0 * scale24 : -INFINITY;
+          x[j][1] = tk + 1 < nv ? sa1 * scale24 : -INFINITY;
         }
         // ---- online softmax for head g ----
         float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
@@ -469,9 +476,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         const bool grow = mx > m_run;
         if (__any_sync(0xffffffffu, grow)) {
-          const float alpha = grow ? exp2f(m_run - mx) : 1.0f;
+          const float alpha = grow ? ex2(m_run - mx) : 1.0f;
           if (grow) m_run = mx;
           l_run *= alpha;
+#pragma unroll
+          for (int grp = 0; grp < NG; ++grp) corr[grp] *= alpha;
           const float ae = __shfl_sync(0xffffffffu, alpha, 8 * t);
           const float ao = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
 #pragma unroll
@@ -484,82 +493,70 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
               o[grp][mi][3] *= ao;
             }
         }
-        const float p00 = exp2f(x[0][0] - m_run), p01 = exp2f(x[0][1] - m_run);
-        const float p10 = exp2f(x[1][0] - m_run), p11 = exp2f(x[1][1] - m_run);
-        l_run += (p00 + p01) + (p10 + p11);
-        const uint32_t pb0 = pack_f16x2(p00, p01), pb1 = pack_f16x2(p10, p11);
-        // ---- O^T += V^T P^T over these 16 tokens ----
-        const int t0 = kc * 16 + 2 * t;
-        if constexpr (W128) {
-          const uint8_t* vq = st + VBASE + kc * zr[1].nx * 2048;
-          const uint8_t* vm = st + VMBASE + kc * zr[3].nx * 2048;
+        float p[2][2];
 #pragma unroll
-          for (int gp = 0; gp < NG / 2; ++gp) {
-            // (scale, offset) of groups 2gp, 2gp+1 for tokens 2t+e+8p
-            const int moc = 16 * gp;
-            float4 mv[2][2];
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) p[j][e] = ex2(x[j][e] - m_run);
+        l_run += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+        // ---- O^T += V^T (P S)^T over these 16 tokens; offsets into corr ----
+        uint32_t vx[2][NVC];  // half-word g of tokens 16kc + 8p + 2t, +1; chunk c
+        if constexpr (NVC == 2) {
+          uint32_t r4[4];
+          ldsm4_t(v_addr(sb, kc, 0, 0), r4);
+          vx[0][0] = r4[0];
+          vx[0][1] = r4[1];
+          vx[1][0] = r4[2];
+          vx[1][1] = r4[3];
+        } else {
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+            for (int cs = 0; cs < VCS; ++cs) {
+              uint32_t r4[4];
+              ldsm4_t(v_addr(sb, kc, pp, cs), r4);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) vx[pp][4 * cs + m] = r4[m];
+            }
+        }
+#pragma unroll
+        for (int cm = 0; cm < NMC; ++cm) {
+          float4 mv[2][2];  // token 8pp + 2t + e
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) mv[pp][e] = lds128(m_addr(sb, 3, kc, pp, e, cm));
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int grp = 2 * cm + q2;
+            float sv[2][2], ov[2][2];
 #pragma unroll
             for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
-              for (int e = 0; e < 2; ++e)
-                mv[pp][e] = *reinterpret_cast<const float4*>(vm + 1024 * pp + 128 * e + (moc >> 7) * 2048 +
-                                                             (MKEY ^ ((moc & 112) ^ (16 * e))));
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-              const int grp = 2 * gp + q2;
-              const int oc = Tr::VBITS == 4 ? 16 * grp : 32 * grp;
-              uint32_t w[2][2];
-#pragma unroll
-              for (int pp = 0; pp < 2; ++pp)
-#pragma unroll
-                for (int e = 0; e < 2; ++e)
-                  w[pp][e] = *reinterpret_cast<const uint32_t*>(vq + 1024 * pp + 128 * e + (oc >> 7) * 2048 +
-                                                                (VKEY ^ ((oc & 112) ^ (16 * e))));
-              const float2 s0 = q2 ? make_float2(mv[0][0].z, mv[0][0].w) : make_float2(mv[0][0].x, mv[0][0].y);
-              const float2 s1 = q2 ? make_float2(mv[0][1].z, mv[0][1].w) : make_float2(mv[0][1].x, mv[0][1].y);
-              const float2 s2 = q2 ? make_float2(mv[1][0].z, mv[1][0].w) : make_float2(mv[1][0].x, mv[1][0].y);
-              const float2 s3 = q2 ? make_float2(mv[1][1].z, mv[1][1].w) : make_float2(mv[1][1].x, mv[1][1].y);
-              const uint32_t sc01 = pack_f16x2(s0.x, s1.x), of01 = pack_f16x2(s0.y, s1.y);
-              const uint32_t sc23 = pack_f16x2(s2.x, s3.x), of23 = pack_f16x2(s2.y, s3.y);
-              uint32_t a[2][4];
-              v_group_frags<Tr::VBITS>(w[0][0], w[0][1], w[1][0], w[1][1], g, a);
+              for (int e = 0; e < 2; ++e) {
+                sv[pp][e] = q2 ? mv[pp][e].z : mv[pp][e].x;
+                ov[pp][e] = q2 ? mv[pp][e].w : mv[pp][e].y;
+              }
+            const uint32_t pb0 = pack_f16x2(p[0][0] * sv[0][0], p[0][1] * sv[0][1]);
+            const uint32_t pb1 = pack_f16x2(p[1][0] * sv[1][0], p[1][1] * sv[1][1]);
+            corr[grp] = fmaf(p[0][0], ov[0][0],
+                             fmaf(p[0][1], ov[0][1], fmaf(p[1][0], ov[1][0], fmaf(p[1][1], ov[1][1], corr[grp]))));
+            if constexpr (Tr::VBITS == 4) {
+              const uint32_t x01 = vx[0][grp], x23 = vx[1][grp];
+              const uint32_t y01 = x01 >> 8, y23 = x23 >> 8;
+              mma_f16_16816(o[grp][0], x01 & 0x000F000Fu, y01 & 0x000F000Fu, x23 & 0x000F000Fu, y23 & 0x000F000Fu,
+                            pb0, pb1);
+              mma_f16_16816(o[grp][1], x01 & 0x00F000F0u, y01 & 0x00F000F0u, x23 & 0x00F000F0u, y23 & 0x00F000F0u,
+                            pb0, pb1);
+            } else {
 #pragma unroll
               for (int mi = 0; mi < 2; ++mi) {
-                const uint32_t d0 = hfma2_u32(hsub2_u32(a[mi][0], kF16Magic2), sc01, of01);
-                const uint32_t d1 = hfma2_u32(hsub2_u32(a[mi][1], kF16Magic2), sc01, of01);
-                const uint32_t d2 = hfma2_u32(hsub2_u32(a[mi][2], kF16Magic2), sc23, of23);
-                const uint32_t d3 = hfma2_u32(hsub2_u32(a[mi][3], kF16Magic2), sc23, of23);
-                mma_f16_16816(o[grp][mi], d0, d1, d2, d3, pb0, pb1);
+                const uint32_t x01 = vx[0][2 * grp + mi], x23 = vx[1][2 * grp + mi];
+                mma_f16_16816(o[grp][mi], __byte_perm(x01, 0u, 0x4240), __byte_perm(x01, 0u, 0x4341),
+                              __byte_perm(x23, 0u, 0x4240), __byte_perm(x23, 0u, 0x4341), pb0, pb1);
               }
             }
           }
-        } else {
-#pragma unroll
-        for (int grp = 0; grp < NG; ++grp) {
-          const int vb = h * Tr::VB + v_word_offset<Tr::VBITS>(grp, g);
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(st + swz(zr[1], t0, vb));
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(st + swz(zr[1], t0 + 1, vb));
-          const uint32_t w2 = *reinterpret_cast<const uint32_t*>(st + swz(zr[1], t0 + 8, vb));
-          const uint32_t w3 = *reinterpret_cast<const uint32_t*>(st + swz(zr[1], t0 + 9, vb));
-          const int mbo = h * Tr::MB + 8 * grp;
-          const float2 s0 = *reinterpret_cast<const float2*>(st + swz(zr[3], t0, mbo));
-          const float2 s1 = *reinterpret_cast<const float2*>(st + swz(zr[3], t0 + 1, mbo));
-          const float2 s2 = *reinterpret_cast<const float2*>(st + swz(zr[3], t0 + 8, mbo));
-          const float2 s3 = *reinterpret_cast<const float2*>(st + swz(zr[3], t0 + 9, mbo));
-          const uint32_t sc01 = pack_f16x2(s0.x, s1.x), of01 = pack_f16x2(s0.y, s1.y);
-          const uint32_t sc23 = pack_f16x2(s2.x, s3.x), of23 = pack_f16x2(s2.y, s3.y);
-          uint32_t a[2][4];
-          v_group_frags<Tr::VBITS>(w0, w1, w2, w3, g, a);
-#pragma unroll
-          for (int mi = 0; mi < 2; ++mi) {
-            // v = s * c + o in fp16, with c = (1024 + c) - 1024 exact
-            const uint32_t d0 = hfma2_u32(hsub2_u32(a[mi][0], kF16Magic2), sc01, of01);
-            const uint32_t d1 = hfma2_u32(hsub2_u32(a[mi][1], kF16Magic2), sc01, of01);
-            const uint32_t d2 = hfma2_u32(hsub2_u32(a[mi][2], kF16Magic2), sc23, of23);
-            const uint32_t d3 = hfma2_u32(hsub2_u32(a[mi][3], kF16Magic2), sc23, of23);
-            mma_f16_16816(o[grp][mi], d0, d1, d2, d3, pb0, pb1);
-          }
-        }
         }
       }
       __syncwarp();
@@ -571,6 +568,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
       l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
       const float me = __shfl_sync(0xffffffffu, m_run, 8 * t), mo = __shfl_sync(0xffffffffu, m_run, 8 * t + 4);
       const float le = __shfl_sync(0xffffffffu, l_run, 8 * t), lo = __shfl_sync(0xffffffffu, l_run, 8 * t + 4);
+      // Offsets term of head g summed over the row's four lanes, then moved to the
+      // lanes that hold heads 2t and 2t+1 in the O^T fragments.
+      float ce[NG], co[NG];
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp) {
+        float c = corr[grp];
+        c += __shfl_xor_sync(0xffffffffu, c, 1);
+        c += __shfl_xor_sync(0xffffffffu, c, 2);
+        ce[grp] = __shfl_sync(0xffffffffu, c, 8 * t);
+        co[grp] = __shfl_sync(0xffffffffu, c, 8 * t + 4);
+      }
+      // 2^24 undoes the subnormal code scale; tile 1 of a 4-bit group read 16c.
+      const float fs[2] = {16777216.0f, Tr::VBITS == 4 ? 1048576.0f : 16777216.0f};
       const int he = 2 * t, ho = 2 * t + 1;
       const int32_t c_lo = UP[b] / C, c_hi = (UP[b + 1] - 1) / C;
       if (c_lo == c_hi) {
@@ -583,12 +593,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
           for (int mi = 0; mi < 2; ++mi) {
             const int d0 = v_out_dim<Tr::VBITS>(grp, mi, 0, g), d1 = v_out_dim<Tr::VBITS>(grp, mi, 1, g);
             if (he < G) {
-              oe[d0] = f2bf(o[grp][mi][0] * ie);
-              oe[d1] = f2bf(o[grp][mi][2] * ie);
+              oe[d0] = f2bf(fmaf(o[grp][mi][0], fs[mi], ce[grp]) * ie);
+              oe[d1] = f2bf(fmaf(o[grp][mi][2], fs[mi], ce[grp]) * ie);
             }
             if (ho < G) {
-              oo[d0] = f2bf(o[grp][mi][1] * io);
-              oo[d1] = f2bf(o[grp][mi][3] * io);
+              oo[d0] = f2bf(fmaf(o[grp][mi][1], fs[mi], co[grp]) * io);
+              oo[d1] = f2bf(fmaf(o[grp][mi][3], fs[mi], co[grp]) * io);
             }
           }
       } else {
@@ -608,12 +618,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
           for (int mi = 0; mi < 2; ++mi) {
             const int d0 = v_out_dim<Tr::VBITS>(grp, mi, 0, g), d1 = v_out_dim<Tr::VBITS>(grp, mi, 1, g);
             if (he < G) {
-              pe[kPartialHeader + d0] = o[grp][mi][0];
-              pe[kPartialHeader + d1] = o[grp][mi][2];
+              pe[kPartialHeader + d0] = fmaf(o[grp][mi][0], fs[mi], ce[grp]);
+              pe[kPartialHeader + d1] = fmaf(o[grp][mi][2], fs[mi], ce[grp]);
             }
             if (ho < G) {
-              po[kPartialHeader + d0] = o[grp][mi][1];
-              po[kPartialHeader + d1] = o[grp][mi][3];
+              po[kPartialHeader + d0] = fmaf(o[grp][mi][1], fs[mi], co[grp]);
+              po[kPartialHeader + d1] = fmaf(o[grp][mi][3], fs[mi], co[grp]);
             }
           }
       }

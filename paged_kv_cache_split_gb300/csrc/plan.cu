@@ -12,7 +12,6 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
   if (fb.k == 0 || hkv < 1 || hkv > 8 || B < 1 || B > 4096) return false;
   const bool packed = fmt != PKV_FMT_BF16;
   const size_t meta = packed ? (size_t)(D / kGroup) * 8 : 0;
-  const size_t per_token = (size_t)hkv * ((size_t)(fb.k + fb.v) * D / 8 + 2 * meta);
   const size_t budget = 232448;  // 227 KB opt-in shared memory per block on sm_100-class parts
   size_t fixed = (size_t)(2 * B + 1 + 4) * 4 + 16 + 128 + 1024 * sizeof(void*);  // + staged slab table (kSmemTableEntries)
   if (packed) fixed += (size_t)hkv * G * D * 4;

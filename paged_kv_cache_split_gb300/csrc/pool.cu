@@ -132,11 +132,14 @@ static bool encode_group_maps(const pkv_pool* p, uint8_t* group, std::vector<CUt
                                     : box == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                     : box == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
                                                 : CU_TENSOR_MAP_SWIZZLE_NONE;
-      const cuuint64_t dims[2] = {(cuuint64_t)row, (cuuint64_t)p->cfg.slab_blocks * kBlockTokens};
-      const cuuint64_t strides[1] = {(cuuint64_t)row};
-      const cuuint32_t boxd[2] = {(cuuint32_t)box, 16u};
-      const cuuint32_t estr[2] = {1u, 1u};
-      if (enc(&maps[(size_t)l * K + k], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, group + off, dims, strides, boxd, estr,
+      // 3-D view [column block][token][W bytes] of the [token][row] tensor: one copy
+      // moves 16 tokens of the whole row and lands as nx boxes of 16 x W bytes.
+      const cuuint64_t nx = (cuuint64_t)(row / box);
+      const cuuint64_t dims[3] = {(cuuint64_t)box, (cuuint64_t)p->cfg.slab_blocks * kBlockTokens, nx};
+      const cuuint64_t strides[2] = {(cuuint64_t)row, (cuuint64_t)box};
+      const cuuint32_t boxd[3] = {(cuuint32_t)box, 16u, (cuuint32_t)nx};
+      const cuuint32_t estr[3] = {1u, 1u, 1u};
+      if (enc(&maps[(size_t)l * K + k], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, group + off, dims, strides, boxd, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
