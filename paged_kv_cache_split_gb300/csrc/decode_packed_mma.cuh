@@ -214,6 +214,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
     const bool use_stab = smem_table_entries(P) > 0;
     const uint64_t kv_policy = l2_policy_evict_first();
     int issued = 0;
+    int ps = 0;           // stage of unit `issued`
+    uint32_t pphase = 0;  // parity of that stage's current round
     bool dead = false;
     for (int32_t ub = u0; ub < u1 && !dead; ub += 32) {
       const int32_t u = ub + lane;
@@ -241,11 +243,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
         }
       }
       const int cnt = min(32, u1 - ub);
-      for (int i = 0; i < cnt; ++i, ++issued) {
+      for (int i = 0; i < cnt; ++i, ++issued, ps = (ps + 1 == NS) ? 0 : ps + 1, pphase ^= (ps == 0)) {
         int bad = 0;
         if (lane == i) {
-          const int s = issued % NS;
-          if (issued >= NS && !mbar_wait_bounded(&empty[s], ((issued / NS) & 1) ^ 1, err)) {
+          const int s = ps;
+          if (issued >= NS && !mbar_wait_bounded(&empty[s], pphase ^ 1, err)) {
             bad = 1;
           } else {
             mbar_arrive_expect_tx(&full[s], (ok ? (uint32_t)(T * (KR + VR + 2 * MR)) : 0u) + (qsrc ? (uint32_t)QB : 0u));
@@ -356,8 +358,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
   };
 
   int b = find_seq(UP, B, u0);
-  int n = 0;
-  for (int32_t u = u0; u < u1; ++u, ++n) {
+  int s = 0;           // stage of unit u
+  uint32_t phase = 0;  // parity of its full barrier
+  for (int32_t u = u0; u < u1; ++u, s = (s + 1 == NS) ? 0 : s + 1, phase ^= (s == 0)) {
     while (u >= UP[b + 1]) ++b;
     const bool seg_start = (u == u0) || (u == UP[b]);
     const bool seg_end = (u == u1 - 1) || (u == UP[b + 1] - 1);
@@ -375,25 +378,42 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
     }
     const int32_t tok0 = (u - UP[b]) * T;
     const int nv = min(T, LS[b] - tok0);
-    const int s = n % NS;
-    if (!dead && !mbar_wait_bounded(&full[s], (n / NS) & 1, err)) dead = true;
+    if (!dead && !mbar_wait_bounded(&full[s], phase, err)) dead = true;
     dead = __shfl_sync(0xffffffffu, dead, 0);
     const uint8_t* st = stages + (size_t)s * P.stage_bytes;
     if (!dead && seg_start) {
-      // q~ = H diag(s) q / sqrt(D) for this kv head's G query heads (FWHT in scratch).
+      // q~ = H diag(s) q / sqrt(D) for this kv head's G query heads: a fast Walsh-
+      // Hadamard transform with lane l holding dims l + 32 r of one head (butterfly
+      // spans 1..16 across lanes, 32.. in registers), written to the warp's scratch.
+      constexpr int R = D / 32;
       const uint16_t* qsm = reinterpret_cast<const uint16_t*>(st + offQ) + (size_t)h * G * D;
-      for (int i = lane; i < G * D; i += 32) qs[i] = __uint_as_float((uint32_t)qsm[i] << 16) * P.signs[i % D];
-      __syncwarp();
-      for (int hs = 1; hs < D; hs <<= 1) {
-        for (int i = lane; i < G * D / 2; i += 32) {
-          const int gg = i / (D / 2), pi = i % (D / 2);
-          const int a = gg * D + (pi / hs) * 2 * hs + (pi % hs);
-          const float x = qs[a], y = qs[a + hs];
-          qs[a] = x + y;
-          qs[a + hs] = x - y;
+      float sg[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) sg[r] = P.signs[lane + 32 * r];
+#pragma unroll 1
+      for (int gg = 0; gg < G; ++gg) {
+        float v[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) v[r] = __uint_as_float((uint32_t)qsm[gg * D + lane + 32 * r] << 16) * sg[r];
+#pragma unroll
+        for (int hs = 1; hs < 32; hs <<= 1) {
+          const float sgn = (lane & hs) ? -1.f : 1.f;  // upper element: x - y; lower: x + y
+#pragma unroll
+          for (int r = 0; r < R; ++r) v[r] = fmaf(sgn, v[r], __shfl_xor_sync(0xffffffffu, v[r], hs));
         }
-        __syncwarp();
+#pragma unroll
+        for (int hr = 1; hr < R; hr <<= 1)
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            if ((r & hr) == 0) {
+              const float x = v[r], y = v[r + hr];
+              v[r] = x + y;
+              v[r + hr] = x - y;
+            }
+#pragma unroll
+        for (int r = 0; r < R; ++r) qs[gg * D + lane + 32 * r] = v[r];
       }
+      __syncwarp();
 #pragma unroll
       for (int grp = 0; grp < NG; ++grp) {
         float tsum = 0.f;
