@@ -58,7 +58,13 @@ def algorithmic_bytes(fmt, D, Hkv, Hq, lens) -> int:
     return kv + qo + bt + 4 * B
 
 
+MIXED = "d256-mixed"
+STEPS_PER_REP = 8  # mixed workload: steps per repetition, each repetition from a fresh setup
+
+
 def workload_for(name: str):
+    if name == MIXED:
+        return wl.MixedWorkload()
     if name == "qwen3-0.6b":
         return wl.qwen3_0_6b()
     if name == "tiny":
@@ -425,6 +431,258 @@ def run_gpu(args, rank, world, local):
     return res, w
 
 
+def mixed_row_bytes(fmt: int, Hkv: int, D: int) -> int:
+    """Bytes of one 32-token block (row) of one layer, all stored tensors."""
+    return 32 * Hkv * token_head_bytes(fmt, D)
+
+
+class MixedRun:
+    """D256 mixed workload on the GPU: two pools (bf16, K4/V4) of one layer.  A
+    repetition is a fresh setup (untimed: initial K/V written, the host plans of its
+    steps and their inputs made resident) followed by STEPS_PER_REP timed steps; a
+    step is, per pool, copy_on_write_block of the step's pairs, write_block of one
+    token per sequence and paged_decode_attention of every sequence."""
+
+    def __init__(self, dev, rank: int):
+        import torch
+        import paged_kv_cache_split_gb300 as pkv
+        self.torch, self.pkv, self.dev, self.rank = torch, pkv, dev, rank
+        m = wl.MixedWorkload()
+        self.m0 = m
+        self.Hq, self.Hkv, self.D, self.scale = m.Hq, m.Hkv, m.D, m.scale
+        self.max_ctx = m.Lmax + 64
+        # rows needed after the last step of a repetition bound the pools' capacity
+        probe = wl.MixedWorkload()
+        for _ in range(STEPS_PER_REP):
+            probe.plan_step()
+        self.pools = []
+        for P, Pp in zip(m.pools, probe.pools):
+            rows = Pp.next_row
+            pool = pkv.Pool(1, m.Hkv, m.D, "bf16" if P.fmt == wl.FMT_BF16 else "k4v4",
+                            hadamard_seed=m.hadamard_seed, max_slabs=(rows + 31) // 32 + 8)
+            pool.reserve_rows(rows)
+            self.pools.append(pool)
+        self.outs = [torch.empty((len(P.seqs), m.Hq, m.D), dtype=torch.bfloat16, device=dev) for P in m.pools]
+        self.ws = [pool.workspace(len(P.seqs), m.Hq, dev) for pool, P in zip(self.pools, m.pools)]
+
+    def setup_rep(self):
+        """Fresh workload state: write every sequence's initial K/V (prefix blocks once
+        per group) and prepare the inputs of the repetition's steps on the device and
+        in pinned host memory."""
+        torch = self.torch
+        m = wl.MixedWorkload()
+        gen = torch.Generator(device=self.dev)
+        for pi, (P, pool) in enumerate(zip(m.pools, self.pools)):
+            rr, ss = [], []
+            for i in range(len(P.seqs)):
+                t = np.arange(P.lens[i])
+                own = np.ones(P.lens[i], bool)
+                if P.group_of[i] * m.group_size != i:
+                    own[: m.prefix] = False
+                rr.append(np.asarray(P.rows[i], np.int32)[t // 32][own])
+                ss.append((t % 32).astype(np.int32)[own])
+            rows = torch.from_numpy(np.concatenate(rr)).to(self.dev)
+            slots = torch.from_numpy(np.concatenate(ss)).to(self.dev)
+            gen.manual_seed(4000 + 10 * pi + self.rank)
+            n = rows.numel()
+            for a in range(0, n, 1 << 18):  # chunks keep the temporaries small
+                b = min(n, a + (1 << 18))
+                k = torch.randn((b - a, m.Hkv, m.D), generator=gen, device=self.dev).to(torch.bfloat16)
+                v = torch.randn((b - a, m.Hkv, m.D), generator=gen, device=self.dev).to(torch.bfloat16)
+                pool.write_block(0, rows[a:b], slots[a:b], k, v)
+        steps = []
+        for step in range(STEPS_PER_REP):
+            plan = m.plan_step()
+            per_pool = []
+            for pi, P in enumerate(m.pools):
+                st = plan[pi]
+                k, v = m.step_kv(step, pi)
+                host = {
+                    "cow_src": st["cow_src"], "cow_dst": st["cow_dst"],
+                    "rows": st["write_rows"], "slots": st["write_slots"],
+                    "k": self._bf16(k), "v": self._bf16(v), "q": self._bf16(m.step_q(step, pi)),
+                    "bt": m.block_table(pi, wl.nblocks(self.max_ctx)), "ctx": m.ctx(pi),
+                }
+                per_pool.append(host)
+            steps.append(per_pool)
+        self.steps_host = steps
+        self.steps_dev = [[{k: self._dev(v) for k, v in h.items()} for h in sp] for sp in steps]
+        self.steps_pin = [[{k: self._pin(v) for k, v in h.items()} for h in sp] for sp in steps]
+        self.steps_e2e = [[{k: torch.empty_like(v) for k, v in h.items()} for h in sp] for sp in self.steps_dev]
+        self.out_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in self.outs]
+        torch.cuda.synchronize()
+        self.m = m
+
+    def _bf16(self, bits):
+        return self.torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(self.torch.bfloat16)
+
+    def _dev(self, x):
+        t = x if isinstance(x, self.torch.Tensor) else self.torch.from_numpy(np.ascontiguousarray(x))
+        return t.to(self.dev)
+
+    def _pin(self, x):
+        t = x if isinstance(x, self.torch.Tensor) else self.torch.from_numpy(np.ascontiguousarray(x))
+        return t.pin_memory()
+
+    def run_step(self, i: int, e2e: bool = False):
+        for pi, pool in enumerate(self.pools):
+            d = self.steps_dev[i][pi]
+            if e2e:
+                e, h = self.steps_e2e[i][pi], self.steps_pin[i][pi]
+                for key in e:
+                    e[key].copy_(h[key], non_blocking=True)
+                d = e
+            if d["cow_src"].numel():
+                pool.copy_on_write_block(d["cow_src"], d["cow_dst"])
+            pool.write_block(0, d["rows"], d["slots"], d["k"], d["v"])
+            pool.paged_decode_attention(0, d["q"], d["bt"], d["ctx"], self.scale, max_ctx=self.max_ctx,
+                                        out=self.outs[pi], workspace=self.ws[pi])
+            if e2e:
+                self.out_h[pi].copy_(self.outs[pi], non_blocking=True)
+
+    def step_bytes(self, i: int) -> int:
+        """Decode algorithmic bytes of both pools at the step's lengths, plus the
+        write (bf16 K/V in, stored rows out) and copy-on-write (block read + write)."""
+        total = 0
+        for pi, P in enumerate(self.m.pools):
+            h = self.steps_host[i][pi]
+            lens = [int(x) for x in h["ctx"]]
+            total += algorithmic_bytes(P.fmt, self.D, self.Hkv, self.Hq, lens)
+            n = len(h["rows"])
+            total += n * self.Hkv * (2 * self.D * 2 + token_head_bytes(P.fmt, self.D))
+            total += 2 * len(h["cow_src"]) * mixed_row_bytes(P.fmt, self.Hkv, self.D)
+        return total
+
+    def launches(self, i: int) -> int:
+        return sum((1 if len(self.steps_host[i][pi]["cow_src"]) else 0) + 1 + LAUNCHES_PER_CALL
+                   for pi in range(len(self.pools)))
+
+    def h2d_d2h(self, i: int):
+        h2d = sum(int(t.numel() * t.element_size()) for sp in self.steps_pin[i] for t in sp.values())
+        d2h = sum(int(o.numel() * o.element_size()) for o in self.outs)
+        return h2d, d2h
+
+
+def run_gpu_mixed(args, rank, world, local):
+    import torch
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mr = MixedRun(dev, rank)
+    stream = torch.cuda.current_stream()
+    reps = max(1, math.ceil(args.steps / STEPS_PER_REP))
+    wreps = max(1, math.ceil(args.warmup / STEPS_PER_REP))
+    sampler = ClockSampler(local)
+    t_dev, t_e2e, nbytes, launches, h2d, d2h = 0.0, 0.0, 0, 0, 0, 0
+    with sampler:
+        for r in range(wreps + reps):
+            timed = r >= wreps
+            for e2e in (False, True):
+                mr.setup_rep()
+                dist_barrier(world)
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for i in range(STEPS_PER_REP):
+                    mr.run_step(i, e2e=e2e)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                dist_barrier(world)
+                if timed:
+                    ms = e0.elapsed_time(e1)
+                    if e2e:
+                        t_e2e += ms
+                    else:
+                        t_dev += ms
+                        nbytes += sum(mr.step_bytes(i) for i in range(STEPS_PER_REP))
+                        launches += sum(mr.launches(i) for i in range(STEPS_PER_REP))
+                        io = [mr.h2d_d2h(i) for i in range(STEPS_PER_REP)]
+                        h2d += sum(x for x, _ in io)
+                        d2h += sum(y for _, y in io)
+    for pool in mr.pools:
+        if pool.check_errors():
+            raise SystemExit("device error word set during the timed region")
+    nsteps = reps * STEPS_PER_REP
+    ms_step = dist_max(t_dev / nsteps, world)
+    ms_e2e = dist_max(t_e2e / nsteps, world)
+    bytes_step = nbytes / nsteps
+    value = bytes_step * world / (ms_step * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    m = mr.m0
+    tokens_step = sum(int(x) for sp in mr.steps_host for h in sp for x in h["ctx"]) / STEPS_PER_REP
+    res = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": nsteps,
+        "warmup": wreps * STEPS_PER_REP,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) bf16 K/V and q; no model weights)",
+        "config": {"workload": (f"D256 long-context mixed: 1 layer, Hq {m.Hq} / Hkv {m.Hkv} / D {m.D}, "
+                                f"{m.B} sequences (16 bf16 + 16 K4/V4 pools), lengths 1024 + U[1..{m.Lmax - 1024}], "
+                                f"8 prefix groups sharing 1024 tokens; per step: 1 token written per sequence, "
+                                f"copy-on-write of {m.n_cow} shared blocks, decode of both pools"),
+                   "global_batch": m.B * world, "seq_len": m.Lmax, "layers": 1,
+                   "steps_per_repetition": STEPS_PER_REP,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB read per step vs 129 MB L2)",
+                   "cuda_graph": False},
+        "kv_tokens_per_s": round(tokens_step * world / (ms_step * 1e-3), 1),
+        "pct_of_nominal_8tbs": round(100 * value / world / 8000.0, 2),
+        "roofline": {"bound": "hbm", "achieved": round(bytes_step / (ms_step * 1e-3) / 1e9, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(bytes_step / (ms_step * 1e-3) / 1e9 / peak, 4),
+                     "traffic": ncu_traffic(MIXED), "per_launch_bytes": int(bytes_step),
+                     "avg_launch_us": round(ms_step * 1e3, 3), "peak_source": peak_src,
+                     "kernel": "whole step: copy-on-write, write_block and decode (attention + combine) of both pools"},
+        "e2e": {"value": round(bytes_step * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": int(h2d / nsteps),
+                "d2h_bytes_per_step": int(d2h / nsteps)},
+        "gpu_launches": int(launches),
+        "clocks": sampler.summary(),
+    }
+    return res, mr
+
+
+def mixed_oracle_sample(budget_s: float = 10.0):
+    """The oracle on one sequence of each pool of the mixed workload (initial state),
+    timed until `budget_s` of CPU work."""
+    import oracle
+    m = wl.MixedWorkload()
+    cores = len(os.sched_getaffinity(0))
+    runs = []
+    for pi, P in enumerate(m.pools):
+        o = oracle.OraclePool(1, m.Hkv, m.D, P.fmt, seed=m.hadamard_seed)
+        o.reserve_rows(P.next_row)
+        k, v = m.initial_kv(pi, 0)
+        t = np.arange(P.lens[0])
+        o.write_block(0, np.asarray(P.rows[0], np.int32)[t // 32], (t % 32).astype(np.int32), k, v)
+        q = m.step_q(0, pi)[:1]
+        bt = m.block_table(pi)[:1]
+        ctx = m.ctx(pi)[:1]
+        runs.append((o, q, bt, ctx, P.fmt, int(ctx[0])))
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while True:
+        t0 = time.perf_counter()
+        for o, q, bt, ctx, _, _ in runs:
+            o.decode_attention(0, q, bt, ctx, m.scale, n_threads=cores)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end or len(times) >= 50:
+            break
+    t = statistics.median(times)
+    nbytes = sum(algorithmic_bytes(f, m.D, m.Hkv, m.Hq, [L]) for _, _, _, _, f, L in runs)
+    return {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": (f"decode of sequence 0 of each pool (bf16 {runs[0][5]} and K4/V4 {runs[1][5]} tokens, "
+                       f"all {m.Hq} query heads, 1 layer); median of {len(times)} runs"),
+            "seconds_per_sample": t, "kv_tokens_per_s": sum(r[5] for r in runs) / t}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,6 +696,28 @@ def main():
                     help="profiling aid: override the workload's layer count (not for reported numbers)")
     args = ap.parse_args()
     rank, world, local = dist_init(args.gpus)
+
+    if args.impl == "reference" and args.workload == MIXED:
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        cb = mixed_oracle_sample(budget_s=max(2.0, 0.05 * (args.warmup + args.steps)))
+        m = wl.MixedWorkload()
+        t = cb["seconds_per_sample"]
+        res = {"impl": "reference", "metric": METRIC, "value": round(cb["value"], 4), "unit": "GB/s", "n_gpus": 1,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+               "data": "synthetic (seeded N(0,1) bf16 K/V and q; no model weights)",
+               "config": {"workload": "D256 long-context mixed (decode of one sequence per pool)",
+                          "global_batch": m.B, "seq_len": m.Lmax, "layers": 1, "parallelism": "host cores"},
+               "kv_tokens_per_s": round(cb["kv_tokens_per_s"], 1),
+               "cpu_baseline": {"value": round(cb["value"], 4), "unit": "GB/s", "cores": cb["cores"],
+                                "kind": "oracle", "sample": cb["sample"]},
+               "e2e": {"value": round(cb["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                       "d2h_bytes_per_step": 0}}
+        print(json.dumps(res), flush=True)
+        return
 
     if args.impl == "reference":
         if rank != 0:
@@ -469,6 +749,18 @@ def main():
                                 "sample": base["sample"]},
                "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(res), flush=True)
+        return
+
+    if args.workload == MIXED:
+        res, _ = run_gpu_mixed(args, rank, world, local)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                cb = mixed_oracle_sample(budget_s=10.0)
+                res["cpu_baseline"] = {k: (round(v, 5) if isinstance(v, float) else v) for k, v in cb.items()}
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
 
     res, w = run_gpu(args, rank, world, local)
