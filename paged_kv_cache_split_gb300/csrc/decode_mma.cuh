@@ -5,11 +5,13 @@
 // by the chained combine kernel (decode_common.cuh).  For bf16 K/V two choices cut
 // the consumer's issue slots by several times against CUDA-core dot products:
 //
-//  * Staging: the producer copies each token's row (all kv heads, contiguous in
-//    the slab) with its own 1-D bulk copy into a padded shared-memory row whose
-//    stride is 16 bytes more than the payload.  Eight consecutive tokens then sit
-//    in eight different 16-byte bank groups, so ldmatrix reads of 8 tokens x 16
-//    bytes are conflict-free.
+//  * Staging: one 3-D tensor copy per 16 tokens and tensor (K, V) moves those
+//    tokens' rows of all kv heads; they land as 128-byte-wide boxes [column
+//    block][16 tokens][128 bytes] with the 128-byte swizzle (16-byte chunk c of
+//    token row r at chunk c ^ (r & 7)), so ldmatrix reads of 8 tokens x 16 bytes
+//    are conflict-free.  The producer's lane i issues every copy of unit i of a
+//    batch of 32 units, after the tensor-map acquire fences it ran when it read
+//    the batch.
 //  * Math on mma.sync.m16n8k16 (bf16 in, fp32 accumulate):
 //      S  = Q K^T  with M = the G query heads of the kv head (padded to 16),
 //                  N = 8 tokens, K = 16 dims; Q is an A fragment held in registers
@@ -63,11 +65,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = P.T, NS = P.NS, B = P.B;
   int32_t* err = P.lv.err;
-  const int ROW = hkv * D * 2;  // one token, all kv heads, in the slab
-  const int PROW = ROW + 16;    // padded shared-memory row
+  const int ROW = hkv * D * 2;  // one token, all kv heads, in the slab (a multiple of 128 bytes)
+  const int NX = ROW >> 7;      // 128-byte column blocks of a row
 
-  uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * P.stage_bytes);
+  // Stages start on a 1024-byte boundary (the 128-byte swizzle repeats every 1 KB).
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + (size_t)NS * P.stage_bytes);
   uint64_t* empty = full + NS;
   const uint8_t** tab = reinterpret_cast<const uint8_t**>(empty + NS);  // [kSmemTableEntries]
   int32_t* UP = reinterpret_cast<int32_t*>(tab + kSmemTableEntries);
@@ -82,8 +85,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   const int32_t u0 = (int32_t)blockIdx.x * C;
   const int32_t u1 = min(U, u0 + C);
   if (u0 >= u1) return;
-  const int offV = T * PROW;
-  const int offQ = 2 * T * PROW;          // q of the sequence, when the unit starts one
+  const int offV = T * ROW;      // K region [T/16][NX][16][128], then V region
+  const int offQ = 2 * T * ROW;  // q of the sequence, when the unit starts one
   const int QB = P.Hq * D * 2;
 
   if (warp == NC) {
@@ -91,62 +94,63 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
     const bool use_stab = smem_table_entries(P) > 0;
     const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once
     int issued = 0;
+    int ps = 0;           // stage of unit `issued`
+    uint32_t pphase = 0;  // parity of that stage's current round
     bool dead = false;
     for (int32_t ub = u0; ub < u1 && !dead; ub += 32) {
       const int32_t u = ub + lane;
-      const uint8_t* kbase = nullptr;
-      const uint8_t* vbase = nullptr;
-      const uint8_t* qsrc = nullptr;
-      int ok = 0;
+      const uint8_t* map = nullptr;   // tensor maps of the unit's slab: K, then V at + 128
+      const uint8_t* qsrc = nullptr;  // q of its sequence when the unit starts a CTA's segment
+      int y0 = 0, ok = 0;             // first slab row of the unit; row valid
       if (u < u1) {
-        const int b = find_seq(UP, B, u);
-        if (u == u0 || u == UP[b]) qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)b * P.Hq * D);
-        const int32_t tok0 = (u - UP[b]) * T;
+        const int bb = find_seq(UP, B, u);
+        if (u == u0 || u == UP[bb]) qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)bb * P.Hq * D);
+        const int32_t tok0 = (u - UP[bb]) * T;
         const int j = tok0 / kBlockTokens, slot0 = tok0 % kBlockTokens;
-        const int32_t row = P.bt[(size_t)b * P.max_blocks + j];
+        const int32_t row = P.bt[(size_t)bb * P.max_blocks + j];
         if (row >= 0 && (int64_t)row < P.lv.rows_capacity) {
           const int32_t slab = row / P.lv.slab_blocks;
           const int32_t r = row - slab * P.lv.slab_blocks;
-          const uint8_t* const* ent = use_stab ? tab + (size_t)slab * P.lv.n_kinds
-                                                : P.lv.tab.base + (size_t)slab * P.lv.tab.stride;
-          const size_t first = (size_t)(r * kBlockTokens + slot0) * ROW;
-          kbase = ent[0] + first;
-          vbase = ent[1] + first;
+          const uint8_t* ent0 =
+              use_stab ? tab[(size_t)slab * P.lv.n_kinds] : P.lv.tab.base[(size_t)slab * P.lv.tab.stride];
+          map = ent0 + P.lv.map_delta;
+          y0 = r * kBlockTokens + slot0;
           ok = 1;
+          tensormap_acquire(map);
+          tensormap_acquire(map + 128);
         } else {
           atomicOr(err, ERR_ROW);
         }
       }
       const int cnt = min(32, u1 - ub);
-      for (int i = 0; i < cnt; ++i) {
-        const uint8_t* kb = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)kbase, i);
-        const uint8_t* vb = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)vbase, i);
-        const uint8_t* qs = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)qsrc, i);
-        const int oki = __shfl_sync(0xffffffffu, ok, i);
-        const int s = issued % NS;
-        if (lane == 0) {
-          if (issued >= NS && !mbar_wait_bounded(&empty[s], ((issued / NS) & 1) ^ 1, err)) dead = true;
-          // A whole unit is always copied (T tokens stay inside the block); tokens
-          // past the context are masked by a zero probability.  A unit that starts
-          // a sequence also brings that sequence's q.
-          if (!dead)
-            mbar_arrive_expect_tx(&full[s], (oki ? (uint32_t)(2 * T * ROW) : 0u) + (qs ? (uint32_t)QB : 0u));
-        }
-        dead = __shfl_sync(0xffffffffu, dead, 0);
-        if (dead) break;
-        __syncwarp();
-        uint8_t* st = stages + (size_t)s * P.stage_bytes;
-        if (qs && lane == 31) bulk_g2s(st + offQ, qs, (uint32_t)QB, &full[s]);
-        if (oki) {
-          for (int c = lane; c < 2 * T; c += 32) {
-            const int kind = c / T, tok = c - kind * T;
-            bulk_g2s_hint(st + kind * offV + tok * PROW, (kind ? vb : kb) + (size_t)tok * ROW, (uint32_t)ROW,
-                          &full[s], kv_policy);
+      for (int i = 0; i < cnt; ++i, ++issued, ps = (ps + 1 == NS) ? 0 : ps + 1, pphase ^= (ps == 0)) {
+        int bad = 0;
+        if (lane == i) {
+          const int s = ps;
+          if (issued >= NS && !mbar_wait_bounded(&empty[s], pphase ^ 1, err)) {
+            bad = 1;
+          } else {
+            // A whole unit is always copied (T tokens stay inside the block); tokens
+            // past the context are masked by a zero probability.  A unit that starts
+            // a sequence also brings that sequence's q.
+            mbar_arrive_expect_tx(&full[s], (ok ? (uint32_t)(2 * T * ROW) : 0u) + (qsrc ? (uint32_t)QB : 0u));
+            uint8_t* st = stages + (size_t)s * P.stage_bytes;
+            if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, &full[s]);
+            if (ok) {
+              for (int cy = 0; cy < T / 16; ++cy) {
+                tma_load_3d(st + cy * 16 * ROW, map, 0, y0 + 16 * cy, 0, &full[s], kv_policy);
+                tma_load_3d(st + offV + cy * 16 * ROW, map + 128, 0, y0 + 16 * cy, 0, &full[s], kv_policy);
+              }
+            }
           }
         }
-        ++issued;
+        if (__any_sync(0xffffffffu, bad)) {
+          dead = true;
+          break;
+        }
       }
     }
+    // After a timeout, leave no copy in flight into a stage that is no longer waited on.
     if (lane == 0) {
       const int first = issued > NS ? issued - NS : 0;
       for (int n = first; n < issued; ++n) mbar_wait_bounded(&full[n % NS], (n / NS) & 1, err);
@@ -161,6 +165,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   // token 8*(mi/2)+ri and dims 8*(mi%2) .. +7 of the current 16-token x 16-dim tile.
   const int ld_tok = 8 * ((lane >> 3) >> 1) + (lane & 7);
   const int ld_dim = 8 * ((lane >> 3) & 1);
+  // Its address in a 16-token box row: the head's first column block, token row
+  // ld_tok; the 16-dim tile kk sits in column block kk / 4 at logical chunk
+  // 2 (kk % 4) + ld_dim / 8, stored at that chunk XOR (ld_tok % 8).
+  const uint32_t ld_base = (uint32_t)(((h * D * 2) >> 7) * 2048 + ld_tok * 128);
+  uint32_t ld_chunk[4];
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) ld_chunk[q4] = (uint32_t)(((2 * q4 + (ld_dim >> 3)) ^ (ld_tok & 7)) << 4);
   uint32_t qa[D / 16][2];
   float o[D / 16][4];
   float m_run = -INFINITY, l_run = 0.f;
@@ -168,8 +179,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   const uint32_t smem_base = smem_u32(stages);
 
   int b = find_seq(UP, B, u0);
-  int n = 0;
-  for (int32_t u = u0; u < u1; ++u, ++n) {
+  int s = 0;           // stage of unit u
+  uint32_t phase = 0;  // parity of its full barrier
+  for (int32_t u = u0; u < u1; ++u, s = (s + 1 == NS) ? 0 : s + 1, phase ^= (s == 0)) {
     while (u >= UP[b + 1]) ++b;
     const bool seg_start = (u == u0) || (u == UP[b]);
     const bool seg_end = (u == u1 - 1) || (u == UP[b + 1] - 1);
@@ -184,8 +196,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
 
     const int32_t tok0 = (u - UP[b]) * T;
     const int nv = min(T, LS[b] - tok0);
-    const int s = n % NS;
-    if (!dead && !mbar_wait_bounded(&full[s], (n / NS) & 1, err)) dead = true;
+    if (!dead && !mbar_wait_bounded(&full[s], phase, err)) dead = true;
     dead = __shfl_sync(0xffffffffu, dead, 0);
     if (!dead && seg_start) {
       // A fragments of Q (rows = query heads of kv head h; rows >= G are zero),
@@ -206,11 +217,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
         float sacc[2][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) sacc[0][i] = sacc[1][i] = 0.f;
-        const uint32_t kaddr = kst + (uint32_t)((kc * 16 + ld_tok) * PROW + h * D * 2 + ld_dim * 2);
+        const uint32_t kaddr = kst + (uint32_t)(kc * NX * 2048) + ld_base;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           uint32_t r0, r1, r2, r3;
-          ldsm_x4(kaddr + kk * 32, r0, r1, r2, r3);
+          ldsm_x4(kaddr + (kk >> 2) * 2048 + ld_chunk[kk & 3], r0, r1, r2, r3);
           mma_bf16_16816(sacc[0], qa[kk][0], 0u, qa[kk][1], 0u, r0, r1);
           mma_bf16_16816(sacc[1], qa[kk][0], 0u, qa[kk][1], 0u, r2, r3);
         }
@@ -245,11 +256,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
         l_run += (p0 + p1) + (p2 + p3);
         const uint32_t pb0 = pack_bf16x2(p0, p1), pb1 = pack_bf16x2(p2, p3);
         // ---- O^T += V^T P^T over these 16 tokens ----
-        const uint32_t vaddr = vst + (uint32_t)((kc * 16 + ld_tok) * PROW + h * D * 2 + ld_dim * 2);
+        const uint32_t vaddr = vst + (uint32_t)(kc * NX * 2048) + ld_base;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(vaddr + mt * 32, a0, a1, a2, a3);
+          ldsm_x4_t(vaddr + (mt >> 2) * 2048 + ld_chunk[mt & 3], a0, a1, a2, a3);
           mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
         }
       }
@@ -327,7 +338,7 @@ cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
   P.partials = a.partials;
   P.T = a.tokens_per_stage;
   P.NS = a.n_stages;
-  P.stage_bytes = 2 * P.T * (a.lv.hkv * D * 2 + 16) + a.Hq * D * 2;
+  P.stage_bytes = 2 * P.T * (a.lv.hkv * D * 2) + ((a.Hq * D * 2 + 1023) & ~1023);
   auto kern = decode_bf16_mma_kernel<D, G>;
   static bool attr_set = false;
   if (!attr_set) {

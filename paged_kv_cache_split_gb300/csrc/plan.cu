@@ -17,21 +17,24 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
   if (packed) fixed += (size_t)hkv * G * D * 4;
   if (fixed >= budget) return false;
   if (!packed) {
-    // Native bf16 (tensor-core kernel): each token's row of all kv heads is copied
-    // into a padded row (payload + 16 bytes) for K and for V; T is 32 or 16 (the
-    // PV product consumes 16 tokens at a time).  Prefer T = 32 with >= 3 stages.
-    const size_t prow = (size_t)hkv * D * 2 + 16;
+    // Native bf16 (tensor-core kernel): T tokens of K and of V for all kv heads, as
+    // swizzled 128-byte-wide boxes, plus q of one sequence (rounded up to 1 KB so
+    // every stage starts on a 1024-byte boundary); T is 32 or 16 (the PV product
+    // consumes 16 tokens at a time).  Prefer T = 32 with >= 3 stages.
+    const size_t row = (size_t)hkv * D * 2;
     const int cand_bf16[2] = {32, 16};
     for (int pass = 0; pass < 2; ++pass) {
       for (int T : cand_bf16) {
-        const size_t stage = 2 * (size_t)T * prow + (size_t)hkv * G * D * 2;  // + q of one sequence
-        size_t ns = (budget - fixed) / (stage + 16);
+        const size_t stage = 2 * (size_t)T * row + (((size_t)hkv * G * D * 2 + 1023) & ~(size_t)1023);
+        // + 1024: the kernel aligns the first stage to a 1024-byte boundary
+        if (fixed + 1024 >= budget) return false;
+        size_t ns = (budget - fixed - 1024) / (stage + 16);
         if (ns > 8) ns = 8;
         if ((pass == 0 && ns >= 3) || (pass == 1 && ns >= 2)) {
           plan->tokens_per_stage = T;
           plan->n_stages = (int)ns;
           plan->stage_bytes = stage;
-          plan->smem_bytes = ns * stage + ns * 16 + fixed;
+          plan->smem_bytes = ns * stage + ns * 16 + fixed + 1024;
           plan->threads = (hkv + 1) * 32;
           return true;
         }

@@ -38,7 +38,7 @@ struct pkv_pool {
   int64_t slab_bytes[4] = {0, 0, 0, 0};  // one slab of one layer, per kind
   int64_t group_bytes = 0;               // one slab index across layers and kinds
   int64_t layer_bytes = 0;               // one slab of one layer, all kinds
-  int64_t maps_offset = 0;               // packed: tensor maps at the group's tail
+  int64_t maps_offset = 0;               // tensor maps at the group's tail
   std::vector<void*> groups;             // allocation per slab index
   uint8_t** table_host = nullptr;        // pinned [max_slabs][n_layers][n_kinds]
   uint8_t** table_dev = nullptr;
@@ -115,9 +115,10 @@ static EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-// 2-D tensor maps of one slab group (packed formats): for every layer and stored
-// tensor, the slab viewed as [slab_blocks * 32 tokens][Hkv * row] bytes, read in
-// boxes of 16 tokens x box_bytes with the matching shared-memory swizzle.
+// Tensor maps of one slab group: for every layer and stored tensor, the slab
+// [slab_blocks * 32 tokens][Hkv * row] bytes viewed in 3-D as [column block][token]
+// [W bytes] (W = box_bytes), read in boxes of 16 tokens x the whole row, which land
+// as row/W boxes of 16 x W bytes with the matching shared-memory swizzle.
 static bool encode_group_maps(const pkv_pool* p, uint8_t* group, std::vector<CUtensorMap>& maps) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
@@ -214,13 +215,11 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_allocator* allo
     p->layer_bytes += p->slab_bytes[k];
   }
   p->group_bytes = p->layer_bytes * cfg->n_layers;
-  if (p->n_kinds == 4) {
-    // Tensor maps (128 bytes each, 64-byte aligned) after the slab data.
-    p->maps_offset = (p->group_bytes + 127) / 128 * 128;
-    p->group_bytes = p->maps_offset + (int64_t)cfg->n_layers * p->n_kinds * 128;
-    for (int k = 0; k < 4; ++k)
-      if (tma_box_bytes(p->row_bytes[k] * cfg->n_kv_heads) == 0) return fail(PKV_ERR_INVALID);
-  }
+  // Tensor maps (128 bytes each, 64-byte aligned) after the slab data.
+  p->maps_offset = (p->group_bytes + 127) / 128 * 128;
+  p->group_bytes = p->maps_offset + (int64_t)cfg->n_layers * p->n_kinds * 128;
+  for (int k = 0; k < p->n_kinds; ++k)
+    if (tma_box_bytes(p->row_bytes[k] * cfg->n_kv_heads) == 0) return fail(PKV_ERR_INVALID);
 
   const size_t table_entries = (size_t)cfg->max_slabs * cfg->n_layers * p->n_kinds;
   e = cudaMallocHost((void**)&p->table_host, table_entries * sizeof(uint8_t*));
@@ -295,9 +294,9 @@ pkv_status pkv_append_slab(pkv_pool* p, int n_slabs, void* stream) {
     }
     fresh.push_back(ptr);
   }
-  // Packed formats: tensor maps of the new slabs, encoded before anything is
-  // enqueued so that a failure leaves the pool unchanged.
-  std::vector<std::vector<CUtensorMap>> maps(p->n_kinds == 4 ? fresh.size() : 0);
+  // Tensor maps of the new slabs, encoded before anything is enqueued so that a
+  // failure leaves the pool unchanged.
+  std::vector<std::vector<CUtensorMap>> maps(fresh.size());
   for (size_t i = 0; i < maps.size(); ++i) {
     if (!encode_group_maps(p, (uint8_t*)fresh[i], maps[i])) {
       for (void* q : fresh) {
