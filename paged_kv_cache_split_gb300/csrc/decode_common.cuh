@@ -63,15 +63,78 @@ __device__ __forceinline__ int find_seq(const int32_t* UP, int B, int32_t u) {
 // this kernel on the stream has completed: the combine kernel relies on that to
 // read the context lengths before its own wait.
 //
-// Before the wait the kernel touches only what no kernel writes: it copies this
+// Before the wait the kernel relies only on what no kernel writes: it copies this
 // layer's slab base pointers into shared memory (`tab`, when they fit; the table
-// changes only through stream-ordered copies issued by append_slab) and issues L2
-// prefetch hints for the context lengths and the block table.
+// changes only through stream-ordered copies issued by append_slab), issues L2
+// prefetch hints for the context lengths and the block table, and prefetches the
+// guessed first units' K/V (prefetch_first_units).
 constexpr int kSmemTableEntries = 1024;
 
 __device__ __forceinline__ int smem_table_entries(const DecodeParams& P) {
   const int64_t n = (P.lv.rows_capacity / P.lv.slab_blocks) * P.lv.n_kinds;
   return n <= kSmemTableEntries ? (int)n : 0;
+}
+
+// Before the dependency wait the producer warp guesses this CTA's first units from
+// the context lengths and block table as they are now (an earlier kernel may still
+// be writing them: the guess only steers L2 prefetches, every address it forms is
+// a pool row checked against the pool, and nothing read here is used after the
+// wait) and prefetches the K/V rows of the first `nunits` of them into L2, so that
+// the copies issued after the wait hit L2.  Units past the CTA's first sequence
+// are not guessed.
+__device__ __forceinline__ void prefetch_first_units(const DecodeParams& P, int nunits) {
+  const int lane = threadIdx.x & 31;
+  const int lim = P.max_blocks * kBlockTokens;
+  auto units_of = [&](int b) -> int32_t {
+    int32_t L = b < P.B ? P.ctx[b] : 0;
+    L = L < 0 ? 0 : (L > lim ? lim : L);
+    return (L + P.T - 1) / P.T;
+  };
+  int32_t tot = 0;
+  for (int base = 0; base < P.B; base += 32) {
+    int32_t n = units_of(base + lane);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+    tot += n;
+  }
+  const int32_t C = (tot + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
+  const int32_t u0 = (int32_t)blockIdx.x * C;
+  if (C == 0 || u0 >= tot) return;
+  // the sequence holding unit u0, and its first unit
+  int32_t carry = 0;
+  int bsel = -1, nsel = 0;
+  int32_t ubase = 0;
+  for (int base = 0; base < P.B && bsel < 0; base += 32) {
+    const int32_t n = units_of(base + lane);
+    int32_t inc = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, base + lane < P.B && carry + inc > u0);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      bsel = base + l;
+      nsel = __shfl_sync(0xffffffffu, n, l);
+      ubase = carry + __shfl_sync(0xffffffffu, inc - n, l);
+    }
+    carry += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  if (bsel < 0) return;
+  const int32_t u = u0 + lane;
+  if (lane >= nunits || u >= ubase + nsel) return;
+  const int32_t tok0 = (u - ubase) * P.T;
+  const int j = tok0 / kBlockTokens, slot0 = tok0 % kBlockTokens;
+  if (j >= P.max_blocks) return;
+  const int32_t row = P.bt[(size_t)bsel * P.max_blocks + j];
+  if (row < 0 || (int64_t)row >= P.lv.rows_capacity) return;
+  const int32_t slab = row / P.lv.slab_blocks, r = row - slab * P.lv.slab_blocks;
+  for (int k = 0; k < P.lv.n_kinds; ++k) {
+    const uint8_t* base = P.lv.tab.base[(size_t)slab * P.lv.tab.stride + k];
+    const int rowk = P.lv.row_bytes[k] * P.lv.hkv;
+    if (base) bulk_prefetch_l2(base + (size_t)(r * kBlockTokens + slot0) * rowk, (uint32_t)(P.T * rowk));
+  }
 }
 
 __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t* full, uint64_t* empty, int NC,
@@ -85,6 +148,7 @@ __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t*
   for (int i = threadIdx.x * 32; i < P.B; i += blockDim.x * 32) prefetch_l2(P.ctx + i);
   for (int64_t i = (int64_t)threadIdx.x * 32; i < (int64_t)P.B * P.max_blocks; i += (int64_t)blockDim.x * 32)
     prefetch_l2(P.bt + i);
+  if (warp == NC) prefetch_first_units(P, P.NS);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
