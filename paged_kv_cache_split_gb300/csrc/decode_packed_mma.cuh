@@ -40,6 +40,8 @@
 
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "decode_common.cuh"
 
 namespace pkv {
@@ -441,7 +443,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
     }
     if (!dead) {
       const uint32_t sb = smem_u32(st);
-      for (int kc = 0; kc * 16 < nv; ++kc) {
+      // One 16-token chunk; kFull: all 16 tokens are inside the context (no mask).
+      auto chunk = [&](auto full_c, const int kc) {
+        constexpr bool kFull = decltype(full_c)::value;
         // ---- logits for 16 tokens: n-tiles (token halves) j = 0, 1 ----
         uint32_t kw[2][NKC];  // word t of token 16kc + 8j + g, chunk c
         if constexpr (NKC == 2) {
@@ -486,9 +490,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
               sa1 = fmaf(q2 ? m1.z : m1.x, cacc[1], fmaf(q2 ? m1.w : m1.y, qsum[grp], sa1));
             }
           }
-          const int tk = kc * 16 + 8 * j + 2 * t;
-          x[j][0] = tk < nv ? sa0 * scale24 : -INFINITY;
-          x[j][1] = tk + 1 < nv ? sa1 * scale24 : -INFINITY;
+          if constexpr (kFull) {
+            x[j][0] = sa0 * scale24;
+            x[j][1] = sa1 * scale24;
+          } else {
+            const int tk = kc * 16 + 8 * j + 2 * t;
+            x[j][0] = tk < nv ? sa0 * scale24 : -INFINITY;
+            x[j][1] = tk + 1 < nv ? sa1 * scale24 : -INFINITY;
+          }
         }
         // ---- online softmax for head g ----
         float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
@@ -578,6 +587,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
             }
           }
         }
+      };
+      if (D <= 64 && T == 32 && nv == 32) {
+        // a whole 32-token unit: both chunks unrolled (registers allow it at D = 64), no masks
+        chunk(std::true_type{}, 0);
+        chunk(std::true_type{}, 1);
+      } else {
+        for (int kc = 0; kc * 16 < nv; ++kc) chunk(std::false_type{}, kc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
