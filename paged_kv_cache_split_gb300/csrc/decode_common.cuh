@@ -138,7 +138,7 @@ __device__ __forceinline__ void prefetch_first_units(const DecodeParams& P, int 
 }
 
 __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t* full, uint64_t* empty, int NC,
-                                                int32_t* UP, int32_t* LS, const uint8_t** tab) {
+                                                int PW, int32_t* UP, int32_t* LS, const uint8_t** tab) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = smem_table_entries(P);
   for (int i = threadIdx.x; i < nt; i += blockDim.x) {
@@ -148,7 +148,7 @@ __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t*
   for (int i = threadIdx.x * 32; i < P.B; i += blockDim.x * 32) prefetch_l2(P.ctx + i);
   for (int64_t i = (int64_t)threadIdx.x * 32; i < (int64_t)P.B * P.max_blocks; i += (int64_t)blockDim.x * 32)
     prefetch_l2(P.bt + i);
-  if (warp == NC) prefetch_first_units(P, P.NS);
+  if (warp == PW) prefetch_first_units(P, P.NS);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   int32_t* UP = reinterpret_cast<int32_t*>(tab + kSmemTableEntries);
   int32_t* LS = UP + (B + 1);
 
-  decode_prologue(P, full, empty, NC, UP, LS, tab);
+  decode_prologue(P, full, empty, NC, NC, UP, LS, tab);
   __syncthreads();
   const int32_t U = UP[B];
   const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;

@@ -157,11 +157,21 @@ __device__ __forceinline__ int swz(const SwzRegion& z, int tok, int b) {
 
 __device__ __forceinline__ int ilog2i(int v) { return 31 - __clz(v); }
 
+// Register split (RS): the block is laid out in warpgroups, ceil(Hkv / 4) of consumer
+// warps and one whose first warp is the producer.  At entry the producer warpgroup
+// gives registers back (setmaxnreg.dec to kProdRegs) and the consumer warpgroups
+// take them (setmaxnreg.inc to kConsRegs): per scheduler, two consumer warps and one
+// producer-group warp fit in the three warps' launch allocation (2 x 224 + 56 = 3 x
+// 168).  The launcher checks the kernel's launch register count before choosing it.
+constexpr int kRsThreads = 384;
+constexpr int kConsRegs = 224;
+constexpr int kProdRegs = 56;
+
 // W128: every stored tensor's all-heads row is a multiple of 128 bytes, so every box
 // is 128 bytes wide; then every shared-memory address below is a per-lane constant
 // plus a per-chunk uniform offset plus an immediate.
-template <int FMT, int D, int G, bool W128>
-__global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const DecodeParams P) {
+template <int FMT, int D, int G, bool W128, bool RS>
+__global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packed_mma_kernel(const DecodeParams P) {
   using Tr = PackedTraits<FMT, D>;
   static_assert(G >= 1 && G <= 8 && D % 32 == 0, "geometry");
   constexpr int NG = Tr::NG;
@@ -169,6 +179,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
   const int hkv = P.lv.hkv;
   const int NC = hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NCW = (hkv + 3) >> 2;               // consumer warpgroups (register split)
+  const int PW = RS ? 4 * NCW : NC;             // the producer warp
   const int T = P.T, NS = P.NS, B = P.B;
   int32_t* err = P.lv.err;
   // Per-token rows of all kv heads in the slab; stage regions of T such rows.
@@ -197,7 +209,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
   int32_t* LS = UP + (B + 1);
   float* qscr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(LS + B) + 15) & ~uintptr_t(15));
 
-  decode_prologue(P, full, empty, NC, UP, LS, tab);
+  decode_prologue(P, full, empty, NC, PW, UP, LS, tab);
   __syncthreads();
   const int32_t U = UP[B];
   const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
@@ -207,7 +219,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
   const int32_t u1 = min(U, u0 + C);
   if (u0 >= u1) return;
 
-  if (warp == NC) {
+  // Register split at the role branch: the producer warpgroup gives registers back,
+  // the consumer warpgroups take them; neither path rejoins the other.
+  if (RS && warp >= 4 * NCW) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
+    if (warp != PW) return;
+  }
+  if (RS && warp < 4 * NCW) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsRegs));
+  if (warp == PW) {
     // ----------------------------- producer ---------------------------------
     // Lanes hold the info of a batch of 32 units; lane i issues every copy of unit
     // i of the batch (one 3-D tensor copy per 16 tokens and stored tensor, plus q
@@ -278,6 +297,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
     return;
   }
 
+  if (warp >= NC) return;  // warps without a role in the register-split layout
   // ------------------------------ consumers ---------------------------------
   constexpr int NKC = Tr::NKC, NVC = Tr::NVC, NMC = Tr::NMC;
   const int h = warp;
@@ -667,7 +687,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_packed_mma_kernel(const
   }
 }
 
-template <int FMT, int D, int G, bool W128>
+template <int FMT, int D, int G, bool W128, bool RS>
 cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   using Tr = PackedTraits<FMT, D>;
   DecodeParams P;
@@ -688,26 +708,44 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   P.NS = a.n_stages;
   const int hkv = a.lv.hkv;
   P.stage_bytes = packed_stage_bytes(P.T, hkv * Tr::KB, hkv * Tr::VB, hkv * Tr::MB, a.Hq * D * 2);
-  auto kern = decode_packed_mma_kernel<FMT, D, G, W128>;
+  auto kern = decode_packed_mma_kernel<FMT, D, G, W128, RS>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  cudaError_t e = launch_with_pdl(kern, a.grid, (hkv + 1) * 32, a.smem_bytes, a.stream, P);
+  const int threads = RS ? 128 * (((hkv + 3) >> 2) + 1) : (hkv + 1) * 32;
+  cudaError_t e = launch_with_pdl(kern, a.grid, threads, a.smem_bytes, a.stream, P);
   if (e != cudaSuccess) return e;
   return launch_combine<D>(P, a.grid, a.stream);
+}
+
+// The register split needs the launch allocation to cover the split: per scheduler
+// 2 x kConsRegs + kProdRegs <= 3 x (registers per thread at launch); otherwise
+// setmaxnreg.inc could never be satisfied.  Checked once per kernel.
+template <typename Kern>
+bool register_split_fits(Kern kern) {
+  static int verdict = -1;
+  if (verdict < 0) {
+    cudaFuncAttributes fa;
+    verdict = cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.maxThreadsPerBlock >= kRsThreads &&
+              2 * kConsRegs + kProdRegs <= 3 * fa.numRegs;
+  }
+  return verdict == 1;
 }
 
 template <int FMT>
 cudaError_t launch_decode_packed_mma(const DecodeArgs& a) {
   const bool w128 = a.lv.box_bytes[0] == 128 && a.lv.box_bytes[1] == 128 && a.lv.box_bytes[2] == 128 &&
                     a.lv.box_bytes[3] == 128;
-#define PKV_CASE(DD, GG)                                                      \
-  if (a.D == DD && a.G == GG)                                                 \
-    return w128 ? launch_decode_packed_mma_t<FMT, DD, GG, true>(a)            \
-                : launch_decode_packed_mma_t<FMT, DD, GG, false>(a);
+#define PKV_CASE(DD, GG)                                                                             \
+  if (a.D == DD && a.G == GG) {                                                                      \
+    if (w128 && DD >= 128 && register_split_fits(decode_packed_mma_kernel<FMT, DD, GG, true, true>)) \
+      return launch_decode_packed_mma_t<FMT, DD, GG, true, true>(a);                                 \
+    return w128 ? launch_decode_packed_mma_t<FMT, DD, GG, true, false>(a)                            \
+                : launch_decode_packed_mma_t<FMT, DD, GG, false, false>(a);                          \
+  }
   PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
   PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
   PKV_CASE(256, 1) PKV_CASE(256, 2) PKV_CASE(256, 4) PKV_CASE(256, 8)
