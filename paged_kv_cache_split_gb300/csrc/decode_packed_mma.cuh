@@ -608,8 +608,8 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
           }
         }
       };
-      if (D <= 64 && T == 32 && nv == 32) {
-        // a whole 32-token unit: both chunks unrolled (registers allow it at D = 64), no masks
+      if ((D <= 64 || (RS && D <= 128)) && T == 32 && nv == 32) {
+        // a whole 32-token unit: both chunks unrolled where registers allow it, no masks
         chunk(std::true_type{}, 0);
         chunk(std::true_type{}, 1);
       } else {
