@@ -148,7 +148,7 @@ __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t*
   for (int i = threadIdx.x * 32; i < P.B; i += blockDim.x * 32) prefetch_l2(P.ctx + i);
   for (int64_t i = (int64_t)threadIdx.x * 32; i < (int64_t)P.B * P.max_blocks; i += (int64_t)blockDim.x * 32)
     prefetch_l2(P.bt + i);
-  if (warp == PW) prefetch_first_units(P, P.NS);
+  if (warp == PW) prefetch_first_units(P, P.NS < 2 ? P.NS : 2);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
