@@ -170,16 +170,22 @@ constexpr int kProdRegs = 56;
 // W128: every stored tensor's all-heads row is a multiple of 128 bytes, so every box
 // is 128 bytes wide; then every shared-memory address below is a per-lane constant
 // plus a per-chunk uniform offset plus an immediate.
-template <int FMT, int D, int G, bool W128, bool RS>
+// DS (dim split, D = 256 with at most 4 kv heads): two consumer warps per kv head,
+// each owning half of the head's affine groups (K dims for the logits, V dims for
+// the output).  Per 16-token chunk the two halves of every logit are exchanged
+// through shared memory and added in a fixed order, so both warps run the same
+// softmax; each keeps the state of its own dims.
+template <int FMT, int D, int G, bool W128, bool RS, bool DS>
 __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packed_mma_kernel(const DecodeParams P) {
   using Tr = PackedTraits<FMT, D>;
   static_assert(G >= 1 && G <= 8 && D % 32 == 0, "geometry");
+  static_assert(!DS || (W128 && D == 256), "dim split: 128-byte boxes, D = 256");
   constexpr int NG = Tr::NG;
   extern __shared__ __align__(128) uint8_t smem[];
   const int hkv = P.lv.hkv;
-  const int NC = hkv;
+  const int NC = DS ? 2 * hkv : hkv;  // consumer warps
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NCW = (hkv + 3) >> 2;               // consumer warpgroups (register split)
+  const int NCW = (NC + 3) >> 2;                // consumer warpgroups (register split)
   const int PW = RS ? 4 * NCW : NC;             // the producer warp
   const int T = P.T, NS = P.NS, B = P.B;
   int32_t* err = P.lv.err;
@@ -208,8 +214,16 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   int32_t* UP = reinterpret_cast<int32_t*>(tab + kSmemTableEntries);
   int32_t* LS = UP + (B + 1);
   float* qscr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(LS + B) + 15) & ~uintptr_t(15));
+  // dim split: per kv head, each half's partial logits of the last two chunks, and
+  // one mbarrier per kv head that pairs the two warps (bounded waits)
+  float4* xbuf = reinterpret_cast<float4*>(qscr + (size_t)hkv * G * D);
+  uint64_t* pbar = reinterpret_cast<uint64_t*>(xbuf + (size_t)hkv * 2 * 2 * 32);
 
   decode_prologue(P, full, empty, NC, PW, UP, LS, tab);
+  if (DS && threadIdx.x == 0) {
+    for (int i = 0; i < hkv; ++i) mbar_init(&pbar[i], 64);
+    fence_mbar_init();
+  }
   __syncthreads();
   const int32_t U = UP[B];
   const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
@@ -299,16 +313,34 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 
   if (warp >= NC) return;  // warps without a role in the register-split layout
   // ------------------------------ consumers ---------------------------------
-  constexpr int NKC = Tr::NKC, NVC = Tr::NVC, NMC = Tr::NMC;
-  const int h = warp;
+  // the warp's share of the head: NGL groups from group gofs; chunk counts per row
+  constexpr int NGL = DS ? NG / 2 : NG;
+  constexpr int NKC = Tr::NKC / (DS ? 2 : 1), NVC = Tr::NVC / (DS ? 2 : 1), NMC = Tr::NMC / (DS ? 2 : 1);
+  const int h = DS ? warp % hkv : warp;
+  const int half = DS ? warp / hkv : 0;
+  const int gofs = half * NGL;
   const int g = lane >> 2, t = lane & 3;
-  float* qs = qscr + (size_t)warp * G * D;
-  uint32_t qa[NG][2][2];  // A fragments per group, k-step, register (rows g; rows g+8 zero)
-  float qsum[NG];         // 2^-24 * sum over the group of the q~ values the MMA sees
-  float o[NG][2][4];      // O^T accumulators, in units of 2^-24: group, M tile, fragment
-  float corr[NG];         // sum_t p_t o_t for head g and each group, this lane's tokens
+  float* qs = qscr + (size_t)h * G * D;  // dim split: shared by the pair, written by half 0
+  uint32_t qa[NGL][2][2];  // A fragments per group, k-step, register (rows g; rows g+8 zero)
+  float qsum[NGL];         // 2^-24 * sum over the group of the q~ values the MMA sees
+  float o[NGL][2][4];      // O^T accumulators, in units of 2^-24: group, M tile, fragment
+  float corr[NGL];         // sum_t p_t o_t for head g and each group, this lane's tokens
+  uint32_t pphase = 0;     // dim split: phase of the pair barrier
+  int xpar = 0;            // dim split: which partial-logit buffer this chunk uses
   float m_run = -INFINITY, l_run = 0.f;
   bool dead = false;
+  // dim split: every lane of both warps of the pair arrives, then waits (bounded) for
+  // the other warp; a warp that gave up (or was already dead) takes no further part,
+  // so its partner gives up at its next wait and no wait is ever repeated.
+  auto pair_sync = [&]() {
+    if constexpr (DS) {
+      if (dead) return;
+      mbar_arrive(&pbar[h]);
+      const bool ok = mbar_wait_bounded(&pbar[h], pphase, err);
+      pphase ^= 1;
+      dead = __any_sync(0xffffffffu, !ok);
+    }
+  };
   const float scale24 = P.scale_log2 * 16777216.0f;
 
   // Shared-memory addresses.  ldmatrix: lane 8i + r gives row r of matrix i.  K codes
@@ -334,17 +366,17 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     for (int cs = 0; cs < KCS; ++cs) {
       const int c = NKC == 2 ? (li & 1) : 4 * cs + li;
       const int row = NKC == 2 ? 8 * (li >> 1) + lr : lr;
-      const int byte = h * Tr::KB + 16 * c;
+      const int byte = h * Tr::KB + 16 * (c + half * NKC);
       kofs[cs] = zr[0].off + (byte >> 7) * 2048 + row * 128 + ((((byte >> 4) & 7) ^ lr) << 4);
     }
 #pragma unroll
     for (int cs = 0; cs < VCS; ++cs) {
       const int c = NVC == 2 ? (li & 1) : 4 * cs + li;
       const int row = NVC == 2 ? 8 * (li >> 1) + lr : lr;
-      const int byte = h * Tr::VB + 16 * c;
+      const int byte = h * Tr::VB + 16 * (c + half * NVC);
       vofs[cs] = zr[1].off + (byte >> 7) * 2048 + row * 128 + ((((byte >> 4) & 7) ^ lr) << 4);
     }
-    const int mb = h * Tr::MB;
+    const int mb = h * Tr::MB + 16 * half * NMC;
 #pragma unroll
     for (int x = 0; x < NMX; ++x)
       mofs[x] = zr[2].off + (mb >> 7) * 2048 + 2 * t * 128 + (((((mb >> 4) & 7) ^ (2 * t)) ^ x) << 4);
@@ -358,7 +390,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     } else {
       const int c = NKC == 2 ? (li & 1) : 4 * cs + li;
       const int row = NKC == 2 ? 8 * (li >> 1) + lr : 8 * j + lr;
-      return sb + swz(zr[0], kc * 16 + row, h * Tr::KB + 16 * c);
+      return sb + swz(zr[0], kc * 16 + row, h * Tr::KB + 16 * (c + half * NKC));
     }
   };
   auto v_addr = [&](uint32_t sb, int kc, int p, int cs) -> uint32_t {
@@ -367,7 +399,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     } else {
       const int c = NVC == 2 ? (li & 1) : 4 * cs + li;
       const int row = NVC == 2 ? 8 * (li >> 1) + lr : 8 * p + lr;
-      return sb + swz(zr[1], kc * 16 + row, h * Tr::VB + 16 * c);
+      return sb + swz(zr[1], kc * 16 + row, h * Tr::VB + 16 * (c + half * NVC));
     }
   };
   // (scale, offset) of groups 2cm, 2cm+1 for token 16kc + 8j + 2t + e; kind 2 = K, 3 = V
@@ -375,7 +407,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     if constexpr (W128) {
       return sb + (kind == 3 ? VMD : 0) + kc * MSTEP + mofs[cm ^ e] + 1024 * j + 128 * e;
     } else {
-      return sb + swz(zr[kind], kc * 16 + 8 * j + 2 * t + e, h * Tr::MB + 16 * cm);
+      return sb + swz(zr[kind], kc * 16 + 8 * j + 2 * t + e, h * Tr::MB + 16 * (cm + half * NMC));
     }
   };
 
@@ -388,7 +420,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     const bool seg_end = (u == u1 - 1) || (u == UP[b + 1] - 1);
     if (seg_start) {
 #pragma unroll
-      for (int grp = 0; grp < NG; ++grp) {
+      for (int grp = 0; grp < NGL; ++grp) {
         corr[grp] = 0.f;
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi)
@@ -403,7 +435,8 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     if (!dead && !mbar_wait_bounded(&full[s], phase, err)) dead = true;
     dead = __shfl_sync(0xffffffffu, dead, 0);
     const uint8_t* st = stages + (size_t)s * P.stage_bytes;
-    if (!dead && seg_start) {
+    if (seg_start) pair_sync();  // the partner is done with the previous segment's q~
+    if (!dead && seg_start && half == 0) {
       // q~ = H diag(s) q / sqrt(D) for this kv head's G query heads: a fast Walsh-
       // Hadamard transform with lane l holding dims l + 32 r of one head (butterfly
       // spans 1..16 across lanes, 32.. in registers), written to the warp's scratch.
@@ -435,9 +468,12 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 #pragma unroll
         for (int r = 0; r < R; ++r) qs[gg * D + lane + 32 * r] = v[r];
       }
+    }
+    if (seg_start) pair_sync();  // q~ of this segment is in qs
+    if (!dead && seg_start) {
       __syncwarp();
 #pragma unroll
-      for (int grp = 0; grp < NG; ++grp) {
+      for (int grp = 0; grp < NGL; ++grp) {
         float tsum = 0.f;
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks)
@@ -447,7 +483,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
             bool d16 = false;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-              const int dd = 32 * grp + k_dim<Tr::KBITS>(t, ks, r, hh, d16);
+              const int dd = 32 * (gofs + grp) + k_dim<Tr::KBITS>(t, ks, r, hh, d16);
               const float qv = g < G ? qs[g * D + dd] * P.inv_sqrt_d : 0.f;
               v[hh] = d16 ? qv * 0.0625f : qv;
             }
@@ -510,13 +546,29 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
               sa1 = fmaf(q2 ? m1.z : m1.x, cacc[1], fmaf(q2 ? m1.w : m1.y, qsum[grp], sa1));
             }
           }
+          x[j][0] = sa0;
+          x[j][1] = sa1;
+        }
+        if constexpr (DS) {
+          // both halves of every logit, added in half order by both warps
+          xbuf[(((size_t)h * 2 + half) * 2 + xpar) * 32 + lane] = make_float4(x[0][0], x[0][1], x[1][0], x[1][1]);
+          pair_sync();
+          const float4 pr = xbuf[(((size_t)h * 2 + (half ^ 1)) * 2 + xpar) * 32 + lane];
+          xpar ^= 1;
+          x[0][0] = half ? pr.x + x[0][0] : x[0][0] + pr.x;
+          x[0][1] = half ? pr.y + x[0][1] : x[0][1] + pr.y;
+          x[1][0] = half ? pr.z + x[1][0] : x[1][0] + pr.z;
+          x[1][1] = half ? pr.w + x[1][1] : x[1][1] + pr.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
           if constexpr (kFull) {
-            x[j][0] = sa0 * scale24;
-            x[j][1] = sa1 * scale24;
+            x[j][0] *= scale24;
+            x[j][1] *= scale24;
           } else {
             const int tk = kc * 16 + 8 * j + 2 * t;
-            x[j][0] = tk < nv ? sa0 * scale24 : -INFINITY;
-            x[j][1] = tk + 1 < nv ? sa1 * scale24 : -INFINITY;
+            x[j][0] = tk < nv ? x[j][0] * scale24 : -INFINITY;
+            x[j][1] = tk + 1 < nv ? x[j][1] * scale24 : -INFINITY;
           }
         }
         // ---- online softmax for head g ----
@@ -529,11 +581,11 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
           if (grow) m_run = mx;
           l_run *= alpha;
 #pragma unroll
-          for (int grp = 0; grp < NG; ++grp) corr[grp] *= alpha;
+          for (int grp = 0; grp < NGL; ++grp) corr[grp] *= alpha;
           const float ae = __shfl_sync(0xffffffffu, alpha, 8 * t);
           const float ao = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
 #pragma unroll
-          for (int grp = 0; grp < NG; ++grp)
+          for (int grp = 0; grp < NGL; ++grp)
 #pragma unroll
             for (int mi = 0; mi < 2; ++mi) {
               o[grp][mi][0] *= ae;
@@ -608,7 +660,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
           }
         }
       };
-      if ((D <= 64 || (RS && D <= 128)) && T == 32 && nv == 32) {
+      if ((D <= 64 || (RS && D <= 128) || DS) && T == 32 && nv == 32) {
         // a whole 32-token unit: both chunks unrolled where registers allow it, no masks
         chunk(std::true_type{}, 0);
         chunk(std::true_type{}, 1);
@@ -626,9 +678,9 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
       const float le = __shfl_sync(0xffffffffu, l_run, 8 * t), lo = __shfl_sync(0xffffffffu, l_run, 8 * t + 4);
       // Offsets term of head g summed over the row's four lanes, then moved to the
       // lanes that hold heads 2t and 2t+1 in the O^T fragments.
-      float ce[NG], co[NG];
+      float ce[NGL], co[NGL];
 #pragma unroll
-      for (int grp = 0; grp < NG; ++grp) {
+      for (int grp = 0; grp < NGL; ++grp) {
         float c = corr[grp];
         c += __shfl_xor_sync(0xffffffffu, c, 1);
         c += __shfl_xor_sync(0xffffffffu, c, 2);
@@ -644,10 +696,10 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
         uint16_t* oe = P.out + ((size_t)b * P.Hq + (size_t)h * G + he) * D;
         uint16_t* oo = P.out + ((size_t)b * P.Hq + (size_t)h * G + ho) * D;
 #pragma unroll
-        for (int grp = 0; grp < NG; ++grp)
+        for (int grp = 0; grp < NGL; ++grp)
 #pragma unroll
           for (int mi = 0; mi < 2; ++mi) {
-            const int d0 = v_out_dim<Tr::VBITS>(grp, mi, 0, g), d1 = v_out_dim<Tr::VBITS>(grp, mi, 1, g);
+            const int d0 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 0, g), d1 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 1, g);
             if (he < G) {
               oe[d0] = f2bf(fmaf(o[grp][mi][0], fs[mi], ce[grp]) * ie);
               oe[d1] = f2bf(fmaf(o[grp][mi][2], fs[mi], ce[grp]) * ie);
@@ -660,19 +712,19 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
       } else {
         float* pe = partial_ptr(P, D, (size_t)blockIdx.x, b, (size_t)h * G + he);
         float* po = partial_ptr(P, D, (size_t)blockIdx.x, b, (size_t)h * G + ho);
-        if (he < G && g == 0) {
+        if (he < G && g == 0 && half == 0) {
           pe[0] = me;
           pe[1] = le;
         }
-        if (ho < G && g == 0) {
+        if (ho < G && g == 0 && half == 0) {
           po[0] = mo;
           po[1] = lo;
         }
 #pragma unroll
-        for (int grp = 0; grp < NG; ++grp)
+        for (int grp = 0; grp < NGL; ++grp)
 #pragma unroll
           for (int mi = 0; mi < 2; ++mi) {
-            const int d0 = v_out_dim<Tr::VBITS>(grp, mi, 0, g), d1 = v_out_dim<Tr::VBITS>(grp, mi, 1, g);
+            const int d0 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 0, g), d1 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 1, g);
             if (he < G) {
               pe[kPartialHeader + d0] = fmaf(o[grp][mi][0], fs[mi], ce[grp]);
               pe[kPartialHeader + d1] = fmaf(o[grp][mi][2], fs[mi], ce[grp]);
@@ -687,7 +739,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   }
 }
 
-template <int FMT, int D, int G, bool W128, bool RS>
+template <int FMT, int D, int G, bool W128, bool RS, bool DS>
 cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   using Tr = PackedTraits<FMT, D>;
   DecodeParams P;
@@ -708,14 +760,15 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   P.NS = a.n_stages;
   const int hkv = a.lv.hkv;
   P.stage_bytes = packed_stage_bytes(P.T, hkv * Tr::KB, hkv * Tr::VB, hkv * Tr::MB, a.Hq * D * 2);
-  auto kern = decode_packed_mma_kernel<FMT, D, G, W128, RS>;
+  auto kern = decode_packed_mma_kernel<FMT, D, G, W128, RS, DS>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int threads = RS ? 128 * (((hkv + 3) >> 2) + 1) : (hkv + 1) * 32;
+  const int ncons = DS ? 2 * hkv : hkv;
+  const int threads = RS ? 128 * (((ncons + 3) >> 2) + 1) : (ncons + 1) * 32;
   cudaError_t e = launch_with_pdl(kern, a.grid, threads, a.smem_bytes, a.stream, P);
   if (e != cudaSuccess) return e;
   return launch_combine<D>(P, a.grid, a.stream);
@@ -739,12 +792,17 @@ template <int FMT>
 cudaError_t launch_decode_packed_mma(const DecodeArgs& a) {
   const bool w128 = a.lv.box_bytes[0] == 128 && a.lv.box_bytes[1] == 128 && a.lv.box_bytes[2] == 128 &&
                     a.lv.box_bytes[3] == 128;
-#define PKV_CASE(DD, GG)                                                                             \
-  if (a.D == DD && a.G == GG) {                                                                      \
-    if (w128 && DD >= 128 && register_split_fits(decode_packed_mma_kernel<FMT, DD, GG, true, true>)) \
-      return launch_decode_packed_mma_t<FMT, DD, GG, true, true>(a);                                 \
-    return w128 ? launch_decode_packed_mma_t<FMT, DD, GG, true, false>(a)                            \
-                : launch_decode_packed_mma_t<FMT, DD, GG, false, false>(a);                          \
+#define PKV_CASE(DD, GG)                                                                                     \
+  if (a.D == DD && a.G == GG) {                                                                              \
+    if (DD == 256 && a.dim_split) {                                                                          \
+      if (register_split_fits(decode_packed_mma_kernel<FMT, 256, GG, true, true, true>))                    \
+        return launch_decode_packed_mma_t<FMT, 256, GG, true, true, true>(a);                                \
+      return launch_decode_packed_mma_t<FMT, 256, GG, true, false, true>(a);                                 \
+    }                                                                                                        \
+    if (w128 && DD >= 128 && register_split_fits(decode_packed_mma_kernel<FMT, DD, GG, true, true, false>))  \
+      return launch_decode_packed_mma_t<FMT, DD, GG, true, true, false>(a);                                  \
+    return w128 ? launch_decode_packed_mma_t<FMT, DD, GG, true, false, false>(a)                             \
+                : launch_decode_packed_mma_t<FMT, DD, GG, false, false, false>(a);                           \
   }
   PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
   PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)

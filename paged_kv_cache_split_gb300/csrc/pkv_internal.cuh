@@ -236,6 +236,7 @@ struct DecodeArgs {
   int n_stages;
   size_t smem_bytes;
   cudaStream_t stream;
+  int dim_split;        // see DecodePlan
 };
 
 // Returns cudaSuccess or the launch error.  Defined per format in decode_*.cu.
@@ -251,6 +252,7 @@ struct DecodePlan {
   size_t stage_bytes;
   size_t smem_bytes;
   int threads;
+  int dim_split;  // packed D = 256, at most 4 kv heads, 128-byte rows: two warps per kv head
 };
 bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan);
 

@@ -15,6 +15,11 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
   const size_t budget = 232448;  // 227 KB opt-in shared memory per block on sm_100-class parts
   size_t fixed = (size_t)(2 * B + 1 + 4) * 4 + 16 + 128 + 1024 * sizeof(void*);  // + staged slab table (kSmemTableEntries)
   if (packed) fixed += (size_t)hkv * G * D * 4;
+  // packed D = 256 with at most 4 kv heads and 128-byte rows: the dim split's partial
+  // logit buffers and pair barriers
+  const bool dim_split = packed && D == 256 && hkv <= 4 && (hkv * D * fb.k / 8) % 128 == 0 &&
+                         (hkv * D * fb.v / 8) % 128 == 0 && (hkv * (int)meta) % 128 == 0;
+  if (dim_split) fixed += (size_t)hkv * (2048 + 8);
   if (fixed >= budget) return false;
   if (!packed) {
     // Native bf16 (tensor-core kernel): T tokens of K and of V for all kv heads, as
@@ -36,6 +41,7 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
           plan->stage_bytes = stage;
           plan->smem_bytes = ns * stage + ns * 16 + fixed + 1024;
           plan->threads = (hkv + 1) * 32;
+          plan->dim_split = 0;
           return true;
         }
       }
@@ -61,7 +67,8 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
           plan->n_stages = (int)ns;
           plan->stage_bytes = stage;
           plan->smem_bytes = ns * stage + ns * 16 + fixed + 1024;
-          plan->threads = (hkv + 1) * 32;
+          plan->dim_split = dim_split;
+          plan->threads = ((dim_split ? 2 * hkv : hkv) + 1) * 32;
           return true;
         }
       }

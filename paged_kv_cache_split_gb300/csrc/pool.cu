@@ -503,6 +503,7 @@ pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, con
   a.grid = decode_grid(p);
   a.tokens_per_stage = plan.tokens_per_stage;
   a.n_stages = plan.n_stages;
+  a.dim_split = plan.dim_split;
   a.smem_bytes = plan.smem_bytes;
   a.stream = (cudaStream_t)stream;
   cudaError_t e;

@@ -104,6 +104,30 @@ def test_geometry_sweep(fmt, D, G):
     assert not got[0].any()  # empty sequence -> zeros
 
 
+@pytest.mark.parametrize("fmt", [wl.FMT_K4V4, wl.FMT_K8V4, wl.FMT_K8V8])
+@pytest.mark.parametrize("Hkv,G", [(2, 4), (4, 1), (4, 4)])
+def test_head_dim_256_two_warps_per_kv_head(fmt, Hkv, G):
+    """Packed D = 256 with 2 or 4 kv heads: each kv head's groups are split over two
+    warps that exchange partial logits every 16 tokens.  Lengths with full and ragged
+    units, sequences spread over many CTAs (partial records) or few (direct writes),
+    and the same bits on a second run."""
+    lens = [0, 1, 17, 32, 500, 2100]
+    rows, used = wl.fragmented_rows([wl.nblocks(L) for L in lens], wl.rng_for(11, Hkv, G))
+    w = wl.Workload(f"d256-{fmt}-{Hkv}-{G}", 1, Hkv * G, Hkv, 256, fmt, lens, rows, used, 1 / 16.0,
+                    0xD256, 5 + Hkv + G)
+    g, o, ol = make_pools(w)
+    fill(w, g, o, ol)
+    ref = o.decode_attention(0, w.q(0), w.block_table(), w.ctx(), w.scale)
+    for ctas in [2, 37, 0]:
+        g.decode_set_ctas(ctas)
+        a = _decode(w, g, 0)
+        assert np.array_equal(a, _decode(w, g, 0)), f"run-to-run difference with {ctas} CTAs"
+        compare(a, ref, f"{w.name} ctas={ctas}")
+        assert not a[0].any()
+    assert g.check_errors() == 0
+    assert o.inexact_rotations == 0
+
+
 def test_split_count_invariance_and_determinism():
     w = wl.llama_1b(wl.FMT_K8V4, B=5, lo=100, hi=3000)
     g, o, ol = make_pools(w)
