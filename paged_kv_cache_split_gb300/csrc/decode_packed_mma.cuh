@@ -214,12 +214,12 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   int32_t* UP = reinterpret_cast<int32_t*>(tab + kSmemTableEntries);
   int32_t* LS = UP + (B + 1);
   float* qscr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(LS + B) + 15) & ~uintptr_t(15));
-  // dim split: per kv head, each half's partial logits of the last two chunks, and
+  // dim split: per kv head, each half's partial logits (up to 32 tokens) of the last two exchanges, and
   // one mbarrier per kv head that pairs the two warps (bounded waits)
   float4* xbuf = reinterpret_cast<float4*>(qscr + (size_t)hkv * G * D);
-  uint64_t* pbar = reinterpret_cast<uint64_t*>(xbuf + (size_t)hkv * 2 * 2 * 32);
+  uint64_t* pbar = reinterpret_cast<uint64_t*>(xbuf + (size_t)hkv * 2 * 2 * 2 * 32);
 
-  decode_prologue(P, full, empty, NC, PW, UP, LS, tab);
+  decode_prologue(P, full, empty, NC * 32, PW, UP, LS, tab);  // every consumer lane arrives on empty
   if (DS && threadIdx.x == 0) {
     for (int i = 0; i < hkv; ++i) mbar_init(&pbar[i], 64);
     fence_mbar_init();
@@ -328,18 +328,17 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   uint32_t pphase = 0;     // dim split: phase of the pair barrier
   int xpar = 0;            // dim split: which partial-logit buffer this chunk uses
   float m_run = -INFINITY, l_run = 0.f;
-  bool dead = false;
   // dim split: every lane of both warps of the pair arrives, then waits (bounded) for
-  // the other warp; a warp that gave up (or was already dead) takes no further part,
-  // so its partner gives up at its next wait and no wait is ever repeated.
-  auto pair_sync = [&]() {
+  // the other warp.  False when the wait gave up: the warp then stops (returns), so
+  // its partner gives up at its next wait and no wait is ever repeated.
+  auto pair_sync = [&]() -> bool {
     if constexpr (DS) {
-      if (dead) return;
       mbar_arrive(&pbar[h]);
       const bool ok = mbar_wait_bounded(&pbar[h], pphase, err);
       pphase ^= 1;
-      dead = __any_sync(0xffffffffu, !ok);
+      return !__any_sync(0xffffffffu, !ok);
     }
+    return true;
   };
   const float scale24 = P.scale_log2 * 16777216.0f;
 
@@ -411,267 +410,305 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     }
   };
 
-  int b = find_seq(UP, B, u0);
-  int s = 0;           // stage of unit u
-  uint32_t phase = 0;  // parity of its full barrier
-  for (int32_t u = u0; u < u1; ++u, s = (s + 1 == NS) ? 0 : s + 1, phase ^= (s == 0)) {
-    while (u >= UP[b + 1]) ++b;
-    const bool seg_start = (u == u0) || (u == UP[b]);
-    const bool seg_end = (u == u1 - 1) || (u == UP[b + 1] - 1);
-    if (seg_start) {
+  // ---- the CTA's units, one sequence segment at a time ----
+  // Logits (unmasked, before the softmax scale) of NT n-tiles: tile jj holds tokens
+  // 16 kc0 + 8 jj + 2t + e of head g.  With the dim split both halves of every logit
+  // are added (in half order, by both warps).  False: a pair wait gave up.
+  auto logits = [&](auto nt_c, const uint32_t sb, const int kc0, float (&x)[4][2]) -> bool {
+    constexpr int NT = decltype(nt_c)::value;
+    uint32_t kw[4][NKC];  // word t of token 16kc + 8j + g, chunk c; tile jj = 2 (kc - kc0) + j
 #pragma unroll
-      for (int grp = 0; grp < NGL; ++grp) {
-        corr[grp] = 0.f;
+    for (int c2 = 0; c2 < NT / 2; ++c2) {
+      if constexpr (NKC == 2) {
+        uint32_t r4[4];
+        ldsm4(k_addr(sb, kc0 + c2, 0, 0), r4);
+        kw[2 * c2][0] = r4[0];
+        kw[2 * c2][1] = r4[1];
+        kw[2 * c2 + 1][0] = r4[2];
+        kw[2 * c2 + 1][1] = r4[3];
+      } else {
 #pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o[grp][mi][i] = 0.f;
-      }
-      m_run = -INFINITY;
-      l_run = 0.f;
-    }
-    const int32_t tok0 = (u - UP[b]) * T;
-    const int nv = min(T, LS[b] - tok0);
-    if (!dead && !mbar_wait_bounded(&full[s], phase, err)) dead = true;
-    dead = __shfl_sync(0xffffffffu, dead, 0);
-    const uint8_t* st = stages + (size_t)s * P.stage_bytes;
-    if (seg_start) pair_sync();  // the partner is done with the previous segment's q~
-    if (!dead && seg_start && half == 0) {
-      // q~ = H diag(s) q / sqrt(D) for this kv head's G query heads: a fast Walsh-
-      // Hadamard transform with lane l holding dims l + 32 r of one head (butterfly
-      // spans 1..16 across lanes, 32.. in registers), written to the warp's scratch.
-      constexpr int R = D / 32;
-      const uint16_t* qsm = reinterpret_cast<const uint16_t*>(st + offQ) + (size_t)h * G * D;
-      float sg[R];
+          for (int cs = 0; cs < KCS; ++cs) {
+            uint32_t r4[4];
+            ldsm4(k_addr(sb, kc0 + c2, j, cs), r4);
 #pragma unroll
-      for (int r = 0; r < R; ++r) sg[r] = P.signs[lane + 32 * r];
-#pragma unroll 1
-      for (int gg = 0; gg < G; ++gg) {
-        float v[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) v[r] = __uint_as_float((uint32_t)qsm[gg * D + lane + 32 * r] << 16) * sg[r];
-#pragma unroll
-        for (int hs = 1; hs < 32; hs <<= 1) {
-          const float sgn = (lane & hs) ? -1.f : 1.f;  // upper element: x - y; lower: x + y
-#pragma unroll
-          for (int r = 0; r < R; ++r) v[r] = fmaf(sgn, v[r], __shfl_xor_sync(0xffffffffu, v[r], hs));
-        }
-#pragma unroll
-        for (int hr = 1; hr < R; hr <<= 1)
-#pragma unroll
-          for (int r = 0; r < R; ++r)
-            if ((r & hr) == 0) {
-              const float x = v[r], y = v[r + hr];
-              v[r] = x + y;
-              v[r + hr] = x - y;
-            }
-#pragma unroll
-        for (int r = 0; r < R; ++r) qs[gg * D + lane + 32 * r] = v[r];
-      }
-    }
-    if (seg_start) pair_sync();  // q~ of this segment is in qs
-    if (!dead && seg_start) {
-      __syncwarp();
-#pragma unroll
-      for (int grp = 0; grp < NGL; ++grp) {
-        float tsum = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            float v[2];
-            bool d16 = false;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int dd = 32 * (gofs + grp) + k_dim<Tr::KBITS>(t, ks, r, hh, d16);
-              const float qv = g < G ? qs[g * D + dd] * P.inv_sqrt_d : 0.f;
-              v[hh] = d16 ? qv * 0.0625f : qv;
-            }
-            qa[grp][ks][r] = pack_f16x2(v[0], v[1]);
-            const float2 back = unpack_f16x2(qa[grp][ks][r]);  // the values the MMA sees
-            tsum += d16 ? 16.f * (back.x + back.y) : (back.x + back.y);
+            for (int m = 0; m < 4; ++m) kw[2 * c2 + j][4 * cs + m] = r4[m];
           }
-        tsum += __shfl_xor_sync(0xffffffffu, tsum, 1);
-        tsum += __shfl_xor_sync(0xffffffffu, tsum, 2);
-        qsum[grp] = tsum * 5.9604644775390625e-08f;  // 2^-24
       }
-      __syncwarp();
     }
-    if (!dead) {
-      const uint32_t sb = smem_u32(st);
-      // One 16-token chunk; kFull: all 16 tokens are inside the context (no mask).
-      auto chunk = [&](auto full_c, const int kc) {
-        constexpr bool kFull = decltype(full_c)::value;
-        // ---- logits for 16 tokens: n-tiles (token halves) j = 0, 1 ----
-        uint32_t kw[2][NKC];  // word t of token 16kc + 8j + g, chunk c
-        if constexpr (NKC == 2) {
+#pragma unroll
+    for (int jj = 0; jj < NT; ++jj) {
+      const int kc = kc0 + (jj >> 1), j = jj & 1;
+      float sa0 = 0.f, sa1 = 0.f;
+#pragma unroll
+      for (int cm = 0; cm < NMC; ++cm) {
+        const float4 m0 = lds128(m_addr(sb, 2, kc, j, 0, cm));  // token 8j + 2t
+        const float4 m1 = lds128(m_addr(sb, 2, kc, j, 1, cm));  // token 8j + 2t + 1
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int grp = 2 * cm + q2;
+          uint32_t bfr[2][2];
+          if constexpr (Tr::KBITS == 4) {
+            k_group_frags4(kw[jj][grp], bfr);
+          } else {
+            k_group_frags8(kw[jj][2 * grp], kw[jj][2 * grp + 1], bfr);
+          }
+          float cacc[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_f16_16816(cacc, qa[grp][0][0], 0u, qa[grp][0][1], 0u, bfr[0][0], bfr[0][1]);
+          mma_f16_16816(cacc, qa[grp][1][0], 0u, qa[grp][1][1], 0u, bfr[1][0], bfr[1][1]);
+          sa0 = fmaf(q2 ? m0.z : m0.x, cacc[0], fmaf(q2 ? m0.w : m0.y, qsum[grp], sa0));
+          sa1 = fmaf(q2 ? m1.z : m1.x, cacc[1], fmaf(q2 ? m1.w : m1.y, qsum[grp], sa1));
+        }
+      }
+      x[jj][0] = sa0;
+      x[jj][1] = sa1;
+    }
+    if constexpr (DS) {
+#pragma unroll
+      for (int q4 = 0; q4 < NT / 2; ++q4)
+        xbuf[((((size_t)h * 2 + half) * 2 + xpar) * 2 + q4) * 32 + lane] =
+            make_float4(x[2 * q4][0], x[2 * q4][1], x[2 * q4 + 1][0], x[2 * q4 + 1][1]);
+      if (!pair_sync()) return false;
+#pragma unroll
+      for (int q4 = 0; q4 < NT / 2; ++q4) {
+        const float4 pr = xbuf[((((size_t)h * 2 + (half ^ 1)) * 2 + xpar) * 2 + q4) * 32 + lane];
+        float* x0 = x[2 * q4];
+        float* x1 = x[2 * q4 + 1];
+        x0[0] = half ? pr.x + x0[0] : x0[0] + pr.x;
+        x0[1] = half ? pr.y + x0[1] : x0[1] + pr.y;
+        x1[0] = half ? pr.z + x1[0] : x1[0] + pr.z;
+        x1[1] = half ? pr.w + x1[1] : x1[1] + pr.w;
+      }
+      xpar ^= 1;
+    }
+    return true;
+  };
+  // Online softmax of head g over NT tiles: x (scaled, masked) -> probabilities p.
+  auto softmax = [&](auto nt_c, float (&x)[4][2], float (&p)[4][2]) {
+    constexpr int NT = decltype(nt_c)::value;
+    float mx = fmaxf(x[0][0], x[0][1]);
+#pragma unroll
+    for (int jj = 1; jj < NT; ++jj) mx = fmaxf(mx, fmaxf(x[jj][0], x[jj][1]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const bool grow = mx > m_run;
+    if (__any_sync(0xffffffffu, grow)) {
+      const float alpha = grow ? ex2(m_run - mx) : 1.0f;
+      if (grow) m_run = mx;
+      l_run *= alpha;
+#pragma unroll
+      for (int grp = 0; grp < NGL; ++grp) corr[grp] *= alpha;
+      const float ae = __shfl_sync(0xffffffffu, alpha, 8 * t);
+      const float ao = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+#pragma unroll
+      for (int grp = 0; grp < NGL; ++grp)
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi) {
+          o[grp][mi][0] *= ae;
+          o[grp][mi][2] *= ae;
+          o[grp][mi][1] *= ao;
+          o[grp][mi][3] *= ao;
+        }
+    }
+#pragma unroll
+    for (int jj = 0; jj < NT; ++jj)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) p[jj][e] = ex2(x[jj][e] - m_run);
+    float ls = p[0][0] + p[0][1];
+#pragma unroll
+    for (int jj = 1; jj < NT; ++jj) ls += p[jj][0] + p[jj][1];
+    l_run += ls;
+  };
+  // O^T += V^T (P S)^T over the 16 tokens of chunk kc (tiles p[jp], p[jp + 1]); offsets into corr.
+  auto pv = [&](const uint32_t sb, const int kc, const float (&p)[4][2], const int jp) {
+    uint32_t vx[2][NVC];  // half-word g of tokens 16kc + 8pp + 2t, +1; chunk c
+    if constexpr (NVC == 2) {
+      uint32_t r4[4];
+      ldsm4_t(v_addr(sb, kc, 0, 0), r4);
+      vx[0][0] = r4[0];
+      vx[0][1] = r4[1];
+      vx[1][0] = r4[2];
+      vx[1][1] = r4[3];
+    } else {
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+        for (int cs = 0; cs < VCS; ++cs) {
           uint32_t r4[4];
-          ldsm4(k_addr(sb, kc, 0, 0), r4);
-          kw[0][0] = r4[0];
-          kw[0][1] = r4[1];
-          kw[1][0] = r4[2];
-          kw[1][1] = r4[3];
+          ldsm4_t(v_addr(sb, kc, pp, cs), r4);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) vx[pp][4 * cs + m] = r4[m];
+        }
+    }
+#pragma unroll
+    for (int cm = 0; cm < NMC; ++cm) {
+      float4 mv[2][2];  // token 8pp + 2t + e
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) mv[pp][e] = lds128(m_addr(sb, 3, kc, pp, e, cm));
+#pragma unroll
+      for (int q2 = 0; q2 < 2; ++q2) {
+        const int grp = 2 * cm + q2;
+        float sv[2][2], ov[2][2];
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            sv[pp][e] = q2 ? mv[pp][e].z : mv[pp][e].x;
+            ov[pp][e] = q2 ? mv[pp][e].w : mv[pp][e].y;
+          }
+        const float* p0 = p[jp];
+        const float* p1 = p[jp + 1];
+        const uint32_t pb0 = pack_f16x2(p0[0] * sv[0][0], p0[1] * sv[0][1]);
+        const uint32_t pb1 = pack_f16x2(p1[0] * sv[1][0], p1[1] * sv[1][1]);
+        corr[grp] = fmaf(p0[0], ov[0][0], fmaf(p0[1], ov[0][1], fmaf(p1[0], ov[1][0], fmaf(p1[1], ov[1][1], corr[grp]))));
+        if constexpr (Tr::VBITS == 4) {
+          const uint32_t x01 = vx[0][grp], x23 = vx[1][grp];
+          const uint32_t y01 = x01 >> 8, y23 = x23 >> 8;
+          mma_f16_16816(o[grp][0], x01 & 0x000F000Fu, y01 & 0x000F000Fu, x23 & 0x000F000Fu, y23 & 0x000F000Fu, pb0,
+                        pb1);
+          mma_f16_16816(o[grp][1], x01 & 0x00F000F0u, y01 & 0x00F000F0u, x23 & 0x00F000F0u, y23 & 0x00F000F0u, pb0,
+                        pb1);
         } else {
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int cs = 0; cs < KCS; ++cs) {
-              uint32_t r4[4];
-              ldsm4(k_addr(sb, kc, j, cs), r4);
-#pragma unroll
-              for (int m = 0; m < 4; ++m) kw[j][4 * cs + m] = r4[m];
-            }
-        }
-        float x[2][2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float sa0 = 0.f, sa1 = 0.f;
-#pragma unroll
-          for (int cm = 0; cm < NMC; ++cm) {
-            const float4 m0 = lds128(m_addr(sb, 2, kc, j, 0, cm));  // token 8j + 2t
-            const float4 m1 = lds128(m_addr(sb, 2, kc, j, 1, cm));  // token 8j + 2t + 1
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-              const int grp = 2 * cm + q2;
-              uint32_t bfr[2][2];
-              if constexpr (Tr::KBITS == 4) {
-                k_group_frags4(kw[j][grp], bfr);
-              } else {
-                k_group_frags8(kw[j][2 * grp], kw[j][2 * grp + 1], bfr);
-              }
-              float cacc[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_f16_16816(cacc, qa[grp][0][0], 0u, qa[grp][0][1], 0u, bfr[0][0], bfr[0][1]);
-              mma_f16_16816(cacc, qa[grp][1][0], 0u, qa[grp][1][1], 0u, bfr[1][0], bfr[1][1]);
-              sa0 = fmaf(q2 ? m0.z : m0.x, cacc[0], fmaf(q2 ? m0.w : m0.y, qsum[grp], sa0));
-              sa1 = fmaf(q2 ? m1.z : m1.x, cacc[1], fmaf(q2 ? m1.w : m1.y, qsum[grp], sa1));
-            }
+          for (int mi = 0; mi < 2; ++mi) {
+            const uint32_t x01 = vx[0][2 * grp + mi], x23 = vx[1][2 * grp + mi];
+            mma_f16_16816(o[grp][mi], __byte_perm(x01, 0u, 0x4240), __byte_perm(x01, 0u, 0x4341),
+                          __byte_perm(x23, 0u, 0x4240), __byte_perm(x23, 0u, 0x4341), pb0, pb1);
           }
-          x[j][0] = sa0;
-          x[j][1] = sa1;
         }
-        if constexpr (DS) {
-          // both halves of every logit, added in half order by both warps
-          xbuf[(((size_t)h * 2 + half) * 2 + xpar) * 32 + lane] = make_float4(x[0][0], x[0][1], x[1][0], x[1][1]);
-          pair_sync();
-          const float4 pr = xbuf[(((size_t)h * 2 + (half ^ 1)) * 2 + xpar) * 32 + lane];
-          xpar ^= 1;
-          x[0][0] = half ? pr.x + x[0][0] : x[0][0] + pr.x;
-          x[0][1] = half ? pr.y + x[0][1] : x[0][1] + pr.y;
-          x[1][0] = half ? pr.z + x[1][0] : x[1][0] + pr.z;
-          x[1][1] = half ? pr.w + x[1][1] : x[1][1] + pr.w;
-        }
+      }
+    }
+  };
+  // A whole 32-token unit (both chunks, one softmax, no masks) where registers allow it.
+  constexpr bool kUnit32 = D <= 64 || (RS && D <= 128) || DS;
+
+  int b = find_seq(UP, B, u0);
+  int s = 0;           // stage of the next unit
+  uint32_t phase = 0;  // parity of its full barrier
+  for (int32_t ua = u0; ua < u1;) {
+    while (ua >= UP[b + 1]) ++b;
+    const int32_t ue = min(u1, UP[b + 1]);  // this segment: units [ua, ue) of sequence b
+    const int32_t Lb = LS[b];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          if constexpr (kFull) {
-            x[j][0] *= scale24;
-            x[j][1] *= scale24;
-          } else {
+    for (int grp = 0; grp < NGL; ++grp) {
+      corr[grp] = 0.f;
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[grp][mi][i] = 0.f;
+    }
+    m_run = -INFINITY;
+    l_run = 0.f;
+    for (int32_t u = ua; u < ue; ++u) {
+      {
+        const bool ok = mbar_wait_bounded(&full[s], phase, err);
+        if (__any_sync(0xffffffffu, !ok)) return;  // a wait gave up: stop (no wait is repeated)
+      }
+      const uint8_t* st = stages + (size_t)s * P.stage_bytes;
+      const uint32_t sb = smem_u32(st);
+      if (u == ua) {
+        if (half == 0) {
+          // q~ = H diag(s) q / sqrt(D) for this kv head's G query heads: a fast Walsh-
+          // Hadamard transform with lane l holding dims l + 32 r of one head (butterfly
+          // spans 1..16 across lanes, 32.. in registers), written to the head's scratch.
+          constexpr int R = D / 32;
+          const uint16_t* qsm = reinterpret_cast<const uint16_t*>(st + offQ) + (size_t)h * G * D;
+          float sg[R];
+#pragma unroll
+          for (int r = 0; r < R; ++r) sg[r] = P.signs[lane + 32 * r];
+#pragma unroll 1
+          for (int gg = 0; gg < G; ++gg) {
+            float v[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) v[r] = __uint_as_float((uint32_t)qsm[gg * D + lane + 32 * r] << 16) * sg[r];
+#pragma unroll
+            for (int hs = 1; hs < 32; hs <<= 1) {
+              const float sgn = (lane & hs) ? -1.f : 1.f;  // upper element: x - y; lower: x + y
+#pragma unroll
+              for (int r = 0; r < R; ++r) v[r] = fmaf(sgn, v[r], __shfl_xor_sync(0xffffffffu, v[r], hs));
+            }
+#pragma unroll
+            for (int hr = 1; hr < R; hr <<= 1)
+#pragma unroll
+              for (int r = 0; r < R; ++r)
+                if ((r & hr) == 0) {
+                  const float x = v[r], y = v[r + hr];
+                  v[r] = x + y;
+                  v[r + hr] = x - y;
+                }
+#pragma unroll
+            for (int r = 0; r < R; ++r) qs[gg * D + lane + 32 * r] = v[r];
+          }
+        }
+        // q~ of this segment is in qs (dim split: written by the pair's first warp;
+        // the partner's reads of the previous segment's q~ preceded at least one
+        // exchange since)
+        if (!pair_sync()) return;
+        __syncwarp();
+#pragma unroll
+        for (int grp = 0; grp < NGL; ++grp) {
+          float tsum = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              float v[2];
+              bool d16 = false;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int dd = 32 * (gofs + grp) + k_dim<Tr::KBITS>(t, ks, r, hh, d16);
+                const float qv = g < G ? qs[g * D + dd] * P.inv_sqrt_d : 0.f;
+                v[hh] = d16 ? qv * 0.0625f : qv;
+              }
+              qa[grp][ks][r] = pack_f16x2(v[0], v[1]);
+              const float2 back = unpack_f16x2(qa[grp][ks][r]);  // the values the MMA sees
+              tsum += d16 ? 16.f * (back.x + back.y) : (back.x + back.y);
+            }
+          tsum += __shfl_xor_sync(0xffffffffu, tsum, 1);
+          tsum += __shfl_xor_sync(0xffffffffu, tsum, 2);
+          qsum[grp] = tsum * 5.9604644775390625e-08f;  // 2^-24
+        }
+        __syncwarp();
+      }
+      const int nv = min(T, Lb - (u - UP[b]) * T);
+      if (kUnit32 && T == 32 && nv == 32) {
+        float x[4][2], p[4][2];
+        if (!logits(std::integral_constant<int, 4>{}, sb, 0, x)) return;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          x[jj][0] *= scale24;
+          x[jj][1] *= scale24;
+        }
+        softmax(std::integral_constant<int, 4>{}, x, p);
+        pv(sb, 0, p, 0);
+        pv(sb, 1, p, 2);
+      } else {
+        for (int kc = 0; kc * 16 < nv; ++kc) {
+          float x[4][2], p[4][2];
+          if (!logits(std::integral_constant<int, 2>{}, sb, kc, x)) return;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
             const int tk = kc * 16 + 8 * j + 2 * t;
             x[j][0] = tk < nv ? x[j][0] * scale24 : -INFINITY;
             x[j][1] = tk + 1 < nv ? x[j][1] * scale24 : -INFINITY;
           }
+          softmax(std::integral_constant<int, 2>{}, x, p);
+          pv(sb, kc, p, 0);
         }
-        // ---- online softmax for head g ----
-        float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const bool grow = mx > m_run;
-        if (__any_sync(0xffffffffu, grow)) {
-          const float alpha = grow ? ex2(m_run - mx) : 1.0f;
-          if (grow) m_run = mx;
-          l_run *= alpha;
-#pragma unroll
-          for (int grp = 0; grp < NGL; ++grp) corr[grp] *= alpha;
-          const float ae = __shfl_sync(0xffffffffu, alpha, 8 * t);
-          const float ao = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
-#pragma unroll
-          for (int grp = 0; grp < NGL; ++grp)
-#pragma unroll
-            for (int mi = 0; mi < 2; ++mi) {
-              o[grp][mi][0] *= ae;
-              o[grp][mi][2] *= ae;
-              o[grp][mi][1] *= ao;
-              o[grp][mi][3] *= ao;
-            }
-        }
-        float p[2][2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) p[j][e] = ex2(x[j][e] - m_run);
-        l_run += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
-        // ---- O^T += V^T (P S)^T over these 16 tokens; offsets into corr ----
-        uint32_t vx[2][NVC];  // half-word g of tokens 16kc + 8p + 2t, +1; chunk c
-        if constexpr (NVC == 2) {
-          uint32_t r4[4];
-          ldsm4_t(v_addr(sb, kc, 0, 0), r4);
-          vx[0][0] = r4[0];
-          vx[0][1] = r4[1];
-          vx[1][0] = r4[2];
-          vx[1][1] = r4[3];
-        } else {
-#pragma unroll
-          for (int pp = 0; pp < 2; ++pp)
-#pragma unroll
-            for (int cs = 0; cs < VCS; ++cs) {
-              uint32_t r4[4];
-              ldsm4_t(v_addr(sb, kc, pp, cs), r4);
-#pragma unroll
-              for (int m = 0; m < 4; ++m) vx[pp][4 * cs + m] = r4[m];
-            }
-        }
-#pragma unroll
-        for (int cm = 0; cm < NMC; ++cm) {
-          float4 mv[2][2];  // token 8pp + 2t + e
-#pragma unroll
-          for (int pp = 0; pp < 2; ++pp)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) mv[pp][e] = lds128(m_addr(sb, 3, kc, pp, e, cm));
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            const int grp = 2 * cm + q2;
-            float sv[2][2], ov[2][2];
-#pragma unroll
-            for (int pp = 0; pp < 2; ++pp)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                sv[pp][e] = q2 ? mv[pp][e].z : mv[pp][e].x;
-                ov[pp][e] = q2 ? mv[pp][e].w : mv[pp][e].y;
-              }
-            const uint32_t pb0 = pack_f16x2(p[0][0] * sv[0][0], p[0][1] * sv[0][1]);
-            const uint32_t pb1 = pack_f16x2(p[1][0] * sv[1][0], p[1][1] * sv[1][1]);
-            corr[grp] = fmaf(p[0][0], ov[0][0],
-                             fmaf(p[0][1], ov[0][1], fmaf(p[1][0], ov[1][0], fmaf(p[1][1], ov[1][1], corr[grp]))));
-            if constexpr (Tr::VBITS == 4) {
-              const uint32_t x01 = vx[0][grp], x23 = vx[1][grp];
-              const uint32_t y01 = x01 >> 8, y23 = x23 >> 8;
-              mma_f16_16816(o[grp][0], x01 & 0x000F000Fu, y01 & 0x000F000Fu, x23 & 0x000F000Fu, y23 & 0x000F000Fu,
-                            pb0, pb1);
-              mma_f16_16816(o[grp][1], x01 & 0x00F000F0u, y01 & 0x00F000F0u, x23 & 0x00F000F0u, y23 & 0x00F000F0u,
-                            pb0, pb1);
-            } else {
-#pragma unroll
-              for (int mi = 0; mi < 2; ++mi) {
-                const uint32_t x01 = vx[0][2 * grp + mi], x23 = vx[1][2 * grp + mi];
-                mma_f16_16816(o[grp][mi], __byte_perm(x01, 0u, 0x4240), __byte_perm(x01, 0u, 0x4341),
-                              __byte_perm(x23, 0u, 0x4240), __byte_perm(x23, 0u, 0x4341), pb0, pb1);
-              }
-            }
-          }
-        }
-      };
-      if ((D <= 64 || (RS && D <= 128) || DS) && T == 32 && nv == 32) {
-        // a whole 32-token unit: both chunks unrolled where registers allow it, no masks
-        chunk(std::true_type{}, 0);
-        chunk(std::true_type{}, 1);
-      } else {
-        for (int kc = 0; kc * 16 < nv; ++kc) chunk(std::false_type{}, kc);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      mbar_arrive(&empty[s]);  // every lane: its reads of the stage are done
+      if (++s == NS) {
+        s = 0;
+        phase ^= 1;
+      }
     }
 
-    if (seg_end) {
+    // ---- end of the segment: output rows, or a partial record for the combine ----
+    {
       l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
       l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
       const float me = __shfl_sync(0xffffffffu, m_run, 8 * t), mo = __shfl_sync(0xffffffffu, m_run, 8 * t + 4);
@@ -736,6 +773,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
           }
       }
     }
+    ua = ue;
   }
 }
 

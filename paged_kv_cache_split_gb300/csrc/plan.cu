@@ -19,7 +19,7 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
   // logit buffers and pair barriers
   const bool dim_split = packed && D == 256 && hkv <= 4 && (hkv * D * fb.k / 8) % 128 == 0 &&
                          (hkv * D * fb.v / 8) % 128 == 0 && (hkv * (int)meta) % 128 == 0;
-  if (dim_split) fixed += (size_t)hkv * (2048 + 8);
+  if (dim_split) fixed += (size_t)hkv * (4096 + 8);
   if (fixed >= budget) return false;
   if (!packed) {
     // Native bf16 (tensor-core kernel): T tokens of K and of V for all kv heads, as
