@@ -28,7 +28,8 @@ struct DecodeParams {
 };
 
 constexpr int kMaxConsumerWarps = 8;
-constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
+constexpr int kProducerWarps = 2;
+constexpr int kMaxThreads = (kMaxConsumerWarps + kProducerWarps) * 32;
 
 // 2^x with the hardware approximation (relative error below 2^-22; results below
 // 2^-126 flush to zero, which a softmax weight can drop).
@@ -51,8 +52,9 @@ __device__ __forceinline__ int find_seq(const int32_t* UP, int B, int32_t u) {
 }
 
 // Prologue of every decode kernel: thread 0 initialises the stage barriers (full:
-// one producer arrival plus the copied bytes; empty: one arrival per consumer
-// warp) and warp 0 builds the unit prefix UP[0..B] over sequences (unit = T tokens
+// one producer arrival plus the copied bytes; empty: NC consumer arrivals, one per
+// consumer warp or lane as the kernel counts them) and the producers' two issue-token
+// barriers, and warp 0 builds the unit prefix UP[0..B] over sequences (unit = T tokens
 // of one sequence) and LS[b], the context length clamped to the block table.  The
 // caller runs __syncthreads() afterwards.
 //
@@ -138,7 +140,8 @@ __device__ __forceinline__ void prefetch_first_units(const DecodeParams& P, int 
 }
 
 __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t* full, uint64_t* empty, int NC,
-                                                int PW, int32_t* UP, int32_t* LS, const uint8_t** tab) {
+                                                int PW, int32_t* UP, int32_t* LS, const uint8_t** tab,
+                                                uint64_t* tok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = smem_table_entries(P);
   for (int i = threadIdx.x; i < nt; i += blockDim.x) {
@@ -156,6 +159,8 @@ __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t*
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NC);
     }
+    mbar_init(&tok[0], 1);
+    mbar_init(&tok[1], 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -183,6 +188,96 @@ __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t*
       carry += __shfl_sync(0xffffffffu, inc, 31);
     }
     if (lane == 0) UP[P.B] = carry;
+  }
+}
+
+// Producer side of the stage ring, run by NPW (1 or 2) warps that take turns over
+// batches of 32 units (warp pw takes batches pw, pw + NPW, ...).  For its batch a
+// warp reads the block table lane by lane and acquires each unit's tensor maps in
+// the lane that will issue that unit's copies.  With two warps it then takes the
+// issue token from the other warp (one mbarrier per batch parity, so units enter the
+// ring in order and never more than one round ahead of the consumers), issues the
+// batch in unit order and hands the token on: while one warp issues, the other
+// prepares its next batch, which keeps the table reads and the fence latency off
+// the issue path.  issue(s, stage, map, y0, ok, qsrc) arms full[s] with the unit's
+// bytes and issues its copies.  Every wait is bounded: a warp that gives up stops,
+// so the other gives up at its next token wait.
+template <int D, int NPW, typename IssueFn>
+__device__ __forceinline__ void run_producer(const DecodeParams& P, const int pw, const int32_t u0, const int32_t u1,
+                                             const int32_t* UP, const uint8_t* const* tab, uint64_t* full,
+                                             uint64_t* empty, uint64_t* tok, uint8_t* stages,
+                                             IssueFn&& issue) {
+  const int lane = threadIdx.x & 31;
+  const int NS = P.NS, B = P.B, T = P.T;
+  int32_t* err = P.lv.err;
+  const bool use_stab = smem_table_entries(P) > 0;
+  const int n_batches = (u1 - u0 + 31) >> 5;
+  int issued = 0;  // units in the ring when this warp stopped as the last issuer (0: not the last)
+  for (int k = pw; k < n_batches; k += NPW) {
+    const int32_t ub = u0 + 32 * k;
+    const int32_t u = ub + lane;
+    const uint8_t* map = nullptr;   // tensor maps of the unit's slab (kind k at + 128 k)
+    const uint8_t* qsrc = nullptr;  // q of its sequence when the unit starts a CTA's segment
+    int y0 = 0, ok = 0;             // first slab row of the unit; row valid
+    if (u < u1) {
+      const int bb = find_seq(UP, B, u);
+      if (u == u0 || u == UP[bb]) qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)bb * P.Hq * D);
+      const int32_t t0 = (u - UP[bb]) * T;
+      const int j = t0 / kBlockTokens, slot0 = t0 % kBlockTokens;
+      const int32_t row = P.bt[(size_t)bb * P.max_blocks + j];
+      if (row >= 0 && (int64_t)row < P.lv.rows_capacity) {
+        const int32_t slab = row / P.lv.slab_blocks;
+        const int32_t r = row - slab * P.lv.slab_blocks;
+        const uint8_t* ent0 =
+            use_stab ? tab[(size_t)slab * P.lv.n_kinds] : P.lv.tab.base[(size_t)slab * P.lv.tab.stride];
+        map = ent0 + P.lv.map_delta;
+        y0 = r * kBlockTokens + slot0;
+        ok = 1;
+        for (int kk = 0; kk < P.lv.n_kinds; ++kk) tensormap_acquire(map + kk * 128);
+      } else {
+        atomicOr(err, ERR_ROW);
+      }
+    }
+    if (NPW == 2 && k > 0) {
+      const bool got = mbar_wait_bounded(&tok[k & 1], ((k - 1) >> 1) & 1, err);
+      if (__any_sync(0xffffffffu, !got)) return;  // the other warp stopped; nothing of this warp is in flight
+    }
+    const int cnt = min(32, u1 - ub);
+    int n = 32 * k;           // ring position of unit ub
+    int s = n % NS;           // its stage
+    uint32_t ph = (n / NS) & 1;  // parity of that stage's round
+    bool dead = false;
+    for (int i = 0; i < cnt; ++i, ++n) {
+      int bad = 0;
+      if (lane == i) {
+        if (n >= NS && !mbar_wait_bounded(&empty[s], ph ^ 1, err))
+          bad = 1;
+        else
+          issue(s, stages + (size_t)s * P.stage_bytes, map, y0, ok, qsrc);
+      }
+      if (__any_sync(0xffffffffu, bad)) {
+        dead = true;
+        break;
+      }
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+    if (dead || k + 1 >= n_batches) {
+      issued = n;
+      break;
+    }
+    if (NPW == 2) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tok[(k + 1) & 1]);
+    }
+  }
+  // The last issuer (or the warp that gave up while holding the token) leaves no
+  // copy in flight into a stage that is no longer waited on.
+  if (issued > 0 && lane == 0) {
+    const int first = issued > NS ? issued - NS : 0;
+    for (int m = first; m < issued; ++m) mbar_wait_bounded(&full[m % NS], (m / NS) & 1, err);
   }
 }
 

@@ -75,8 +75,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   const uint8_t** tab = reinterpret_cast<const uint8_t**>(empty + NS);  // [kSmemTableEntries]
   int32_t* UP = reinterpret_cast<int32_t*>(tab + kSmemTableEntries);
   int32_t* LS = UP + (B + 1);
+  uint64_t* tok = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(LS + B) + 7) & ~uintptr_t(7));
 
-  decode_prologue(P, full, empty, NC, NC, UP, LS, tab);
+  decode_prologue(P, full, empty, NC, NC, UP, LS, tab, tok);
   __syncthreads();
   const int32_t U = UP[B];
   const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
@@ -90,71 +91,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   const int QB = P.Hq * D * 2;
 
   if (warp == NC) {
-    // ----------------------------- producer ---------------------------------
-    const bool use_stab = smem_table_entries(P) > 0;
+    // ----------------------------- producers --------------------------------
+    // A whole unit is always copied (T tokens stay inside the block); tokens past
+    // the context are masked by a zero probability.  A unit that starts a CTA's
+    // segment of a sequence also brings that sequence's q.
     const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once
-    int issued = 0;
-    int ps = 0;           // stage of unit `issued`
-    uint32_t pphase = 0;  // parity of that stage's current round
-    bool dead = false;
-    for (int32_t ub = u0; ub < u1 && !dead; ub += 32) {
-      const int32_t u = ub + lane;
-      const uint8_t* map = nullptr;   // tensor maps of the unit's slab: K, then V at + 128
-      const uint8_t* qsrc = nullptr;  // q of its sequence when the unit starts a CTA's segment
-      int y0 = 0, ok = 0;             // first slab row of the unit; row valid
-      if (u < u1) {
-        const int bb = find_seq(UP, B, u);
-        if (u == u0 || u == UP[bb]) qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)bb * P.Hq * D);
-        const int32_t tok0 = (u - UP[bb]) * T;
-        const int j = tok0 / kBlockTokens, slot0 = tok0 % kBlockTokens;
-        const int32_t row = P.bt[(size_t)bb * P.max_blocks + j];
-        if (row >= 0 && (int64_t)row < P.lv.rows_capacity) {
-          const int32_t slab = row / P.lv.slab_blocks;
-          const int32_t r = row - slab * P.lv.slab_blocks;
-          const uint8_t* ent0 =
-              use_stab ? tab[(size_t)slab * P.lv.n_kinds] : P.lv.tab.base[(size_t)slab * P.lv.tab.stride];
-          map = ent0 + P.lv.map_delta;
-          y0 = r * kBlockTokens + slot0;
-          ok = 1;
-          tensormap_acquire(map);
-          tensormap_acquire(map + 128);
-        } else {
-          atomicOr(err, ERR_ROW);
-        }
-      }
-      const int cnt = min(32, u1 - ub);
-      for (int i = 0; i < cnt; ++i, ++issued, ps = (ps + 1 == NS) ? 0 : ps + 1, pphase ^= (ps == 0)) {
-        int bad = 0;
-        if (lane == i) {
-          const int s = ps;
-          if (issued >= NS && !mbar_wait_bounded(&empty[s], pphase ^ 1, err)) {
-            bad = 1;
-          } else {
-            // A whole unit is always copied (T tokens stay inside the block); tokens
-            // past the context are masked by a zero probability.  A unit that starts
-            // a sequence also brings that sequence's q.
-            mbar_arrive_expect_tx(&full[s], (ok ? (uint32_t)(2 * T * ROW) : 0u) + (qsrc ? (uint32_t)QB : 0u));
-            uint8_t* st = stages + (size_t)s * P.stage_bytes;
-            if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, &full[s]);
-            if (ok) {
-              for (int cy = 0; cy < T / 16; ++cy) {
-                tma_load_3d(st + cy * 16 * ROW, map, 0, y0 + 16 * cy, 0, &full[s], kv_policy);
-                tma_load_3d(st + offV + cy * 16 * ROW, map + 128, 0, y0 + 16 * cy, 0, &full[s], kv_policy);
-              }
-            }
-          }
-        }
-        if (__any_sync(0xffffffffu, bad)) {
-          dead = true;
-          break;
-        }
-      }
-    }
-    // After a timeout, leave no copy in flight into a stage that is no longer waited on.
-    if (lane == 0) {
-      const int first = issued > NS ? issued - NS : 0;
-      for (int n = first; n < issued; ++n) mbar_wait_bounded(&full[n % NS], (n / NS) & 1, err);
-    }
+    run_producer<D, 1>(P, 0, u0, u1, UP, tab, full, empty, tok, stages,
+                    [&](int s, uint8_t* st, const uint8_t* map, int y0, int ok, const uint8_t* qsrc) {
+                      mbar_arrive_expect_tx(&full[s], (ok ? (uint32_t)(2 * T * ROW) : 0u) + (qsrc ? (uint32_t)QB : 0u));
+                      if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, &full[s]);
+                      if (ok) {
+                        for (int cy = 0; cy < T / 16; ++cy) {
+                          tma_load_3d(st + cy * 16 * ROW, map, 0, y0 + 16 * cy, 0, &full[s], kv_policy);
+                          tma_load_3d(st + offV + cy * 16 * ROW, map + 128, 0, y0 + 16 * cy, 0, &full[s], kv_policy);
+                        }
+                      }
+                    });
     return;
   }
 

@@ -3,11 +3,11 @@
 //
 // Work partition and split-K epilogue are those of the bf16 kernel
 // (decode_mma.cuh): units of T tokens x all kv heads split evenly over one CTA per
-// SM, a producer warp and one consumer warp per kv head.  Staging uses TMA tensor
-// copies: each stored tensor of a slab (K codes, V codes, K meta, V meta) has a 2-D
-// tensor map [tokens][all-heads row bytes]; a stage holds T tokens of each tensor as
-// boxes of 16 tokens x W bytes (W = 128, 64, 32 or 16, the largest dividing the
-// row), written with the W-byte shared-memory swizzle (16-byte chunk c of box row r
+// SM, two producer warps and one consumer warp per kv head (two with the dim split).
+// Staging uses TMA tensor copies: each stored tensor of a slab (K codes, V codes, K
+// meta, V meta) has a tensor map over [tokens][all-heads row bytes]; a stage holds
+// T tokens of each tensor as boxes of 16 tokens x W bytes (W = 128, 64, 32 or 16,
+// the largest dividing the row), written with the W-byte shared-memory swizzle (16-byte chunk c of box row r
 // lands at chunk c ^ f(r)), so 16-byte chunks of 8 consecutive tokens sit in
 // distinct banks and are read with ldmatrix.  q comes with the first unit of a
 // sequence (one bulk copy).  The packed pages are consumed directly, never
@@ -158,7 +158,7 @@ __device__ __forceinline__ int swz(const SwzRegion& z, int tok, int b) {
 __device__ __forceinline__ int ilog2i(int v) { return 31 - __clz(v); }
 
 // Register split (RS): the block is laid out in warpgroups, ceil(Hkv / 4) of consumer
-// warps and one whose first warp is the producer.  At entry the producer warpgroup
+// warps and one whose first two warps are the producers.  At the role branch the producer warpgroup
 // gives registers back (setmaxnreg.dec to kProdRegs) and the consumer warpgroups
 // take them (setmaxnreg.inc to kConsRegs): per scheduler, two consumer warps and one
 // producer-group warp fit in the three warps' launch allocation (2 x 224 + 56 = 3 x
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   const int NC = DS ? 2 * hkv : hkv;  // consumer warps
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NCW = (NC + 3) >> 2;                // consumer warpgroups (register split)
-  const int PW = RS ? 4 * NCW : NC;             // the producer warp
+  const int PW = RS ? 4 * NCW : NC;             // the first of the two producer warps
   const int T = P.T, NS = P.NS, B = P.B;
   int32_t* err = P.lv.err;
   // Per-token rows of all kv heads in the slab; stage regions of T such rows.
@@ -218,8 +218,12 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   // one mbarrier per kv head that pairs the two warps (bounded waits)
   float4* xbuf = reinterpret_cast<float4*>(qscr + (size_t)hkv * G * D);
   uint64_t* pbar = reinterpret_cast<uint64_t*>(xbuf + (size_t)hkv * 2 * 2 * 2 * 32);
+  // the producers' issue token, one barrier per batch parity (after the dim-split
+  // buffers, or where they would start)
+  uint64_t* tok = DS ? pbar + hkv : reinterpret_cast<uint64_t*>(xbuf);
 
-  decode_prologue(P, full, empty, NC * 32, PW, UP, LS, tab);  // every consumer lane arrives on empty
+  // every consumer lane arrives on empty
+  decode_prologue(P, full, empty, NC * 32, PW, UP, LS, tab, tok);
   if (DS && threadIdx.x == 0) {
     for (int i = 0; i < hkv; ++i) mbar_init(&pbar[i], 64);
     fence_mbar_init();
@@ -233,81 +237,33 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   const int32_t u1 = min(U, u0 + C);
   if (u0 >= u1) return;
 
+  // ----------------------------- producers --------------------------------
+  // One 3-D tensor copy per 16 tokens and stored tensor, plus q when the unit starts
+  // a CTA's segment of a sequence.
+  auto issue = [&](int s, uint8_t* st, const uint8_t* map, int y0, int ok, const uint8_t* qsrc) {
+    const uint64_t kv_policy = l2_policy_evict_first();
+    mbar_arrive_expect_tx(&full[s], (ok ? (uint32_t)(T * (KR + VR + 2 * MR)) : 0u) + (qsrc ? (uint32_t)QB : 0u));
+    if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, &full[s]);
+    if (ok) {
+      for (int cy = 0; cy < T / 16; ++cy)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tma_load_3d(st + zr[k].off + ((cy * zr[k].nx) << (zr[k].lg + 4)), map + k * 128, 0, y0 + 16 * cy, 0,
+                      &full[s], kv_policy);
+    }
+  };
   // Register split at the role branch: the producer warpgroup gives registers back,
   // the consumer warpgroups take them; neither path rejoins the other.
-  if (RS && warp >= 4 * NCW) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
-    if (warp != PW) return;
-  }
-  if (RS && warp < 4 * NCW) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsRegs));
-  if (warp == PW) {
-    // ----------------------------- producer ---------------------------------
-    // Lanes hold the info of a batch of 32 units; lane i issues every copy of unit
-    // i of the batch (one 3-D tensor copy per 16 tokens and stored tensor, plus q
-    // when the unit starts a sequence), so the tensor-map acquire fences of a unit
-    // run when its batch is read, ahead of its copies, in the thread that issues them.
-    const bool use_stab = smem_table_entries(P) > 0;
-    const uint64_t kv_policy = l2_policy_evict_first();
-    int issued = 0;
-    int ps = 0;           // stage of unit `issued`
-    uint32_t pphase = 0;  // parity of that stage's current round
-    bool dead = false;
-    for (int32_t ub = u0; ub < u1 && !dead; ub += 32) {
-      const int32_t u = ub + lane;
-      const uint8_t* map = nullptr;  // tensor maps of the unit's slab (kind k at + 128 k)
-      const uint8_t* qsrc = nullptr; // q of its sequence when the unit starts a CTA's segment
-      int y0 = 0, ok = 0;            // first slab row of the unit; row valid
-      if (u < u1) {
-        const int bb = find_seq(UP, B, u);
-        if (u == u0 || u == UP[bb]) qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)bb * P.Hq * D);
-        const int32_t t0 = (u - UP[bb]) * T;
-        const int j = t0 / kBlockTokens, slot0 = t0 % kBlockTokens;
-        const int32_t row = P.bt[(size_t)bb * P.max_blocks + j];
-        if (row >= 0 && (int64_t)row < P.lv.rows_capacity) {
-          const int32_t slab = row / P.lv.slab_blocks;
-          const int32_t r = row - slab * P.lv.slab_blocks;
-          const uint8_t* ent0 =
-              use_stab ? tab[(size_t)slab * P.lv.n_kinds] : P.lv.tab.base[(size_t)slab * P.lv.tab.stride];
-          map = ent0 + P.lv.map_delta;
-          y0 = r * kBlockTokens + slot0;
-          ok = 1;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) tensormap_acquire(map + k * 128);
-        } else {
-          atomicOr(err, ERR_ROW);
-        }
-      }
-      const int cnt = min(32, u1 - ub);
-      for (int i = 0; i < cnt; ++i, ++issued, ps = (ps + 1 == NS) ? 0 : ps + 1, pphase ^= (ps == 0)) {
-        int bad = 0;
-        if (lane == i) {
-          const int s = ps;
-          if (issued >= NS && !mbar_wait_bounded(&empty[s], pphase ^ 1, err)) {
-            bad = 1;
-          } else {
-            mbar_arrive_expect_tx(&full[s], (ok ? (uint32_t)(T * (KR + VR + 2 * MR)) : 0u) + (qsrc ? (uint32_t)QB : 0u));
-            uint8_t* st = stages + (size_t)s * P.stage_bytes;
-            if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, &full[s]);
-            if (ok) {
-              for (int cy = 0; cy < T / 16; ++cy)
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  tma_load_3d(st + zr[k].off + ((cy * zr[k].nx) << (zr[k].lg + 4)), map + k * 128, 0, y0 + 16 * cy,
-                              0, &full[s], kv_policy);
-            }
-          }
-        }
-        if (__any_sync(0xffffffffu, bad)) {
-          dead = true;
-          break;
-        }
-      }
+  if constexpr (RS) {
+    if (warp >= 4 * NCW) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
+      if (warp <= PW + 1)
+        run_producer<D, kProducerWarps>(P, warp - PW, u0, u1, UP, tab, full, empty, tok, stages, issue);
+      return;
     }
-    // After a timeout, leave no copy in flight into a stage that is no longer waited on.
-    if (lane == 0) {
-      const int first = issued > NS ? issued - NS : 0;
-      for (int k = first; k < issued; ++k) mbar_wait_bounded(&full[k % NS], (k / NS) & 1, err);
-    }
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsRegs));
+  } else if (warp >= PW) {
+    run_producer<D, kProducerWarps>(P, warp - PW, u0, u1, UP, tab, full, empty, tok, stages, issue);
     return;
   }
 
@@ -806,7 +762,7 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
     attr_set = true;
   }
   const int ncons = DS ? 2 * hkv : hkv;
-  const int threads = RS ? 128 * (((ncons + 3) >> 2) + 1) : (ncons + 1) * 32;
+  const int threads = RS ? 128 * (((ncons + 3) >> 2) + 1) : (ncons + kProducerWarps) * 32;
   cudaError_t e = launch_with_pdl(kern, a.grid, threads, a.smem_bytes, a.stream, P);
   if (e != cudaSuccess) return e;
   return launch_combine<D>(P, a.grid, a.stream);

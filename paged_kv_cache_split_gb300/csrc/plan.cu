@@ -13,7 +13,8 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
   const bool packed = fmt != PKV_FMT_BF16;
   const size_t meta = packed ? (size_t)(D / kGroup) * 8 : 0;
   const size_t budget = 232448;  // 227 KB opt-in shared memory per block on sm_100-class parts
-  size_t fixed = (size_t)(2 * B + 1 + 4) * 4 + 16 + 128 + 1024 * sizeof(void*);  // + staged slab table (kSmemTableEntries)
+  // + staged slab table (kSmemTableEntries) + the producers' two token barriers
+  size_t fixed = (size_t)(2 * B + 1 + 4) * 4 + 16 + 128 + 1024 * sizeof(void*) + 32;
   if (packed) fixed += (size_t)hkv * G * D * 4;
   // packed D = 256 with at most 4 kv heads and 128-byte rows: the dim split's partial
   // logit buffers and pair barriers
@@ -68,7 +69,7 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
           plan->stage_bytes = stage;
           plan->smem_bytes = ns * stage + ns * 16 + fixed + 1024;
           plan->dim_split = dim_split;
-          plan->threads = ((dim_split ? 2 * hkv : hkv) + 1) * 32;
+          plan->threads = ((dim_split ? 2 * hkv : hkv) + 2) * 32;
           return true;
         }
       }
