@@ -68,8 +68,8 @@ __device__ __forceinline__ int find_seq(const int32_t* UP, int B, int32_t u) {
 // Before the wait the kernel relies only on what no kernel writes: it copies this
 // layer's slab base pointers into shared memory (`tab`, when they fit; the table
 // changes only through stream-ordered copies issued by append_slab), issues L2
-// prefetch hints for the context lengths and the block table, and prefetches the
-// guessed first units' K/V (prefetch_first_units).
+// prefetch hints for the context lengths and the block table, prefetches the
+// guessed first units' K/V and acquires their tensor maps (guess_first_units).
 constexpr int kSmemTableEntries = 1024;
 
 __device__ __forceinline__ int smem_table_entries(const DecodeParams& P) {
@@ -77,14 +77,19 @@ __device__ __forceinline__ int smem_table_entries(const DecodeParams& P) {
   return n <= kSmemTableEntries ? (int)n : 0;
 }
 
-// Before the dependency wait the producer warp guesses this CTA's first units from
-// the context lengths and block table as they are now (an earlier kernel may still
-// be writing them: the guess only steers L2 prefetches, every address it forms is
-// a pool row checked against the pool, and nothing read here is used after the
-// wait) and prefetches the K/V rows of the first `nunits` of them into L2, so that
-// the copies issued after the wait hit L2.  Units past the CTA's first sequence
-// are not guessed.
-__device__ __forceinline__ void prefetch_first_units(const DecodeParams& P, int nunits) {
+// Before the dependency wait the first producer warp guesses this CTA's first units
+// from the context lengths and block table as they are now (an earlier kernel may
+// still be writing them: every address the guess forms is a pool row checked
+// against the pool, and nothing read here is used after the wait except as a
+// hint).  Lane l takes unit u0 + l while it lies in the CTA's first sequence: it
+// acquires that unit's tensor maps and, for l < nprefetch, prefetches the unit's
+// K/V rows into L2, so that the copies issued after the wait hit L2.  The maps'
+// contents were final before this kernel started (they are written by
+// stream-ordered copies when a slab is appended), and lane l of this warp is the
+// thread that reads unit u0 + l's maps after the wait (the producer's first
+// batch), so it may skip its own acquire when the real unit uses the same maps.
+// Returns the lane's acquired map address (nullptr when there is no guess).
+__device__ __forceinline__ const uint8_t* guess_first_units(const DecodeParams& P, int nprefetch) {
   const int lane = threadIdx.x & 31;
   const int lim = P.max_blocks * kBlockTokens;
   auto units_of = [&](int b) -> int32_t {
@@ -101,7 +106,7 @@ __device__ __forceinline__ void prefetch_first_units(const DecodeParams& P, int 
   }
   const int32_t C = (tot + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
   const int32_t u0 = (int32_t)blockIdx.x * C;
-  if (C == 0 || u0 >= tot) return;
+  if (C == 0 || u0 >= tot) return nullptr;
   // the sequence holding unit u0, and its first unit
   int32_t carry = 0;
   int bsel = -1, nsel = 0;
@@ -123,25 +128,32 @@ __device__ __forceinline__ void prefetch_first_units(const DecodeParams& P, int 
     }
     carry += __shfl_sync(0xffffffffu, inc, 31);
   }
-  if (bsel < 0) return;
+  if (bsel < 0) return nullptr;
   const int32_t u = u0 + lane;
-  if (lane >= nunits || u >= ubase + nsel) return;
+  if (u >= ubase + nsel || u >= u0 + C) return nullptr;
   const int32_t tok0 = (u - ubase) * P.T;
   const int j = tok0 / kBlockTokens, slot0 = tok0 % kBlockTokens;
-  if (j >= P.max_blocks) return;
+  if (j >= P.max_blocks) return nullptr;
   const int32_t row = P.bt[(size_t)bsel * P.max_blocks + j];
-  if (row < 0 || (int64_t)row >= P.lv.rows_capacity) return;
+  if (row < 0 || (int64_t)row >= P.lv.rows_capacity) return nullptr;
   const int32_t slab = row / P.lv.slab_blocks, r = row - slab * P.lv.slab_blocks;
-  for (int k = 0; k < P.lv.n_kinds; ++k) {
-    const uint8_t* base = P.lv.tab.base[(size_t)slab * P.lv.tab.stride + k];
-    const int rowk = P.lv.row_bytes[k] * P.lv.hkv;
-    if (base) bulk_prefetch_l2(base + (size_t)(r * kBlockTokens + slot0) * rowk, (uint32_t)(P.T * rowk));
+  const uint8_t* ent0 = P.lv.tab.base[(size_t)slab * P.lv.tab.stride];
+  if (!ent0) return nullptr;
+  if (lane < nprefetch) {
+    for (int k = 0; k < P.lv.n_kinds; ++k) {
+      const uint8_t* base = P.lv.tab.base[(size_t)slab * P.lv.tab.stride + k];
+      const int rowk = P.lv.row_bytes[k] * P.lv.hkv;
+      if (base) bulk_prefetch_l2(base + (size_t)(r * kBlockTokens + slot0) * rowk, (uint32_t)(P.T * rowk));
+    }
   }
+  const uint8_t* map = ent0 + P.lv.map_delta;
+  for (int k = 0; k < P.lv.n_kinds; ++k) tensormap_acquire(map + k * 128);
+  return map;
 }
 
-__device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t* full, uint64_t* empty, int NC,
-                                                int PW, int32_t* UP, int32_t* LS, const uint8_t** tab,
-                                                uint64_t* tok) {
+__device__ __forceinline__ const uint8_t* decode_prologue(const DecodeParams& P, uint64_t* full, uint64_t* empty,
+                                                          int NC, int PW, int32_t* UP, int32_t* LS,
+                                                          const uint8_t** tab, uint64_t* tok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = smem_table_entries(P);
   for (int i = threadIdx.x; i < nt; i += blockDim.x) {
@@ -151,7 +163,8 @@ __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t*
   for (int i = threadIdx.x * 32; i < P.B; i += blockDim.x * 32) prefetch_l2(P.ctx + i);
   for (int64_t i = (int64_t)threadIdx.x * 32; i < (int64_t)P.B * P.max_blocks; i += (int64_t)blockDim.x * 32)
     prefetch_l2(P.bt + i);
-  if (warp == PW) prefetch_first_units(P, P.NS < 2 ? P.NS : 2);
+  const uint8_t* gmap = nullptr;
+  if (warp == PW) gmap = guess_first_units(P, P.NS < 2 ? P.NS : 2);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
@@ -189,6 +202,7 @@ __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t*
     }
     if (lane == 0) UP[P.B] = carry;
   }
+  return gmap;
 }
 
 // Producer side of the stage ring, run by NPW (1 or 2) warps that take turns over
@@ -200,13 +214,15 @@ __device__ __forceinline__ void decode_prologue(const DecodeParams& P, uint64_t*
 // batch in unit order and hands the token on: while one warp issues, the other
 // prepares its next batch, which keeps the table reads and the fence latency off
 // the issue path.  issue(s, stage, map, y0, ok, qsrc) arms full[s] with the unit's
-// bytes and issues its copies.  Every wait is bounded: a warp that gives up stops,
+// bytes and issues its copies.  `gmap` is the map address this lane acquired
+// before the dependency wait (guess_first_units; first warp only): a unit of the
+// first batch whose maps are those skips the acquire.  Every wait is bounded: a warp that gives up stops,
 // so the other gives up at its next token wait.
 template <int D, int NPW, typename IssueFn>
 __device__ __forceinline__ void run_producer(const DecodeParams& P, const int pw, const int32_t u0, const int32_t u1,
                                              const int32_t* UP, const uint8_t* const* tab, uint64_t* full,
                                              uint64_t* empty, uint64_t* tok, uint8_t* stages,
-                                             IssueFn&& issue) {
+                                             const uint8_t* gmap, IssueFn&& issue) {
   const int lane = threadIdx.x & 31;
   const int NS = P.NS, B = P.B, T = P.T;
   int32_t* err = P.lv.err;
@@ -233,7 +249,8 @@ __device__ __forceinline__ void run_producer(const DecodeParams& P, const int pw
         map = ent0 + P.lv.map_delta;
         y0 = r * kBlockTokens + slot0;
         ok = 1;
-        for (int kk = 0; kk < P.lv.n_kinds; ++kk) tensormap_acquire(map + kk * 128);
+        if (k != 0 || map != gmap)
+          for (int kk = 0; kk < P.lv.n_kinds; ++kk) tensormap_acquire(map + kk * 128);
       } else {
         atomicOr(err, ERR_ROW);
       }
@@ -312,19 +329,80 @@ struct VecF<4> {
   using T = float4;
 };
 
+// Merge of up to N parts of one (sequence, query head), parts i0 .. i0+cnt-1 of
+// the records at `base` (one every `pstride` floats), into the running (M, den,
+// num): lane k holds part k's (m, l) for the max and the denominator, every lane
+// its V = D/32 dims of each part for the numerator.  All loads are issued before
+// any is used.  `first` (no earlier chunk) skips the rescale of an empty state,
+// which would multiply zeros by zero.
+template <int D, int N>
+__device__ __forceinline__ void merge_chunk(const float* base, size_t pstride, int i0, int cnt, int lane, bool first,
+                                            float& M, float& den, float (&num)[D / 32]) {
+  constexpr int V = D / 32;
+  constexpr int NV = V / 2 > 2 ? 2 : 1;  // vector loads per lane per part
+  constexpr int VW = V / NV;             // floats per vector load: 2 or 4
+  using Vec = typename VecF<VW>::T;
+  float2 ml = make_float2(-INFINITY, 0.f);
+  if (lane < cnt) ml = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(i0 + lane) * pstride));
+  Vec v[N][NV];
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    if (k < cnt) {
+#pragma unroll
+      for (int x = 0; x < NV; ++x)
+        v[k][x] = __ldcg(reinterpret_cast<const Vec*>(base + (size_t)(i0 + k) * pstride + kPartialHeader + lane * V) + x);
+    }
+  }
+  // Lanes = parts: chunk max, weights, denominator.
+  float Mc = ml.x;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, off));
+  Mc = fmaxf(Mc, M);
+  const float wgt = exp2f(ml.x - Mc);
+  float dc = wgt * ml.y;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) dc += __shfl_xor_sync(0xffffffffu, dc, off);
+  if (first) {
+    den = dc;
+  } else {
+    const float a = exp2f(M - Mc);  // rescales earlier chunks
+    den = fmaf(den, a, dc);
+#pragma unroll
+    for (int j = 0; j < V; ++j) num[j] *= a;
+  }
+  M = Mc;
+  // Lanes = dims: add the chunk's parts in order.
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    if (k < cnt) {
+      const float wk = __shfl_sync(0xffffffffu, wgt, k);
+      const float* vf = reinterpret_cast<const float*>(&v[k][0]);
+#pragma unroll
+      for (int j = 0; j < V; ++j) num[j] = fmaf(wk, vf[j], num[j]);
+    }
+  }
+}
+
 // Split-K merge, a separate kernel chained after the attention kernel: one warp
 // per (sequence, query head) of every sequence that more than one CTA worked on.
 // Parts are merged one after another in CTA order with the online-softmax rule
 // (running max, rescaled denominator and numerator), so the result does not
-// depend on which CTA finished first.  Each lane owns D/32 consecutive dims; the
-// loads of up to CH parts (their (m, l) and the lane's dims; CH = 32 for D <= 128,
-// 16 for D = 256) are issued before any is used, so a sequence split into <= CH
-// parts costs one L2 round trip.
+// depend on which CTA finished first.  Each lane owns D/32 consecutive dims.  A
+// sequence split into at most 32 parts is merged from one round of loads, with
+// the code specialised on 8, 16 or 32 parts (at D = 256: 8 or 16 parts per round).
 //
-// The attention kernel signals its dependents only after its own wait, so the
-// context lengths (inputs of the attention call, never written by it) are final
-// when this kernel starts: the unit prefix is built before waiting for the
-// partials.
+// The kernel is latency-bound (a few hundred dependent instructions per warp
+// around one L2 round trip), so everything that does not need the partials (the
+// unit prefix, the CTA share, each warp's first (sequence, head) and its part
+// range) is computed before the dependency wait.  The attention kernel signals its
+// dependents only after its own wait, so the context lengths (inputs of the
+// attention call, never written by it) are final when this kernel starts.
+//
+// This kernel releases its own dependents before its wait: the next kernel
+// (typically the next call's attention kernel) may then be scheduled onto SMs
+// that the tail of this call's attention grid has left, and run its prologue and
+// L2 prefetches there; its own wait still covers this kernel's completion, and
+// this kernel completes only after the attention grid has.
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams P, int main_grid) {
   extern __shared__ int32_t cup[];  // unit prefix UP[0..B]
@@ -352,74 +430,61 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams P, int 
     if (lane == 0) cup[P.B] = carry;
   }
   __syncthreads();
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  constexpr int V = D / 32;  // dims per lane: 2, 4 or 8
   const int32_t U = cup[P.B];
   const int32_t C = (U + main_grid - 1) / main_grid;
-  if (C == 0) return;
-  constexpr int V = D / 32;                // dims per lane: 2, 4 or 8
-  constexpr int NV = V / 2 > 2 ? 2 : 1;    // vector loads per lane per part
-  constexpr int VW = V / NV;               // floats per vector load: 2 or 4
-  using Vec = typename VecF<VW>::T;
-  constexpr int CH = D <= 128 ? 32 : 16;  // parts in flight per lane
   const size_t pstride = (size_t)P.Hq * partial_floats(D);
   const int nwarps = gridDim.x * (blockDim.x >> 5);
-  for (int pair = blockIdx.x * (blockDim.x >> 5) + warp; pair < P.B * P.Hq; pair += nwarps) {
-    const int b = pair / P.Hq;
-    const size_t head = (size_t)(pair % P.Hq);
-    if (cup[b + 1] == cup[b]) continue;  // empty: zeros written by the attention kernel
-    const int32_t c_lo = cup[b] / C, c_hi = (cup[b + 1] - 1) / C;
-    if (c_lo == c_hi) continue;  // one CTA: output written directly
+  // this warp's first (sequence, head) and its part range, before the wait
+  int pair = blockIdx.x * (blockDim.x >> 5) + warp;
+  int b = pair / P.Hq;
+  int32_t c_lo = 0, c_hi = 0;
+  if (C > 0 && pair < P.B * P.Hq && cup[b + 1] > cup[b]) {
+    c_lo = cup[b] / C;
+    c_hi = (cup[b + 1] - 1) / C;
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (C == 0) return;
+  while (pair < P.B * P.Hq) {
+    const size_t head = (size_t)(pair - b * P.Hq);
     const int nparts = c_hi - c_lo + 1;
-    const float* base = partial_ptr(P, D, (size_t)c_lo, b, head);
-    float M = -INFINITY, den = 0.f, num[V];
+    // empty sequences (zeros written by the attention kernel) and sequences of one
+    // CTA (output written directly) have c_hi == c_lo
+    if (nparts > 1) {
+      const float* base = partial_ptr(P, D, (size_t)c_lo, b, head);
+      float M = -INFINITY, den = 0.f, num[V];
 #pragma unroll
-    for (int j = 0; j < V; ++j) num[j] = 0.f;
-    for (int i0 = 0; i0 < nparts; i0 += CH) {
-      const int cnt = min(CH, nparts - i0);
-      // Issue every load of the chunk first: lane k's (m, l) of part i0+k, and the
-      // lane's dims of each part.
-      float2 ml = make_float2(-INFINITY, 0.f);
-      if (lane < cnt) ml = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(i0 + lane) * pstride));
-      Vec v[CH][NV];
-#pragma unroll
-      for (int k = 0; k < CH; ++k) {
-        if (k < cnt) {
-#pragma unroll
-          for (int x = 0; x < NV; ++x)
-            v[k][x] = __ldcg(reinterpret_cast<const Vec*>(base + (size_t)(i0 + k) * pstride + kPartialHeader +
-                                                          lane * V) + x);
-        }
+      for (int j = 0; j < V; ++j) num[j] = 0.f;
+      {
+        // chunks of 32 parts (16 at D = 256, whose lanes hold 8 dims per part)
+        constexpr int NC = D <= 128 ? 32 : 16;
+#pragma unroll 1
+        for (int i0 = 0; i0 < nparts; i0 += NC)
+          merge_chunk<D, NC>(base, pstride, i0, min(NC, nparts - i0), lane, i0 == 0, M, den, num);
       }
-      // Lanes = parts: chunk max, weights, denominator.
-      float Mc = ml.x;
+      const float inv = 1.0f / den;
+      uint32_t w[V / 2];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, off));
-      Mc = fmaxf(Mc, M);
-      const float a = exp2f(M - Mc);  // rescales earlier chunks (0 on the first)
-      const float wgt = exp2f(ml.x - Mc);
-      float dc = wgt * ml.y;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) dc += __shfl_xor_sync(0xffffffffu, dc, off);
-      den = fmaf(den, a, dc);
-#pragma unroll
-      for (int j = 0; j < V; ++j) num[j] *= a;
-      M = Mc;
-      // Lanes = dims: add the chunk's parts in order.
-#pragma unroll
-      for (int k = 0; k < CH; ++k) {
-        if (k < cnt) {
-          const float wk = __shfl_sync(0xffffffffu, wgt, k);
-          const float* vf = reinterpret_cast<const float*>(&v[k][0]);
-#pragma unroll
-          for (int j = 0; j < V; ++j) num[j] = fmaf(wk, vf[j], num[j]);
-        }
+      for (int j = 0; j < V / 2; ++j)
+        w[j] = (uint32_t)f2bf(num[2 * j] * inv) | ((uint32_t)f2bf(num[2 * j + 1] * inv) << 16);
+      uint16_t* o = P.out + ((size_t)b * P.Hq + head) * D + lane * V;
+      if constexpr (V == 2) {
+        *reinterpret_cast<uint32_t*>(o) = w[0];
+      } else if constexpr (V == 4) {
+        *reinterpret_cast<uint2*>(o) = make_uint2(w[0], w[1]);
+      } else {
+        *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    const float inv = 1.0f / den;
-    uint16_t* o = P.out + ((size_t)b * P.Hq + head) * D + lane * V;
-#pragma unroll
-    for (int j = 0; j < V; ++j) o[j] = f2bf(num[j] * inv);
+    pair += nwarps;
+    if (pair >= P.B * P.Hq) break;
+    b = pair / P.Hq;
+    c_lo = c_hi = 0;
+    if (cup[b + 1] > cup[b]) {
+      c_lo = cup[b] / C;
+      c_hi = (cup[b + 1] - 1) / C;
+    }
   }
 }
 

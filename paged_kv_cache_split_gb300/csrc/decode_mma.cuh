@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   int32_t* LS = UP + (B + 1);
   uint64_t* tok = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(LS + B) + 7) & ~uintptr_t(7));
 
-  decode_prologue(P, full, empty, NC, NC, UP, LS, tab, tok);
+  const uint8_t* gmap = decode_prologue(P, full, empty, NC, NC, UP, LS, tab, tok);
   __syncthreads();
   const int32_t U = UP[B];
   const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
     // the context are masked by a zero probability.  A unit that starts a CTA's
     // segment of a sequence also brings that sequence's q.
     const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once
-    run_producer<D, 1>(P, 0, u0, u1, UP, tab, full, empty, tok, stages,
+    run_producer<D, 1>(P, 0, u0, u1, UP, tab, full, empty, tok, stages, gmap,
                     [&](int s, uint8_t* st, const uint8_t* map, int y0, int ok, const uint8_t* qsrc) {
                       mbar_arrive_expect_tx(&full[s], (ok ? (uint32_t)(2 * T * ROW) : 0u) + (qsrc ? (uint32_t)QB : 0u));
                       if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, &full[s]);

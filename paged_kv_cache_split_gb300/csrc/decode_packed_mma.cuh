@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   uint64_t* tok = DS ? pbar + hkv : reinterpret_cast<uint64_t*>(xbuf);
 
   // every consumer lane arrives on empty
-  decode_prologue(P, full, empty, NC * 32, PW, UP, LS, tab, tok);
+  const uint8_t* gmap = decode_prologue(P, full, empty, NC * 32, PW, UP, LS, tab, tok);
   if (DS && threadIdx.x == 0) {
     for (int i = 0; i < hkv; ++i) mbar_init(&pbar[i], 64);
     fence_mbar_init();
@@ -258,12 +258,12 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     if (warp >= 4 * NCW) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
       if (warp <= PW + 1)
-        run_producer<D, kProducerWarps>(P, warp - PW, u0, u1, UP, tab, full, empty, tok, stages, issue);
+        run_producer<D, kProducerWarps>(P, warp - PW, u0, u1, UP, tab, full, empty, tok, stages, gmap, issue);
       return;
     }
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsRegs));
   } else if (warp >= PW) {
-    run_producer<D, kProducerWarps>(P, warp - PW, u0, u1, UP, tab, full, empty, tok, stages, issue);
+    run_producer<D, kProducerWarps>(P, warp - PW, u0, u1, UP, tab, full, empty, tok, stages, gmap, issue);
     return;
   }
 
