@@ -1,6 +1,7 @@
 // decode_common.cuh — pieces shared by the decode-attention kernels: launch
-// parameters, the per-CTA unit prefix over sequences, and the split-K epilogue
-// (arrival ticket and in-order merge of partials by the last CTA of a sequence).
+// parameters, the prologue (unit prefix over sequences, guessed and speculatively
+// copied first units), the producer side of the stage ring, and the split-K merge
+// kernel (in-order merge of the partials).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -88,8 +89,18 @@ __device__ __forceinline__ int smem_table_entries(const DecodeParams& P) {
 // stream-ordered copies when a slab is appended), and lane l of this warp is the
 // thread that reads unit u0 + l's maps after the wait (the producer's first
 // batch), so it may skip its own acquire when the real unit uses the same maps.
-// Returns the lane's acquired map address (nullptr when there is no guess).
-__device__ __forceinline__ const uint8_t* guess_first_units(const DecodeParams& P, int nprefetch) {
+// Returns the lane's guess (map == nullptr when there is none).
+struct FirstGuess {
+  const uint8_t* map = nullptr;   // tensor maps of the unit's slab, acquired by this lane
+  const uint8_t* qsrc = nullptr;  // q copied with the unit (it starts the CTA's segment)
+  int32_t u = -1, row = -1;       // unit index and its pool row
+  int b = -1, y0 = 0;             // sequence; first slab row of the unit
+  bool spec = false;              // its copies were issued right after the wait
+};
+
+template <int D>
+__device__ __forceinline__ FirstGuess guess_first_units(const DecodeParams& P, int nprefetch) {
+  FirstGuess g;
   const int lane = threadIdx.x & 31;
   const int lim = P.max_blocks * kBlockTokens;
   auto units_of = [&](int b) -> int32_t {
@@ -106,7 +117,7 @@ __device__ __forceinline__ const uint8_t* guess_first_units(const DecodeParams& 
   }
   const int32_t C = (tot + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
   const int32_t u0 = (int32_t)blockIdx.x * C;
-  if (C == 0 || u0 >= tot) return nullptr;
+  if (C == 0 || u0 >= tot) return g;
   // the sequence holding unit u0, and its first unit
   int32_t carry = 0;
   int bsel = -1, nsel = 0;
@@ -128,17 +139,17 @@ __device__ __forceinline__ const uint8_t* guess_first_units(const DecodeParams& 
     }
     carry += __shfl_sync(0xffffffffu, inc, 31);
   }
-  if (bsel < 0) return nullptr;
+  if (bsel < 0) return g;
   const int32_t u = u0 + lane;
-  if (u >= ubase + nsel || u >= u0 + C) return nullptr;
+  if (u >= ubase + nsel || u >= u0 + C) return g;
   const int32_t tok0 = (u - ubase) * P.T;
   const int j = tok0 / kBlockTokens, slot0 = tok0 % kBlockTokens;
-  if (j >= P.max_blocks) return nullptr;
+  if (j >= P.max_blocks) return g;
   const int32_t row = P.bt[(size_t)bsel * P.max_blocks + j];
-  if (row < 0 || (int64_t)row >= P.lv.rows_capacity) return nullptr;
+  if (row < 0 || (int64_t)row >= P.lv.rows_capacity) return g;
   const int32_t slab = row / P.lv.slab_blocks, r = row - slab * P.lv.slab_blocks;
   const uint8_t* ent0 = P.lv.tab.base[(size_t)slab * P.lv.tab.stride];
-  if (!ent0) return nullptr;
+  if (!ent0) return g;
   if (lane < nprefetch) {
     for (int k = 0; k < P.lv.n_kinds; ++k) {
       const uint8_t* base = P.lv.tab.base[(size_t)slab * P.lv.tab.stride + k];
@@ -148,12 +159,38 @@ __device__ __forceinline__ const uint8_t* guess_first_units(const DecodeParams& 
   }
   const uint8_t* map = ent0 + P.lv.map_delta;
   for (int k = 0; k < P.lv.n_kinds; ++k) tensormap_acquire(map + k * 128);
-  return map;
+  g.map = map;
+  g.u = u;
+  g.row = row;
+  g.b = bsel;
+  g.y0 = r * kBlockTokens + slot0;
+  if (u == u0) g.qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)bsel * P.Hq * D);
+  return g;
 }
 
-__device__ __forceinline__ const uint8_t* decode_prologue(const DecodeParams& P, uint64_t* full, uint64_t* empty,
-                                                          int NC, int PW, int32_t* UP, int32_t* LS,
-                                                          const uint8_t** tab, uint64_t* tok) {
+// Speculative copies: right after the dependency wait, lane l < kSpecUnits of the
+// first producer warp issues the copies of its guessed unit into stage l, counted
+// on spec[l] instead of full[l] (reads issued after the wait see every earlier
+// write; only the choice of rows is a guess).  The producer's first batch then
+// compares the guess with the real unit: when they agree it waits for the copies
+// and completes full[l] with a plain arrival, otherwise it waits for them and
+// issues the real unit's copies into the stage.  This takes the context-length and
+// block-table reads after the wait off the path to the first data.
+// The bf16 kernel uses this (SPEC); the packed kernels measured slower with it and
+// issue their first units after the wait.
+constexpr int kSpecUnits = 2;
+
+// A lane that issued speculative copies waits for them (a CTA left without work,
+// or a producer that stopped) before its CTA may exit.
+__device__ __forceinline__ void finish_spec(const FirstGuess& g, uint64_t* spec, int32_t* err) {
+  if (g.spec) mbar_wait_bounded(&spec[threadIdx.x & 31], 0, err);
+}
+
+template <int D, bool SPEC, typename IssueFn>
+__device__ __forceinline__ FirstGuess decode_prologue(const DecodeParams& P, uint64_t* full, uint64_t* empty, int NC,
+                                                      int PW, int32_t* UP, int32_t* LS, const uint8_t** tab,
+                                                      uint64_t* tok, uint64_t* spec, uint8_t* stages,
+                                                      IssueFn&& issue) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = smem_table_entries(P);
   for (int i = threadIdx.x; i < nt; i += blockDim.x) {
@@ -163,10 +200,21 @@ __device__ __forceinline__ const uint8_t* decode_prologue(const DecodeParams& P,
   for (int i = threadIdx.x * 32; i < P.B; i += blockDim.x * 32) prefetch_l2(P.ctx + i);
   for (int64_t i = (int64_t)threadIdx.x * 32; i < (int64_t)P.B * P.max_blocks; i += (int64_t)blockDim.x * 32)
     prefetch_l2(P.bt + i);
-  const uint8_t* gmap = nullptr;
-  if (warp == PW) gmap = guess_first_units(P, P.NS < 2 ? P.NS : 2);
+  FirstGuess g;
+  if (warp == PW) {
+    if (lane == 0) {
+      for (int i = 0; i < kSpecUnits; ++i) mbar_init(&spec[i], 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    g = guess_first_units<D>(P, P.NS < 2 ? P.NS : 2);
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (SPEC && warp == PW && g.map && lane < kSpecUnits && lane < P.NS) {
+    issue(&spec[lane], stages + (size_t)lane * P.stage_bytes, g.map, g.y0, 1, g.qsrc);
+    g.spec = true;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.NS; ++s) {
       mbar_init(&full[s], 1);
@@ -202,7 +250,7 @@ __device__ __forceinline__ const uint8_t* decode_prologue(const DecodeParams& P,
     }
     if (lane == 0) UP[P.B] = carry;
   }
-  return gmap;
+  return g;
 }
 
 // Producer side of the stage ring, run by NPW (1 or 2) warps that take turns over
@@ -213,16 +261,17 @@ __device__ __forceinline__ const uint8_t* decode_prologue(const DecodeParams& P,
 // ring in order and never more than one round ahead of the consumers), issues the
 // batch in unit order and hands the token on: while one warp issues, the other
 // prepares its next batch, which keeps the table reads and the fence latency off
-// the issue path.  issue(s, stage, map, y0, ok, qsrc) arms full[s] with the unit's
-// bytes and issues its copies.  `gmap` is the map address this lane acquired
-// before the dependency wait (guess_first_units; first warp only): a unit of the
-// first batch whose maps are those skips the acquire.  Every wait is bounded: a warp that gives up stops,
+// the issue path.  issue(bar, stage, map, y0, ok, qsrc) arms barrier `bar` with the
+// unit's bytes and issues its copies.  `g` is this lane's guess of its first-batch
+// unit (guess_first_units; first warp only): a unit whose maps are the guessed
+// ones skips the acquire, and the stages of speculatively copied units are settled
+// as described at kSpecUnits.  Every wait is bounded: a warp that gives up stops,
 // so the other gives up at its next token wait.
 template <int D, int NPW, typename IssueFn>
 __device__ __forceinline__ void run_producer(const DecodeParams& P, const int pw, const int32_t u0, const int32_t u1,
                                              const int32_t* UP, const uint8_t* const* tab, uint64_t* full,
                                              uint64_t* empty, uint64_t* tok, uint8_t* stages,
-                                             const uint8_t* gmap, IssueFn&& issue) {
+                                             const FirstGuess& g, uint64_t* spec, IssueFn&& issue) {
   const int lane = threadIdx.x & 31;
   const int NS = P.NS, B = P.B, T = P.T;
   int32_t* err = P.lv.err;
@@ -235,6 +284,7 @@ __device__ __forceinline__ void run_producer(const DecodeParams& P, const int pw
     const uint8_t* map = nullptr;   // tensor maps of the unit's slab (kind k at + 128 k)
     const uint8_t* qsrc = nullptr;  // q of its sequence when the unit starts a CTA's segment
     int y0 = 0, ok = 0;             // first slab row of the unit; row valid
+    bool reuse = false;             // the speculative copies of this stage hold exactly this unit
     if (u < u1) {
       const int bb = find_seq(UP, B, u);
       if (u == u0 || u == UP[bb]) qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)bb * P.Hq * D);
@@ -249,8 +299,9 @@ __device__ __forceinline__ void run_producer(const DecodeParams& P, const int pw
         map = ent0 + P.lv.map_delta;
         y0 = r * kBlockTokens + slot0;
         ok = 1;
-        if (k != 0 || map != gmap)
+        if (k != 0 || map != g.map)
           for (int kk = 0; kk < P.lv.n_kinds; ++kk) tensormap_acquire(map + kk * 128);
+        reuse = k == 0 && g.spec && g.u == u && g.b == bb && g.row == row && g.map == map && g.qsrc == qsrc;
       } else {
         atomicOr(err, ERR_ROW);
       }
@@ -260,17 +311,39 @@ __device__ __forceinline__ void run_producer(const DecodeParams& P, const int pw
       if (__any_sync(0xffffffffu, !got)) return;  // the other warp stopped; nothing of this warp is in flight
     }
     const int cnt = min(32, u1 - ub);
-    int n = 32 * k;           // ring position of unit ub
-    int s = n % NS;           // its stage
-    uint32_t ph = (n / NS) & 1;  // parity of that stage's round
+    int i0 = 0;  // first unit of the batch left to the in-order loop below
     bool dead = false;
-    for (int i = 0; i < cnt; ++i, ++n) {
+    if (k == 0) {
+      // First round of the ring (no stage in use yet): units without speculative
+      // copies are issued first, then each speculative stage is settled by its lane
+      // once its copies have landed.
+      const unsigned smask = __ballot_sync(0xffffffffu, g.spec);
+      i0 = min(cnt, NS);
+      for (int i = 0; i < i0; ++i)
+        if (lane == i && !((smask >> i) & 1u)) issue(&full[i], stages + (size_t)i * P.stage_bytes, map, y0, ok, qsrc);
+      int bad = 0;
+      if (g.spec) {
+        if (!mbar_wait_bounded(&spec[lane], 0, err))
+          bad = 1;
+        else if (lane < cnt) {
+          if (reuse)
+            mbar_arrive(&full[lane]);
+          else
+            issue(&full[lane], stages + (size_t)lane * P.stage_bytes, map, y0, ok, qsrc);
+        }
+      }
+      dead = __any_sync(0xffffffffu, bad);
+    }
+    int n = 32 * k + i0;         // ring position of unit ub + i0
+    int s = n % NS;              // its stage
+    uint32_t ph = (n / NS) & 1;  // parity of that stage's round
+    for (int i = i0; i < cnt && !dead; ++i, ++n) {
       int bad = 0;
       if (lane == i) {
         if (n >= NS && !mbar_wait_bounded(&empty[s], ph ^ 1, err))
           bad = 1;
         else
-          issue(s, stages + (size_t)s * P.stage_bytes, map, y0, ok, qsrc);
+          issue(&full[s], stages + (size_t)s * P.stage_bytes, map, y0, ok, qsrc);
       }
       if (__any_sync(0xffffffffu, bad)) {
         dead = true;

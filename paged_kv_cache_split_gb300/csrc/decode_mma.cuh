@@ -77,36 +77,41 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   int32_t* LS = UP + (B + 1);
   uint64_t* tok = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(LS + B) + 7) & ~uintptr_t(7));
 
-  const uint8_t* gmap = decode_prologue(P, full, empty, NC, NC, UP, LS, tab, tok);
+  uint64_t* spec = tok + 2;  // [kSpecUnits]
+  const int offV = T * ROW;      // K region [T/16][NX][16][128], then V region
+  const int offQ = 2 * T * ROW;  // q of the sequence, when the unit starts one
+  const int QB = P.Hq * D * 2;
+  // Arms `bar` with a unit's bytes and issues its copies.  A whole unit is always
+  // copied (T tokens stay inside the block); tokens past the context are masked by
+  // a zero probability.  A unit that starts a CTA's segment of a sequence also
+  // brings that sequence's q.
+  auto issue = [&](uint64_t* bar, uint8_t* st, const uint8_t* map, int y0, int ok, const uint8_t* qsrc) {
+    const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once
+    mbar_arrive_expect_tx(bar, (ok ? (uint32_t)(2 * T * ROW) : 0u) + (qsrc ? (uint32_t)QB : 0u));
+    if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, bar);
+    if (ok) {
+      for (int cy = 0; cy < T / 16; ++cy) {
+        tma_load_3d(st + cy * 16 * ROW, map, 0, y0 + 16 * cy, 0, bar, kv_policy);
+        tma_load_3d(st + offV + cy * 16 * ROW, map + 128, 0, y0 + 16 * cy, 0, bar, kv_policy);
+      }
+    }
+  };
+
+  const FirstGuess fg = decode_prologue<D, true>(P, full, empty, NC, NC, UP, LS, tab, tok, spec, stages, issue);
   __syncthreads();
   const int32_t U = UP[B];
   const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
   zero_empty_sequences<D>(P, LS);
-  if (C == 0) return;
   const int32_t u0 = (int32_t)blockIdx.x * C;
   const int32_t u1 = min(U, u0 + C);
-  if (u0 >= u1) return;
-  const int offV = T * ROW;      // K region [T/16][NX][16][128], then V region
-  const int offQ = 2 * T * ROW;  // q of the sequence, when the unit starts one
-  const int QB = P.Hq * D * 2;
+  if (C == 0 || u0 >= u1) {
+    if (warp == NC) finish_spec(fg, spec, err);
+    return;
+  }
 
   if (warp == NC) {
-    // ----------------------------- producers --------------------------------
-    // A whole unit is always copied (T tokens stay inside the block); tokens past
-    // the context are masked by a zero probability.  A unit that starts a CTA's
-    // segment of a sequence also brings that sequence's q.
-    const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once
-    run_producer<D, 1>(P, 0, u0, u1, UP, tab, full, empty, tok, stages, gmap,
-                    [&](int s, uint8_t* st, const uint8_t* map, int y0, int ok, const uint8_t* qsrc) {
-                      mbar_arrive_expect_tx(&full[s], (ok ? (uint32_t)(2 * T * ROW) : 0u) + (qsrc ? (uint32_t)QB : 0u));
-                      if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, &full[s]);
-                      if (ok) {
-                        for (int cy = 0; cy < T / 16; ++cy) {
-                          tma_load_3d(st + cy * 16 * ROW, map, 0, y0 + 16 * cy, 0, &full[s], kv_policy);
-                          tma_load_3d(st + offV + cy * 16 * ROW, map + 128, 0, y0 + 16 * cy, 0, &full[s], kv_policy);
-                        }
-                      }
-                    });
+    // ----------------------------- producer ---------------------------------
+    run_producer<D, 1>(P, 0, u0, u1, UP, tab, full, empty, tok, stages, fg, spec, issue);
     return;
   }
 

@@ -222,8 +222,25 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   // buffers, or where they would start)
   uint64_t* tok = DS ? pbar + hkv : reinterpret_cast<uint64_t*>(xbuf);
 
+  uint64_t* spec = tok + 2;  // [kSpecUnits]
+
+  // Producers: one 3-D tensor copy per 16 tokens and stored tensor, plus q when the
+  // unit starts a CTA's segment of a sequence, all counted on barrier `bar`.
+  auto issue = [&](uint64_t* bar, uint8_t* st, const uint8_t* map, int y0, int ok, const uint8_t* qsrc) {
+    const uint64_t kv_policy = l2_policy_evict_first();
+    mbar_arrive_expect_tx(bar, (ok ? (uint32_t)(T * (KR + VR + 2 * MR)) : 0u) + (qsrc ? (uint32_t)QB : 0u));
+    if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, bar);
+    if (ok) {
+      for (int cy = 0; cy < T / 16; ++cy)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tma_load_3d(st + zr[k].off + ((cy * zr[k].nx) << (zr[k].lg + 4)), map + k * 128, 0, y0 + 16 * cy, 0,
+                      bar, kv_policy);
+    }
+  };
+
   // every consumer lane arrives on empty
-  const uint8_t* gmap = decode_prologue(P, full, empty, NC * 32, PW, UP, LS, tab, tok);
+  const FirstGuess fg = decode_prologue<D, false>(P, full, empty, NC * 32, PW, UP, LS, tab, tok, spec, stages, issue);
   if (DS && threadIdx.x == 0) {
     for (int i = 0; i < hkv; ++i) mbar_init(&pbar[i], 64);
     fence_mbar_init();
@@ -232,38 +249,25 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   const int32_t U = UP[B];
   const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
   zero_empty_sequences<D>(P, LS);
-  if (C == 0) return;
   const int32_t u0 = (int32_t)blockIdx.x * C;
   const int32_t u1 = min(U, u0 + C);
-  if (u0 >= u1) return;
+  if (C == 0 || u0 >= u1) {
+    if (warp == PW) finish_spec(fg, spec, err);
+    return;
+  }
 
-  // ----------------------------- producers --------------------------------
-  // One 3-D tensor copy per 16 tokens and stored tensor, plus q when the unit starts
-  // a CTA's segment of a sequence.
-  auto issue = [&](int s, uint8_t* st, const uint8_t* map, int y0, int ok, const uint8_t* qsrc) {
-    const uint64_t kv_policy = l2_policy_evict_first();
-    mbar_arrive_expect_tx(&full[s], (ok ? (uint32_t)(T * (KR + VR + 2 * MR)) : 0u) + (qsrc ? (uint32_t)QB : 0u));
-    if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, &full[s]);
-    if (ok) {
-      for (int cy = 0; cy < T / 16; ++cy)
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tma_load_3d(st + zr[k].off + ((cy * zr[k].nx) << (zr[k].lg + 4)), map + k * 128, 0, y0 + 16 * cy, 0,
-                      &full[s], kv_policy);
-    }
-  };
   // Register split at the role branch: the producer warpgroup gives registers back,
   // the consumer warpgroups take them; neither path rejoins the other.
   if constexpr (RS) {
     if (warp >= 4 * NCW) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
       if (warp <= PW + 1)
-        run_producer<D, kProducerWarps>(P, warp - PW, u0, u1, UP, tab, full, empty, tok, stages, gmap, issue);
+        run_producer<D, kProducerWarps>(P, warp - PW, u0, u1, UP, tab, full, empty, tok, stages, fg, spec, issue);
       return;
     }
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsRegs));
   } else if (warp >= PW) {
-    run_producer<D, kProducerWarps>(P, warp - PW, u0, u1, UP, tab, full, empty, tok, stages, gmap, issue);
+    run_producer<D, kProducerWarps>(P, warp - PW, u0, u1, UP, tab, full, empty, tok, stages, fg, spec, issue);
     return;
   }
 
