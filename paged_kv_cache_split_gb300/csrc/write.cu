@@ -162,7 +162,9 @@ template <int D>
 cudaError_t launch_write_d(const LayerView& lv, int fmt, int n, const int32_t* rows, const int32_t* slots,
                            const uint16_t* k, const uint16_t* v, const float* signs, double inv, cudaStream_t s) {
   const int64_t warps = (int64_t)n * lv.hkv;
-  const int threads = 256;
+  // A step's write (a few tokens) runs one warp per CTA, so its warps spread over
+  // the SMs: the packed kernel's FP64 butterflies are throughput-bound per SM.
+  const int threads = warps < 4096 ? 32 : 256;
   const unsigned grid = (unsigned)((warps * 32 + threads - 1) / threads);
   switch (fmt) {
     case PKV_FMT_BF16: write_bf16_kernel<D><<<grid, threads, 0, s>>>(lv, n, rows, slots, k, v); break;
