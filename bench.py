@@ -683,6 +683,123 @@ def mixed_oracle_sample(budget_s: float = 10.0):
             "seconds_per_sample": t, "kv_tokens_per_s": sum(r[5] for r in runs) / t}
 
 
+BLOCKS = "blocks-export"
+
+
+def blocks_oracle_sample(budget_s: float = 10.0, n_blocks: int = 64):
+    """The oracle's export of n_blocks blocks of a 28-layer Qwen3-0.6B-shaped bf16 image."""
+    import oracle
+    oracle.build()
+    w = wl.qwen3_0_6b()
+    o = oracle.OraclePool(w.n_layers, w.Hkv, w.D, w.fmt, seed=w.hadamard_seed)
+    o.reserve_rows(n_blocks)
+    rng = wl.rng_for(77)
+    rows = np.repeat(np.arange(n_blocks, dtype=np.int32), 32)
+    slots = np.tile(np.arange(32, dtype=np.int32), n_blocks)
+    for layer in range(w.n_layers):
+        o.write_block(layer, rows, slots, wl.bf16_normal(rng, (rows.size, w.Hkv, w.D)),
+                      wl.bf16_normal(rng, (rows.size, w.Hkv, w.D)))
+    blk = np.arange(n_blocks, dtype=np.int32)
+    times, t_end = [], time.perf_counter() + budget_s
+    while time.perf_counter() < t_end or len(times) < 3:
+        t0 = time.perf_counter()
+        o.export_blocks(blk)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    nbytes = 2 * n_blocks * o.record_bytes
+    return {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"export of {n_blocks} of 1024 blocks (28 layers, bf16), read + write bytes; median of {len(times)} runs",
+            "seconds_per_sample": t}
+
+
+def run_gpu_blocks(args, rank, world, local):
+    """Block records: export every block of the Qwen3-0.6B-shaped pool (28 layers, 8 x 4096
+    tokens) to a device buffer; a step moves each record's bytes once in and once out."""
+    import torch
+    import paged_kv_cache_split_gb300 as pkv
+
+    torch.cuda.set_device(local)
+    w = wl.qwen3_0_6b(n_layers=args.layers) if args.layers else wl.qwen3_0_6b()
+    dev = torch.device("cuda", local)
+    pool = pkv.Pool(w.n_layers, w.Hkv, w.D, pkv.FORMAT_NAMES[w.fmt], hadamard_seed=w.hadamard_seed,
+                    max_slabs=(w.rows_used + 31) // 32 + 8)
+    pool.reserve_rows(w.rows_used)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2000 + rank)
+    rows = np.concatenate([w.token_placement(b)[0] for b in range(w.B)])
+    slots = np.concatenate([w.token_placement(b)[1] for b in range(w.B)])
+    rows_d, slots_d = torch.from_numpy(rows).to(dev), torch.from_numpy(slots).to(dev)
+    for layer in range(w.n_layers):
+        k = torch.randn((rows.size, w.Hkv, w.D), generator=gen, device=dev).to(torch.bfloat16)
+        v = torch.randn((rows.size, w.Hkv, w.D), generator=gen, device=dev).to(torch.bfloat16)
+        pool.write_block(layer, rows_d, slots_d, k, v)
+        del k, v
+    bt = w.block_table()
+    blocks = np.concatenate([bt[b][: wl.nblocks(w.lens[b])] for b in range(w.B)]).astype(np.int32)
+    blocks_d = torch.from_numpy(blocks).to(dev)
+    rec = pool.export_blocks(blocks_d)
+    stream = torch.cuda.current_stream()
+    rec_h = torch.empty(rec.shape, dtype=torch.uint8, pin_memory=True)
+    blocks_h = torch.from_numpy(blocks).pin_memory()
+    blocks_e = torch.empty_like(blocks_d)
+
+    def step():
+        pool.export_blocks(blocks_d, out=rec)
+
+    def e2e_step():
+        blocks_e.copy_(blocks_h, non_blocking=True)
+        pool.export_blocks(blocks_e, out=rec)
+        rec_h.copy_(rec, non_blocking=True)
+
+    sampler = ClockSampler(local)
+    with sampler:
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        ms_step = t0.elapsed_time(t1) / args.steps
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        ms_e2e = e0.elapsed_time(e1) / args.steps
+    if pool.check_errors():
+        raise SystemExit("device error word set during the timed region")
+    ms_step, ms_e2e = dist_max(ms_step, world), dist_max(ms_e2e, world)
+    moved = 2 * rec.numel()  # each record byte read from the slabs and written to the buffer
+    value = moved * world / (ms_step * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    res = {"metric": "block export: achieved HBM GB/s (read + write bytes)", "value": round(value, 1), "unit": "GB/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+           "data": "synthetic (seeded N(0,1) bf16 K/V; no model weights)",
+           "config": {"workload": f"block export: {blocks.size} blocks x {pool.block_record_bytes()} B records "
+                                  f"(Qwen3-0.6B-shaped pool, {w.n_layers} layers, bf16)",
+                      "global_batch": w.B * world, "seq_len": max(w.lens), "layers": w.n_layers,
+                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                      "l2": f"inputs larger than L2 ({rec.numel() / 1e9:.2f} GB per step vs 129 MB L2)"},
+           "roofline": {"bound": "hbm", "achieved": round(value / world, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(value / world / peak, 4), "traffic": None, "per_launch_bytes": int(moved),
+                        "avg_launch_us": round(ms_step * 1e3, 3), "peak_source": peak_src, "kernel": "serde_blocks_kernel"},
+           "e2e": {"value": round(moved * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms_e2e, 5),
+                   "h2d_bytes_per_step": int(blocks.nbytes), "d2h_bytes_per_step": int(rec.numel())},
+           "gpu_launches": args.steps, "clocks": sampler.summary()}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -717,6 +834,33 @@ def main():
                "e2e": {"value": round(cb["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                        "d2h_bytes_per_step": 0}}
         print(json.dumps(res), flush=True)
+        return
+
+    if args.workload == BLOCKS:
+        if rank != 0 and args.impl == "reference":
+            return
+        if args.impl == "reference":
+            cb = blocks_oracle_sample(budget_s=max(2.0, 0.05 * (args.warmup + args.steps)))
+            res = {"impl": "reference", "metric": "block export: achieved HBM GB/s (read + write bytes)",
+                   "value": round(cb["value"], 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+                   "warmup": args.warmup, "ms_per_step": round(cb["seconds_per_sample"] * 1e3, 3),
+                   "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+                   "data": "synthetic (seeded N(0,1) bf16 K/V; no model weights)",
+                   "config": {"workload": "block export (oracle sample)", "parallelism": "host cores"},
+                   "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                   "e2e": {"value": round(cb["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}}
+            print(json.dumps(res), flush=True)
+            return
+        res = run_gpu_blocks(args, rank, world, local)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                cb = blocks_oracle_sample(budget_s=10.0)
+                res["cpu_baseline"] = {k: (round(v, 5) if isinstance(v, float) else v) for k, v in cb.items()}
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
 
     if args.impl == "reference":

@@ -234,6 +234,43 @@ pkv_status pkv_slab_address(const pkv_pool* pool, int layer, int kind, int slab,
  *   [mlx-swift-lm #142, Summary: reject incompatible storage identities] */
 pkv_status pkv_pool_check_identity(const pkv_pool* pool, const pkv_pool_config* cfg);
 
+/* The pool's configuration (its storage identity plus n_layers and max_slabs), for
+ * a checkpoint header.  Synchronous, host only. */
+pkv_status pkv_pool_get_config(const pkv_pool* pool, pkv_pool_config* out);
+
+/* Bytes of one block record: every stored byte of one block (row) of every layer,
+ * layer-major, then tensor kind (K, V, K meta, V meta), each the block's
+ * [block_size, n_kv_heads, row_bytes(kind)] bytes exactly as stored.  Equals
+ * n_layers * block_size * n_kv_heads * sum over kinds of row_bytes(kind).
+ * Synchronous, host only. */
+pkv_status pkv_block_record_bytes(const pkv_pool* pool, size_t* bytes);
+
+/* export_blocks: write the records of blocks rows_dev[0..n) to out_dev, one after
+ * another in list order (n records; packed codes and FP32 metadata are copied
+ * bit for bit, nothing is dequantised).  rows_dev: n int32 on the device; out_dev:
+ * caller-owned device buffer, 16-byte aligned, at least n records long
+ * (out_bytes).  Errors: PKV_ERR_INVALID for null or misaligned pointers,
+ * PKV_ERR_RANGE when out_bytes is too small; a row outside the pool sets the
+ * device error word (bit 1) and its record is left unwritten.  Asynchronous.
+ *   [mlxcel #235, touch point 6: serde block-content extraction localised to the
+ *    row's slab by the mapping helper; mlx-swift-lm #142, Summary: complete
+ *    checkpoints preserve packed bytes] */
+pkv_status pkv_export_blocks(pkv_pool* pool, int n, const int32_t* rows_dev, void* out_dev, size_t out_bytes,
+                             void* stream);
+
+/* import_blocks: the restore path.  Copy n records from in_dev (layout of
+ * pkv_export_blocks) into blocks rows_dev[0..n) of this pool (live, distinct rows;
+ * the caller allocates them).  `identity` is the configuration of the pool the
+ * records came from: when its storage identity (pkv_pool_check_identity) or its
+ * n_layers differs from this pool's, PKV_ERR_FORMAT is returned before any device
+ * work, so an incompatible checkpoint is rejected before anything is written.
+ * Other errors as for export.  Asynchronous.
+ *   [mlxcel #235, touch point 6: restore path; mlx-swift-lm #142, Summary: reject
+ *    incompatible storage identities before allocation; After: exact packed
+ *    checkpoint with format identity] */
+pkv_status pkv_import_blocks(pkv_pool* pool, const pkv_pool_config* identity, int n, const int32_t* rows_dev,
+                             const void* in_dev, size_t in_bytes, void* stream);
+
 /* Synchronise `stream`, read and clear the device error word.  PKV_ERR_DEVICE if it
  * was set (bits: 1 row out of range, 2 context too long, 4 slot out of range,
  * 8 wait limit reached); *word_out (optional) receives the bits. */

@@ -81,6 +81,12 @@ def _load():
         lib.oracle_read_block.restype = i32
         lib.oracle_read_slab.argtypes = [P, i32, i32, i32, P]
         lib.oracle_read_slab.restype = i32
+        lib.oracle_record_bytes.argtypes = [P]
+        lib.oracle_record_bytes.restype = ctypes.c_size_t
+        lib.oracle_export_blocks.argtypes = [P, i32, P, P]
+        lib.oracle_export_blocks.restype = i32
+        lib.oracle_import_blocks.argtypes = [P, i32, P, P]
+        lib.oracle_import_blocks.restype = i32
         _lib = lib
         return lib
 
@@ -227,6 +233,23 @@ class OraclePool:
         out = np.zeros(self.block_size * self.n_kv_heads * self.row_bytes[kind], np.uint8)
         _check(self._lib.oracle_read_block(self._h, layer, kind, row, _ptr(out)), "read_block")
         return out
+
+    @property
+    def record_bytes(self) -> int:
+        return int(self._lib.oracle_record_bytes(self._h))
+
+    def export_blocks(self, rows) -> np.ndarray:
+        """[n, record_bytes] uint8 records of blocks `rows` (layer-major, then K, V, K meta, V meta)."""
+        rows = np.ascontiguousarray(rows, np.int32)
+        out = np.zeros((rows.size, self.record_bytes), np.uint8)
+        _check(self._lib.oracle_export_blocks(self._h, rows.size, _ptr(rows), _ptr(out)), "export_blocks")
+        return out
+
+    def import_blocks(self, rows, records: np.ndarray):
+        rows = np.ascontiguousarray(rows, np.int32)
+        rec = np.ascontiguousarray(records, np.uint8)
+        assert rec.size == rows.size * self.record_bytes
+        _check(self._lib.oracle_import_blocks(self._h, rows.size, _ptr(rows), _ptr(rec)), "import_blocks")
 
     def read_slab(self, layer: int, kind: int, slab: int) -> np.ndarray:
         n = self.slab_blocks * self.block_size * self.n_kv_heads * self.row_bytes[kind]

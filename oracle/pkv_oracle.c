@@ -535,6 +535,47 @@ int oracle_decode_attention(const oracle_pool* p, int layer, int B, int Hq, cons
   return OR_OK;
 }
 
+/* Block record [SLAB, touch point 6 (serde block content, restore path); PACK,
+ * Summary (complete checkpoints preserve packed bytes)]: every stored byte of one
+ * block, for each layer in order and, within a layer, for each stored tensor in
+ * the order K, V, K meta, V meta, the block's [block_size][n_kv_heads][row]
+ * bytes as stored.  Nothing is converted. */
+size_t oracle_record_bytes(const oracle_pool* p) {
+  size_t per_layer = 0;
+  for (int kind = 0; kind < p->n_kinds; ++kind) per_layer += (size_t)p->block_size * p->n_kv_heads * p->row_bytes[kind];
+  return per_layer * (size_t)p->n_layers;
+}
+
+/* export: the records of rows[0..n) one after another in list order. */
+int oracle_export_blocks(const oracle_pool* p, int n, const int32_t* rows, uint8_t* out) {
+  for (int i = 0; i < n; ++i)
+    if (!row_ok(p, rows[i])) return OR_ERR_RANGE;
+  uint8_t* o = out;
+  for (int i = 0; i < n; ++i)
+    for (int l = 0; l < p->n_layers; ++l)
+      for (int kind = 0; kind < p->n_kinds; ++kind) {
+        size_t blk = (size_t)p->block_size * p->n_kv_heads * p->row_bytes[kind];
+        memcpy(o, addr(p, l, kind, rows[i], 0, 0), blk);
+        o += blk;
+      }
+  return OR_OK;
+}
+
+/* import (restore): record i is written back into block rows[i]. */
+int oracle_import_blocks(oracle_pool* p, int n, const int32_t* rows, const uint8_t* in) {
+  for (int i = 0; i < n; ++i)
+    if (!row_ok(p, rows[i])) return OR_ERR_RANGE;
+  const uint8_t* r = in;
+  for (int i = 0; i < n; ++i)
+    for (int l = 0; l < p->n_layers; ++l)
+      for (int kind = 0; kind < p->n_kinds; ++kind) {
+        size_t blk = (size_t)p->block_size * p->n_kv_heads * p->row_bytes[kind];
+        memcpy(addr(p, l, kind, rows[i], 0, 0), r, blk);
+        r += blk;
+      }
+  return OR_OK;
+}
+
 /* Raw bytes of one (layer, kind, row) block, for tests. */
 int oracle_read_block(const oracle_pool* p, int layer, int kind, int32_t row, uint8_t* out) {
   if (layer < 0 || layer >= p->n_layers || kind < 0 || kind >= p->n_kinds || !row_ok(p, row))

@@ -86,6 +86,10 @@ SIGNATURES = {
     "pkv_slab_address": ([_P, _I, _I, _I, ctypes.POINTER(_P)], _I),
     "pkv_pool_check_identity": ([_P, ctypes.POINTER(PoolConfig)], _I),
     "pkv_pool_check_errors": ([_P, _P, ctypes.POINTER(ctypes.c_int32)], _I),
+    "pkv_pool_get_config": ([_P, ctypes.POINTER(PoolConfig)], _I),
+    "pkv_block_record_bytes": ([_P, ctypes.POINTER(_SZ)], _I),
+    "pkv_export_blocks": ([_P, _I, _P, _P, _SZ, _P], _I),
+    "pkv_import_blocks": ([_P, ctypes.POINTER(PoolConfig), _I, _P, _P, _SZ, _P], _I),
     "pkv_status_string": ([_I], ctypes.c_char_p),
     "pkv_last_error": ([], ctypes.c_char_p),
 }
@@ -247,6 +251,37 @@ class Pool:
         _check(self._lib.pkv_gather_visible(self._h, layer, _dev(bt_row, torch.int32, "bt_row"), ctx_len,
                                             *ptrs, _stream(stream)), "gather_visible")
         return outs
+
+    # -- block records (export / import) ---------------------------------------
+    def config(self) -> PoolConfig:
+        """The pool's configuration (storage identity, layer count, table size)."""
+        c = PoolConfig()
+        _check(self._lib.pkv_pool_get_config(self._h, ctypes.byref(c)), "pool_get_config")
+        return c
+
+    def block_record_bytes(self) -> int:
+        n = _SZ()
+        _check(self._lib.pkv_block_record_bytes(self._h, ctypes.byref(n)), "block_record_bytes")
+        return int(n.value)
+
+    def export_blocks(self, rows, out=None, stream=None):
+        """[n, record_bytes] uint8 device tensor with the records of blocks `rows`."""
+        torch = _torch()
+        n, rec = int(rows.numel()), self.block_record_bytes()
+        if out is None:
+            out = torch.empty((n, rec), dtype=torch.uint8, device=rows.device)
+        _check(self._lib.pkv_export_blocks(self._h, n, _dev(rows, torch.int32, "rows"),
+                                           _dev(out, torch.uint8, "out"), out.numel(), _stream(stream)),
+               "export_blocks")
+        return out
+
+    def import_blocks(self, identity: PoolConfig, rows, records, stream=None):
+        """Write records (layout of export_blocks) into blocks `rows`; raises PkvError
+        (status PKV_ERR_FORMAT) before any device work if `identity` differs."""
+        torch = _torch()
+        _check(self._lib.pkv_import_blocks(self._h, ctypes.byref(identity), int(rows.numel()),
+                                           _dev(rows, torch.int32, "rows"), _dev(records, torch.uint8, "records"),
+                                           records.numel(), _stream(stream)), "import_blocks")
 
     # -- attention -----------------------------------------------------------
     def decode_workspace_bytes(self, B: int, Hq: int, max_ctx: int = 0) -> int:

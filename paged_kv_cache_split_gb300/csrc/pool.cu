@@ -56,6 +56,10 @@ struct pkv_pool {
 static thread_local std::string g_last_error;
 
 namespace pkv {
+// Defined in write.cu.
+cudaError_t launch_serde_blocks(const uint8_t* const* table, int n_layers, int n_kinds, const int64_t* block_bytes,
+                               int slab_blocks, int64_t rows_capacity, int n, const int32_t* rows, uint8_t* buf,
+                               int64_t rec_bytes, int to_pool, int32_t* err, cudaStream_t s);
 void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
 }  // namespace pkv
 
@@ -423,6 +427,60 @@ pkv_status pkv_copy_on_write_block(pkv_pool* p, int n, const int32_t* src, const
            "copy_on_write_block launch");
   p->last_stream = s;
   return PKV_OK;
+}
+
+// Bytes of one block record: every layer, every stored tensor.
+static size_t record_bytes(const pkv_pool* p, int64_t* block_bytes) {
+  size_t per_layer = 0;
+  for (int k = 0; k < 4; ++k) block_bytes[k] = 0;
+  for (int k = 0; k < p->n_kinds; ++k) {
+    block_bytes[k] = p->row_bytes[k] * kBlockTokens * p->cfg.n_kv_heads;
+    per_layer += (size_t)block_bytes[k];
+  }
+  return per_layer * (size_t)p->cfg.n_layers;
+}
+
+pkv_status pkv_pool_get_config(const pkv_pool* p, pkv_pool_config* out) {
+  if (!p || !out) return PKV_ERR_INVALID;
+  *out = p->cfg;
+  return PKV_OK;
+}
+
+pkv_status pkv_block_record_bytes(const pkv_pool* p, size_t* bytes) {
+  if (!p || !bytes) return PKV_ERR_INVALID;
+  int64_t bb[4];
+  *bytes = record_bytes(p, bb);
+  return PKV_OK;
+}
+
+static pkv_status serde_blocks(pkv_pool* p, int n, const int32_t* rows, uint8_t* buf, size_t buf_bytes, int to_pool,
+                               cudaStream_t s) {
+  if (n == 0) return PKV_OK;
+  if (!rows || !buf || ((uintptr_t)buf & 15u) != 0) return PKV_ERR_INVALID;
+  int64_t bb[4];
+  const size_t rec = record_bytes(p, bb);
+  if (buf_bytes / rec < (size_t)n) return PKV_ERR_RANGE;
+  PKV_CUDA(launch_serde_blocks(p->table_dev, p->cfg.n_layers, p->n_kinds, bb, p->cfg.slab_blocks,
+                               (int64_t)p->groups.size() * p->cfg.slab_blocks, n, rows, buf, (int64_t)rec, to_pool,
+                               p->err_dev, s),
+           to_pool ? "import_blocks launch" : "export_blocks launch");
+  p->last_stream = s;
+  return PKV_OK;
+}
+
+pkv_status pkv_export_blocks(pkv_pool* p, int n, const int32_t* rows_dev, void* out_dev, size_t out_bytes,
+                             void* stream) {
+  if (!p || n < 0) return PKV_ERR_INVALID;
+  return serde_blocks(p, n, rows_dev, (uint8_t*)out_dev, out_bytes, 0, (cudaStream_t)stream);
+}
+
+pkv_status pkv_import_blocks(pkv_pool* p, const pkv_pool_config* identity, int n, const int32_t* rows_dev,
+                             const void* in_dev, size_t in_bytes, void* stream) {
+  if (!p || !identity || n < 0) return PKV_ERR_INVALID;
+  // The records' storage identity (and layer count) must be this pool's, checked
+  // before any device work.
+  if (pkv_pool_check_identity(p, identity) != PKV_OK || identity->n_layers != p->cfg.n_layers) return PKV_ERR_FORMAT;
+  return serde_blocks(p, n, rows_dev, (uint8_t*)const_cast<void*>(in_dev), in_bytes, 1, (cudaStream_t)stream);
 }
 
 pkv_status pkv_gather_visible(pkv_pool* p, int layer, const int32_t* bt_row, int ctx, void* k_out,

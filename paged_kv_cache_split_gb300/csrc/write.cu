@@ -198,6 +198,48 @@ __global__ void copy_blocks_kernel(const uint8_t* const* __restrict__ table, int
     dp[c] = sp[c];
 }
 
+// export / import of block records.  A record holds every stored byte of one
+// block, layer-major, then kind (K, V, K meta, V meta), each the block's
+// [32 tokens][Hkv][row] bytes as stored.  Work item = one (block, layer, kind)
+// piece; CTAs stride over the pieces, and each thread keeps four 16-byte loads in
+// flight before storing them.
+__global__ void __launch_bounds__(256) serde_blocks_kernel(const uint8_t* const* __restrict__ table, int n_layers,
+                                                           int n_kinds, int64_t b0, int64_t b1, int64_t b2,
+                                                           int64_t b3, int slab_blocks, int64_t rows_capacity,
+                                                           int n, const int32_t* __restrict__ rows, uint8_t* buf,
+                                                           int64_t rec_bytes, int to_pool, int32_t* err) {
+  const int64_t per_layer = b0 + b1 + (n_kinds == 4 ? b2 + b3 : 0);
+  const int ppb = n_layers * n_kinds;  // pieces per block; also the pointer-table stride per slab
+  const int64_t pieces = (int64_t)n * ppb;
+  constexpr int U = 4;
+  for (int64_t pc = blockIdx.x; pc < pieces; pc += gridDim.x) {
+    const int i = (int)(pc / ppb), lk = (int)(pc - (int64_t)i * ppb);
+    const int layer = lk / n_kinds, kind = lk - layer * n_kinds;
+    const int32_t r = rows[i];
+    if (r < 0 || (int64_t)r >= rows_capacity) {
+      if (threadIdx.x == 0 && lk == 0) atomicOr(err, ERR_ROW);
+      continue;
+    }
+    const int64_t bytes = kind == 0 ? b0 : kind == 1 ? b1 : kind == 2 ? b2 : b3;
+    const int64_t koff = kind == 0 ? 0 : kind == 1 ? b0 : kind == 2 ? b0 + b1 : b0 + b1 + b2;
+    uint8_t* blk = const_cast<uint8_t*>(table[(size_t)(r / slab_blocks) * ppb + (size_t)lk]) +
+                   (int64_t)(r % slab_blocks) * bytes;
+    uint8_t* rec = buf + (int64_t)i * rec_bytes + (int64_t)layer * per_layer + koff;
+    uint4* dp = reinterpret_cast<uint4*>(to_pool ? blk : rec);
+    const uint4* sp = reinterpret_cast<const uint4*>(to_pool ? rec : blk);
+    const int64_t chunks = bytes / 16;
+    int64_t c = threadIdx.x;
+    for (; c + (U - 1) * (int64_t)blockDim.x < chunks; c += U * (int64_t)blockDim.x) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = sp[c + u * blockDim.x];
+#pragma unroll
+      for (int u = 0; u < U; ++u) dp[c + u * blockDim.x] = v[u];
+    }
+    for (; c < chunks; c += blockDim.x) dp[c] = sp[c];
+  }
+}
+
 // gather_visible: blockIdx.y = kind; grid-stride over (head, token, 16-B chunk).
 __global__ void gather_kernel(LayerView lv, const int32_t* __restrict__ bt_row, int ctx, uint8_t* o0, uint8_t* o1,
                               uint8_t* o2, uint8_t* o3) {
@@ -251,6 +293,20 @@ cudaError_t launch_copy_blocks(const uint8_t* const* table, int n_layers, int n_
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_serde_blocks(const uint8_t* const* table, int n_layers, int n_kinds, const int64_t* block_bytes,
+                               int slab_blocks, int64_t rows_capacity, int n, const int32_t* rows, uint8_t* buf,
+                               int64_t rec_bytes, int to_pool, int32_t* err, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
+  const int64_t pieces = (int64_t)n * n_layers * n_kinds;
+  const int64_t grid = pieces < 8LL * sms ? pieces : 8LL * sms;  // eight 256-thread CTAs per SM
+  serde_blocks_kernel<<<(unsigned)grid, 256, 0, s>>>(table, n_layers, n_kinds, block_bytes[0], block_bytes[1],
+                                                     block_bytes[2], block_bytes[3], slab_blocks, rows_capacity, n,
+                                                     rows, buf, rec_bytes, to_pool, err);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const LayerView& lv, const int32_t* bt_row, int ctx, uint8_t* const* outs, cudaStream_t s) {
