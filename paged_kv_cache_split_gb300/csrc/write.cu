@@ -175,27 +175,40 @@ cudaError_t launch_write_d(const LayerView& lv, int fmt, int n, const int32_t* r
   return cudaGetLastError();
 }
 
-// copy_on_write_block: grid (chunks, pair, layer*kind); 16-byte copies.
-__global__ void copy_blocks_kernel(const uint8_t* const* __restrict__ table, int n_layers, int n_kinds,
-                                   int64_t b0, int64_t b1, int64_t b2, int64_t b3, int slab_blocks,
-                                   int64_t rows_capacity, const int32_t* __restrict__ src,
-                                   const int32_t* __restrict__ dst, int32_t* err) {
-  const int pair = blockIdx.y;
-  const int layer = blockIdx.z / n_kinds, kind = blockIdx.z % n_kinds;
-  const int64_t bytes = kind == 0 ? b0 : kind == 1 ? b1 : kind == 2 ? b2 : b3;
-  const int32_t rs = src[pair], rd = dst[pair];
-  if (rs < 0 || rd < 0 || (int64_t)rs >= rows_capacity || (int64_t)rd >= rows_capacity) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(err, ERR_ROW);
-    return;
+// copy_on_write_block: CTAs stride over (pair, layer, kind) pieces; each thread
+// keeps four 16-byte loads in flight before storing them.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const uint8_t* const* __restrict__ table, int n_layers,
+                                                          int n_kinds, int64_t b0, int64_t b1, int64_t b2, int64_t b3,
+                                                          int slab_blocks, int64_t rows_capacity, int n,
+                                                          const int32_t* __restrict__ src,
+                                                          const int32_t* __restrict__ dst, int32_t* err) {
+  const int ppb = n_layers * n_kinds;  // pieces per pair; also the pointer-table stride per slab
+  const int64_t pieces = (int64_t)n * ppb;
+  constexpr int U = 4;
+  for (int64_t pc = blockIdx.x; pc < pieces; pc += gridDim.x) {
+    const int pair = (int)(pc / ppb), lk = (int)(pc - (int64_t)pair * ppb);
+    const int kind = lk % n_kinds;
+    const int64_t bytes = kind == 0 ? b0 : kind == 1 ? b1 : kind == 2 ? b2 : b3;
+    const int32_t rs = src[pair], rd = dst[pair];
+    if (rs < 0 || rd < 0 || (int64_t)rs >= rows_capacity || (int64_t)rd >= rows_capacity) {
+      if (threadIdx.x == 0 && lk == 0) atomicOr(err, ERR_ROW);
+      continue;
+    }
+    const uint4* sp = reinterpret_cast<const uint4*>(table[(size_t)(rs / slab_blocks) * ppb + (size_t)lk] +
+                                                     (int64_t)(rs % slab_blocks) * bytes);
+    uint4* dp = reinterpret_cast<uint4*>(const_cast<uint8_t*>(table[(size_t)(rd / slab_blocks) * ppb + (size_t)lk]) +
+                                         (int64_t)(rd % slab_blocks) * bytes);
+    const int64_t chunks = bytes / 16;
+    int64_t c = threadIdx.x;
+    for (; c + (U - 1) * (int64_t)blockDim.x < chunks; c += U * (int64_t)blockDim.x) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = sp[c + u * blockDim.x];
+#pragma unroll
+      for (int u = 0; u < U; ++u) dp[c + u * blockDim.x] = v[u];
+    }
+    for (; c < chunks; c += blockDim.x) dp[c] = sp[c];
   }
-  const int stride = n_layers * n_kinds;
-  const uint8_t* sbase = table[(size_t)(rs / slab_blocks) * stride + (size_t)layer * n_kinds + kind];
-  uint8_t* dbase = const_cast<uint8_t*>(table[(size_t)(rd / slab_blocks) * stride + (size_t)layer * n_kinds + kind]);
-  const uint4* sp = reinterpret_cast<const uint4*>(sbase + (int64_t)(rs % slab_blocks) * bytes);
-  uint4* dp = reinterpret_cast<uint4*>(dbase + (int64_t)(rd % slab_blocks) * bytes);
-  const int64_t chunks = bytes / 16;
-  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < chunks; c += (int64_t)gridDim.x * blockDim.x)
-    dp[c] = sp[c];
 }
 
 // export / import of block records.  A record holds every stored byte of one
@@ -275,34 +288,31 @@ cudaError_t launch_write(const LayerView& lv, int fmt, int D, int n, const int32
   }
 }
 
+static int sm_count() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
+  return sms;
+}
+
 cudaError_t launch_copy_blocks(const uint8_t* const* table, int n_layers, int n_kinds, const int64_t* block_bytes,
                                int slab_blocks, int64_t rows_capacity, int n, const int32_t* src,
                                const int32_t* dst, int32_t* err, cudaStream_t s) {
-  int64_t maxb = 0;
-  for (int k = 0; k < n_kinds; ++k) maxb = block_bytes[k] > maxb ? block_bytes[k] : maxb;
-  const int threads = 256;
-  const unsigned gx = (unsigned)((maxb / 16 + threads - 1) / threads);
-  // gridDim.y <= 65535 pairs per launch: split larger requests.
-  for (int first = 0; first < n; first += 65535) {
-    const int cnt = (n - first) < 65535 ? (n - first) : 65535;
-    dim3 grid(gx, (unsigned)cnt, (unsigned)(n_layers * n_kinds));
-    copy_blocks_kernel<<<grid, threads, 0, s>>>(table, n_layers, n_kinds, block_bytes[0], block_bytes[1],
-                                                block_bytes[2], block_bytes[3], slab_blocks, rows_capacity,
-                                                src + first, dst + first, err);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  const int64_t pieces = (int64_t)n * n_layers * n_kinds;
+  const int64_t cap = 8LL * sm_count();  // eight 256-thread CTAs per SM
+  const int64_t grid = pieces < cap ? pieces : cap;
+  copy_blocks_kernel<<<(unsigned)grid, 256, 0, s>>>(table, n_layers, n_kinds, block_bytes[0], block_bytes[1],
+                                                    block_bytes[2], block_bytes[3], slab_blocks, rows_capacity, n,
+                                                    src, dst, err);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_serde_blocks(const uint8_t* const* table, int n_layers, int n_kinds, const int64_t* block_bytes,
                                int slab_blocks, int64_t rows_capacity, int n, const int32_t* rows, uint8_t* buf,
                                int64_t rec_bytes, int to_pool, int32_t* err, cudaStream_t s) {
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
   const int64_t pieces = (int64_t)n * n_layers * n_kinds;
-  const int64_t grid = pieces < 8LL * sms ? pieces : 8LL * sms;  // eight 256-thread CTAs per SM
+  const int64_t cap = 8LL * sm_count();  // eight 256-thread CTAs per SM
+  const int64_t grid = pieces < cap ? pieces : cap;
   serde_blocks_kernel<<<(unsigned)grid, 256, 0, s>>>(table, n_layers, n_kinds, block_bytes[0], block_bytes[1],
                                                      block_bytes[2], block_bytes[3], slab_blocks, rows_capacity, n,
                                                      rows, buf, rec_bytes, to_pool, err);
