@@ -112,21 +112,24 @@ def test_quant_worked_example(golden_dir):
     assert meta[0, 0] == float(rows["scale"][0]) and meta[0, 1] == float(rows["offset"][0])
 
 
+@pytest.mark.parametrize("group", [32, 64])
 @pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("D", [64, 128, 256])
-def test_quant_error_bound(bits, D):
-    rng = np.random.default_rng(bits * 1000 + D)
+def test_quant_error_bound(bits, D, group):
+    rng = np.random.default_rng(bits * 1000 + D + group)
     for trial in range(20):
         x = (rng.standard_normal(D) * rng.choice([1e-3, 1.0, 40.0])).astype(np.float32)
-        codes, meta = oracle.quantize(x, bits)
-        xh = oracle.dequantize(codes, meta, D, bits)
-        for g in range(D // 32):
-            xs = x[32 * g: 32 * g + 32].astype(np.float64)
+        codes, meta = oracle.quantize(x, bits, group)
+        assert meta.shape == (D // group, 2)
+        xh = oracle.dequantize(codes, meta, D, bits, group)
+        for g in range(D // group):
+            xs = x[group * g: group * g + group].astype(np.float64)
             sc = float(meta[g, 0])
             # half a step plus the float32 rounding of the scale, offset and difference
             slack = 4 * np.spacing(np.float32(np.abs(xs).max()))
-            assert np.abs(xs - xh[32 * g: 32 * g + 32]).max() <= sc / 2 + slack
+            assert np.abs(xs - xh[group * g: group * g + group]).max() <= sc / 2 + slack
             assert meta[g, 1] == np.float32(xs.min())
+            assert sc == np.float32(np.float32(xs.max()) - np.float32(xs.min())) / np.float32(2 ** bits - 1)
 
 
 @pytest.mark.parametrize("bits", [4, 8])
@@ -169,6 +172,11 @@ def test_payload_ratio(golden_dir):
         bits = 8 * sum(p.row_bytes) / (2 * 128)
         assert bits == rows[key][0]
         assert abs(16 / bits - rows[key][1]) < 1e-12
+    # groups of 64 with one FP32 pair reach the page's five bits
+    p = OraclePool(1, 8, 128, FMT_K4V4, group_size=64)
+    bits = 8 * sum(p.row_bytes) / (2 * 128)
+    assert bits == rows["k4v4_g64_f32pair"][0] == rows["page_k4v4_5bit"][0]
+    assert 16 / bits == rows["k4v4_g64_f32pair"][1]
 
 
 # ---------------------------------------------------------------------------
@@ -295,14 +303,15 @@ def _decode_gathered(p, g, L):
         return k, v
     kb, vb = oracle.FORMAT_BITS[p.fmt]
     out = []
+    gs = p.group_size
     for codes, meta, bits in [(g[0], g[2], kb), (g[1], g[3], vb)]:
-        m = meta.view(np.float32).reshape(H, L, D // 32, 2)
+        m = meta.view(np.float32).reshape(H, L, D // gs, 2)
         if bits == 8:
             c = codes.reshape(H, L, D).astype(np.float64)
         else:
             c = np.stack([codes & 15, codes >> 4], -1).reshape(H, L, D).astype(np.float64)
-        sc = np.repeat(m[..., 0].astype(np.float64), 32, axis=-1)
-        of = np.repeat(m[..., 1].astype(np.float64), 32, axis=-1)
+        sc = np.repeat(m[..., 0].astype(np.float64), gs, axis=-1)
+        of = np.repeat(m[..., 1].astype(np.float64), gs, axis=-1)
         out.append(c * sc + of)
     return out[0], out[1]
 
@@ -327,14 +336,15 @@ def _brute(p, q_bits, bt, lens, scale):
     return out
 
 
-@pytest.mark.parametrize("fmt", [FMT_BF16, FMT_K4V4, FMT_K8V4, FMT_K8V8])
-def test_attention_brute_force(fmt):
-    H, G, D = 2, 3, 64
+@pytest.mark.parametrize("fmt,group,D", [(FMT_BF16, 32, 64), (FMT_K4V4, 32, 64), (FMT_K8V4, 32, 64),
+                                         (FMT_K8V8, 32, 64), (FMT_K4V4, 64, 128)])
+def test_attention_brute_force(fmt, group, D):
+    H, G = 2, 3
     lens = [1, 31, 33, 97, 0]
     rng = wl.rng_for(21, fmt)
     nblk = [max(1, wl.nblocks(L)) for L in lens]
     rows, used = wl.fragmented_rows(nblk, wl.rng_for(22))
-    p = OraclePool(1, H, D, fmt, seed=0x77)
+    p = OraclePool(1, H, D, fmt, seed=0x77, group_size=group)
     p.reserve_rows(used)
     _fill(p, 0, rows, lens, [(wl.bf16_normal(rng, (L, H, D)), wl.bf16_normal(rng, (L, H, D))) for L in lens])
     q = wl.bf16_normal(rng, (len(lens), H * G, D))
@@ -409,11 +419,12 @@ def test_gqa_mapping_uses_floor_division():
     assert np.allclose(out[0, :, 0], np.arange(H * G) // G)
 
 
-@pytest.mark.parametrize("fmt,kb,vb", [(FMT_K4V4, 4, 4), (FMT_K8V4, 8, 4), (FMT_K8V8, 8, 8)])
-def test_pool_write_equals_rotate_then_quantize(fmt, kb, vb):
+@pytest.mark.parametrize("fmt,kb,vb,group", [(FMT_K4V4, 4, 4, 32), (FMT_K8V4, 8, 4, 32), (FMT_K8V8, 8, 8, 32),
+                                            (FMT_K4V4, 4, 4, 64)])
+def test_pool_write_equals_rotate_then_quantize(fmt, kb, vb, group):
     """The pool image's packed write path equals the pinned primitives composed."""
     H, D = 2, 128
-    p = OraclePool(1, H, D, fmt, seed=0x5EED)
+    p = OraclePool(1, H, D, fmt, seed=0x5EED, group_size=group)
     p.reserve_rows(32)
     rng = wl.rng_for(61)
     k, v = wl.bf16_normal(rng, (5, H, D), 0.01), wl.bf16_normal(rng, (5, H, D), 0.01)
@@ -424,8 +435,8 @@ def test_pool_write_equals_rotate_then_quantize(fmt, kb, vb):
         for h in range(H):
             rk, exact = oracle.rotate_k(k[t, h], s)
             assert exact
-            c, m = oracle.quantize(rk, kb)
+            c, m = oracle.quantize(rk, kb, group)
             assert np.array_equal(kc[h, t], c) and np.array_equal(km[h, t].view(np.float32), m.reshape(-1))
-            c, m = oracle.quantize(wl.bf16_bits_to_f32(v[t, h]), vb)
+            c, m = oracle.quantize(wl.bf16_bits_to_f32(v[t, h]), vb, group)
             assert np.array_equal(vc[h, t], c) and np.array_equal(vm[h, t].view(np.float32), m.reshape(-1))
     assert p.inexact_rotations == 0
