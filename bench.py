@@ -44,15 +44,15 @@ FMT_ROW_BYTES = {wl.FMT_BF16: (2.0, 2.0, 0), wl.FMT_K4V4: (0.5, 0.5, 1), wl.FMT_
                  wl.FMT_K8V8: (1.0, 1.0, 1)}
 
 
-def token_head_bytes(fmt: int, D: int) -> int:
+def token_head_bytes(fmt: int, D: int, group: int = 32) -> int:
     kb, vb, packed = FMT_ROW_BYTES[fmt]
-    return int(kb * D + vb * D + packed * 2 * (D // 32) * 8)
+    return int(kb * D + vb * D + packed * 2 * (D // group) * 8)
 
 
-def algorithmic_bytes(fmt, D, Hkv, Hq, lens) -> int:
+def algorithmic_bytes(fmt, D, Hkv, Hq, lens, group: int = 32) -> int:
     """K/V payload + metadata of tokens < L, q and out, block-table entries used, ctx."""
     B = len(lens)
-    kv = sum(lens) * Hkv * token_head_bytes(fmt, D)
+    kv = sum(lens) * Hkv * token_head_bytes(fmt, D, group)
     qo = 2 * B * Hq * D * 2
     bt = sum(wl.nblocks(L) for L in lens) * 4
     return kv + qo + bt + 4 * B
@@ -71,6 +71,8 @@ def workload_for(name: str):
         return wl.tiny()
     if name == "qwen3-1.7b-k4v4":
         return wl.qwen3_1_7b_k4v4()
+    if name == "qwen3-1.7b-k4v4-g64":
+        return wl.qwen3_1_7b_k4v4_g64()
     if name == "llama-3.2-1b-k8v4":
         return wl.llama_1b(wl.FMT_K8V4)
     if name == "llama-3.2-1b-k8v8":
@@ -82,7 +84,8 @@ def describe(w) -> str:
     L = sorted(set(w.lens))
     lens = f"{w.B} x {L[0]}" if len(L) == 1 else f"{w.B} x [{min(w.lens)}..{max(w.lens)}]"
     return (f"{w.name}-shaped decode: {w.n_layers} layer(s), Hq {w.Hq} / Hkv {w.Hkv} / D {w.D}, "
-            f"{wl.FMT_NAMES[w.fmt]}, {lens} tokens, 32-token blocks, 32-block slabs")
+            f"{wl.FMT_NAMES[w.fmt]}{'' if w.fmt == wl.FMT_BF16 else f' (groups of {w.group})'}, {lens} tokens, "
+            f"32-token blocks, 32-block slabs")
 
 
 # ---------------------------------------------------------------------------
@@ -227,7 +230,7 @@ class OracleRun:
         import oracle
         self.cores = len(os.sched_getaffinity(0))
         self.seqs = list(range(w.B if max_seqs is None else min(max_seqs, w.B)))
-        o = oracle.OraclePool(1, w.Hkv, w.D, w.fmt, seed=w.hadamard_seed)
+        o = oracle.OraclePool(1, w.Hkv, w.D, w.fmt, seed=w.hadamard_seed, group_size=w.group)
         o.reserve_rows(w.rows_used)
         for b in self.seqs:
             k, v = w.kv(0, b)
@@ -238,7 +241,7 @@ class OracleRun:
         self.bt = w.block_table()[self.seqs]
         self.ctx = w.ctx()[self.seqs]
         self.lens = [w.lens[b] for b in self.seqs]
-        self.nbytes = algorithmic_bytes(w.fmt, w.D, w.Hkv, w.Hq, self.lens)
+        self.nbytes = algorithmic_bytes(w.fmt, w.D, w.Hkv, w.Hq, self.lens, w.group)
 
     def run(self) -> float:
         t0 = time.perf_counter()
@@ -279,7 +282,7 @@ def run_gpu(args, rank, world, local):
         w = wl.scaled(w, w.name, n_layers=args.layers)
     dev = torch.device("cuda", local)
     pool = pkv.Pool(w.n_layers, w.Hkv, w.D, pkv.FORMAT_NAMES[w.fmt], hadamard_seed=w.hadamard_seed,
-                    max_slabs=(w.rows_used + 31) // 32 + 8)
+                    max_slabs=(w.rows_used + 31) // 32 + 8, group_size=w.group)
     pool.reserve_rows(w.rows_used)
     gen = torch.Generator(device=dev)
     gen.manual_seed(1000 + w.seed * 100 + rank)
@@ -390,7 +393,7 @@ def run_gpu(args, rank, world, local):
 
     ms_step = dist_max(ms_step, world)
     ms_e2e = dist_max(ms_e2e, world)
-    bytes_layer = algorithmic_bytes(w.fmt, w.D, w.Hkv, w.Hq, w.lens)
+    bytes_layer = algorithmic_bytes(w.fmt, w.D, w.Hkv, w.Hq, w.lens, w.group)
     bytes_step = bytes_layer * w.n_layers
     tokens_step = sum(w.lens) * w.n_layers
     value = bytes_step * world / (ms_step * 1e-3) / 1e9

@@ -170,9 +170,10 @@ class Pool:
 
     def __init__(self, n_layers: int, n_kv_heads: int, head_dim: int, format="bf16", hadamard_seed: int = 0,
                  slab_blocks: int = 32, max_slabs: int = 1024, allocator: Optional[Allocator] = None,
-                 stream=None):
+                 stream=None, group_size: int = 32):
         self._lib = lib()
-        self.cfg = make_config(n_layers, n_kv_heads, head_dim, format, hadamard_seed, slab_blocks, max_slabs)
+        self.cfg = make_config(n_layers, n_kv_heads, head_dim, format, hadamard_seed, slab_blocks, max_slabs,
+                               group_size=group_size)
         self.n_layers, self.n_kv_heads, self.head_dim = n_layers, n_kv_heads, head_dim
         self.format = FORMAT_NAMES[self.cfg.format]
         self.slab_blocks = slab_blocks

@@ -2,5 +2,8 @@
 #include "decode_packed_mma.cuh"
 
 namespace pkv {
-cudaError_t launch_decode_k4v4(const DecodeArgs& a) { return launch_decode_packed_mma<PKV_FMT_K4V4>(a); }
+cudaError_t launch_decode_k4v4(const DecodeArgs& a) {
+  if (a.group == kGroupWide) return launch_decode_k4v4_g64(a);
+  return launch_decode_packed_mma<PKV_FMT_K4V4>(a);
+}
 }  // namespace pkv

@@ -81,17 +81,21 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t r) {
   return __half22float2(*reinterpret_cast<const __half2*>(&r));
 }
 
-template <int FMT, int D>
+template <int FMT, int D, int GS = kGroup>
 struct PackedTraits {
   static constexpr int KBITS = FMT == PKV_FMT_K4V4 ? 4 : 8;
   static constexpr int VBITS = FMT == PKV_FMT_K8V8 ? 8 : 4;
   static constexpr int KB = D * KBITS / 8;   // K code bytes per (token, head)
   static constexpr int VB = D * VBITS / 8;
-  static constexpr int NG = D / kGroup;      // affine groups per row
-  static constexpr int MB = NG * 8;          // (scale, offset) bytes per (token, head)
+  static constexpr int NG = D / 32;          // 32-dim groups per row (the unit of the fold)
+  static constexpr int SPP = GS / 32;        // 32-dim groups sharing one (scale, offset) pair
+  static constexpr int MB = (D / GS) * 8;    // (scale, offset) bytes per (token, head)
   static constexpr int NKC = KB / 16;        // 16-byte chunks per (token, head)
   static constexpr int NVC = VB / 16;
-  static constexpr int NMC = MB / 16;        // = NG / 2: two groups' (s, o) per chunk
+  static constexpr int NMC = MB / 16;        // two pairs per chunk
+  static constexpr int SPC = 2 * SPP;        // 32-dim groups per metadata chunk
+  static_assert(GS == 32 || GS == 64, "group size");
+  static_assert(MB % 16 == 0, "whole metadata chunks per (token, head)");
 };
 
 // B fragments of K for one group and one token (this lane's token of the n-tile),
@@ -175,9 +179,9 @@ constexpr int kProdRegs = 56;
 // the output).  Per 16-token chunk the two halves of every logit are exchanged
 // through shared memory and added in a fixed order, so both warps run the same
 // softmax; each keeps the state of its own dims.
-template <int FMT, int D, int G, bool W128, bool RS, bool DS>
+template <int FMT, int D, int G, bool W128, bool RS, bool DS, int GS>
 __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packed_mma_kernel(const DecodeParams P) {
-  using Tr = PackedTraits<FMT, D>;
+  using Tr = PackedTraits<FMT, D, GS>;
   static_assert(G >= 1 && G <= 8 && D % 32 == 0, "geometry");
   static_assert(!DS || (W128 && D == 256), "dim split: 128-byte boxes, D = 256");
   constexpr int NG = Tr::NG;
@@ -407,8 +411,9 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
         const float4 m0 = lds128(m_addr(sb, 2, kc, j, 0, cm));  // token 8j + 2t
         const float4 m1 = lds128(m_addr(sb, 2, kc, j, 1, cm));  // token 8j + 2t + 1
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-          const int grp = 2 * cm + q2;
+        for (int q = 0; q < Tr::SPC; ++q) {
+          const int grp = Tr::SPC * cm + q;
+          const bool q2 = q >= Tr::SPP;  // second pair of the chunk
           uint32_t bfr[2][2];
           if constexpr (Tr::KBITS == 4) {
             k_group_frags4(kw[jj][grp], bfr);
@@ -510,8 +515,9 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 #pragma unroll
         for (int e = 0; e < 2; ++e) mv[pp][e] = lds128(m_addr(sb, 3, kc, pp, e, cm));
 #pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2) {
-        const int grp = 2 * cm + q2;
+      for (int q = 0; q < Tr::SPC; ++q) {
+        const int grp = Tr::SPC * cm + q;
+        const bool q2 = q >= Tr::SPP;  // second pair of the chunk
         float sv[2][2], ov[2][2];
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp)
@@ -737,9 +743,9 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   }
 }
 
-template <int FMT, int D, int G, bool W128, bool RS, bool DS>
+template <int FMT, int D, int G, bool W128, bool RS, bool DS, int GS>
 cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
-  using Tr = PackedTraits<FMT, D>;
+  using Tr = PackedTraits<FMT, D, GS>;
   DecodeParams P;
   P.lv = a.lv;
   P.B = a.B;
@@ -758,7 +764,7 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   P.NS = a.n_stages;
   const int hkv = a.lv.hkv;
   P.stage_bytes = packed_stage_bytes(P.T, hkv * Tr::KB, hkv * Tr::VB, hkv * Tr::MB, a.Hq * D * 2);
-  auto kern = decode_packed_mma_kernel<FMT, D, G, W128, RS, DS>;
+  auto kern = decode_packed_mma_kernel<FMT, D, G, W128, RS, DS, GS>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
@@ -786,23 +792,25 @@ bool register_split_fits(Kern kern) {
   return verdict == 1;
 }
 
-template <int FMT>
+template <int FMT, int GS = kGroup>
 cudaError_t launch_decode_packed_mma(const DecodeArgs& a) {
   const bool w128 = a.lv.box_bytes[0] == 128 && a.lv.box_bytes[1] == 128 && a.lv.box_bytes[2] == 128 &&
                     a.lv.box_bytes[3] == 128;
-#define PKV_CASE(DD, GG)                                                                                     \
-  if (a.D == DD && a.G == GG) {                                                                              \
-    if (DD == 256 && a.dim_split) {                                                                          \
-      if (register_split_fits(decode_packed_mma_kernel<FMT, 256, GG, true, true, true>))                    \
-        return launch_decode_packed_mma_t<FMT, 256, GG, true, true, true>(a);                                \
-      return launch_decode_packed_mma_t<FMT, 256, GG, true, false, true>(a);                                 \
-    }                                                                                                        \
-    if (w128 && DD >= 128 && register_split_fits(decode_packed_mma_kernel<FMT, DD, GG, true, true, false>))  \
-      return launch_decode_packed_mma_t<FMT, DD, GG, true, true, false>(a);                                  \
-    return w128 ? launch_decode_packed_mma_t<FMT, DD, GG, true, false, false>(a)                             \
-                : launch_decode_packed_mma_t<FMT, DD, GG, false, false, false>(a);                           \
+#define PKV_CASE(DD, GG)                                                                                      \
+  if (a.D == DD && a.G == GG) {                                                                               \
+    if (DD == 256 && a.dim_split) {                                                                           \
+      if (register_split_fits(decode_packed_mma_kernel<FMT, 256, GG, true, true, true, GS>))                 \
+        return launch_decode_packed_mma_t<FMT, 256, GG, true, true, true, GS>(a);                             \
+      return launch_decode_packed_mma_t<FMT, 256, GG, true, false, true, GS>(a);                              \
+    }                                                                                                         \
+    if (w128 && DD >= 128 && register_split_fits(decode_packed_mma_kernel<FMT, DD, GG, true, true, false, GS>)) \
+      return launch_decode_packed_mma_t<FMT, DD, GG, true, true, false, GS>(a);                               \
+    return w128 ? launch_decode_packed_mma_t<FMT, DD, GG, true, false, false, GS>(a)                          \
+                : launch_decode_packed_mma_t<FMT, DD, GG, false, false, false, GS>(a);                        \
   }
-  PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
+  if constexpr (GS == kGroup) {
+    PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
+  }
   PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
   PKV_CASE(256, 1) PKV_CASE(256, 2) PKV_CASE(256, 4) PKV_CASE(256, 8)
 #undef PKV_CASE

@@ -19,7 +19,8 @@ enum : int32_t {
 };
 
 constexpr int kBlockTokens = 32;  // tokens per block (block_size)
-constexpr int kGroup = 32;        // values per affine group
+constexpr int kGroup = 32;        // values per affine group (default)
+constexpr int kGroupWide = 64;    // K4/V4 only, D >= 128: one (scale, offset) pair per 64 values
 
 struct FormatBits {
   int k, v;  // bits per stored K / V value (16 = bf16)
@@ -237,11 +238,13 @@ struct DecodeArgs {
   size_t smem_bytes;
   cudaStream_t stream;
   int dim_split;        // see DecodePlan
+  int group;            // values per affine group of the packed formats: 32 or 64 (K4/V4)
 };
 
 // Returns cudaSuccess or the launch error.  Defined per format in decode_*.cu.
 cudaError_t launch_decode_bf16(const DecodeArgs& a);
 cudaError_t launch_decode_k4v4(const DecodeArgs& a);
+cudaError_t launch_decode_k4v4_g64(const DecodeArgs& a);  // groups of 64 (decode_k4v4g64.cu)
 cudaError_t launch_decode_k8v4(const DecodeArgs& a);
 cudaError_t launch_decode_k8v8(const DecodeArgs& a);
 
@@ -254,9 +257,9 @@ struct DecodePlan {
   int threads;
   int dim_split;  // packed D = 256, at most 4 kv heads, 128-byte rows: two warps per kv head
 };
-bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan);
+bool plan_decode(int fmt, int D, int G, int hkv, int B, int group, DecodePlan* plan);
 
-cudaError_t launch_write(const LayerView& lv, int fmt, int D, int n, const int32_t* rows,
+cudaError_t launch_write(const LayerView& lv, int fmt, int D, int group, int n, const int32_t* rows,
                          const int32_t* slots, const uint16_t* k, const uint16_t* v,
                          const float* signs, double inv_sqrt_d, cudaStream_t s);
 cudaError_t launch_copy_blocks(const uint8_t* const* table, int n_layers, int n_kinds,

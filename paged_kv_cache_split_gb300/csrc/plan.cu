@@ -7,11 +7,12 @@ namespace pkv {
 // or 16, NS <= 8), leaving room for the barriers, the staged slab table, the
 // per-sequence unit prefix and, for packed formats, the per-warp q scratch used by
 // the Hadamard rotation.
-bool plan_decode(int fmt, int D, int G, int hkv, int B, DecodePlan* plan) {
+bool plan_decode(int fmt, int D, int G, int hkv, int B, int group, DecodePlan* plan) {
   const FormatBits fb = format_bits(fmt);
   if (fb.k == 0 || hkv < 1 || hkv > 8 || B < 1 || B > 4096) return false;
   const bool packed = fmt != PKV_FMT_BF16;
-  const size_t meta = packed ? (size_t)(D / kGroup) * 8 : 0;
+  if (packed && (group <= 0 || D % group)) return false;
+  const size_t meta = packed ? (size_t)(D / group) * 8 : 0;
   const size_t budget = 232448;  // 227 KB opt-in shared memory per block on sm_100-class parts
   // + staged slab table (kSmemTableEntries) + the producers' two token barriers
   size_t fixed = (size_t)(2 * B + 1 + 4) * 4 + 16 + 128 + 1024 * sizeof(void*) + 32;

@@ -180,7 +180,12 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_allocator* allo
       !(D == 64 || D == 128 || D == 256) || cfg->block_size != kBlockTokens || cfg->slab_blocks < 1 ||
       cfg->slab_blocks > 4096 || cfg->max_slabs < 1)
     return PKV_ERR_INVALID;
-  if (cfg->format != PKV_FMT_BF16 && cfg->group_size != kGroup) return PKV_ERR_INVALID;
+  // Groups of 32 for every packed format; groups of 64 (the five-bit K4/V4 layout)
+  // for K4/V4 with head_dim >= 128, so a (token, head) metadata row stays a whole
+  // number of 16-byte chunks.
+  if (cfg->format != PKV_FMT_BF16 && cfg->group_size != kGroup &&
+      !(cfg->group_size == kGroupWide && cfg->format == PKV_FMT_K4V4 && D >= 128))
+    return PKV_ERR_INVALID;
   if (alloc && (!alloc->alloc || !alloc->release)) return PKV_ERR_INVALID;
 
   pkv_pool* p = new (std::nothrow) pkv_pool();
@@ -209,7 +214,7 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_allocator* allo
   p->row_bytes[PKV_KIND_K] = (int64_t)D * fb.k / 8;
   p->row_bytes[PKV_KIND_V] = (int64_t)D * fb.v / 8;
   if (p->n_kinds == 4) {
-    p->row_bytes[PKV_KIND_KMETA] = (int64_t)(D / kGroup) * 2 * sizeof(float);
+    p->row_bytes[PKV_KIND_KMETA] = (int64_t)(D / cfg->group_size) * 2 * sizeof(float);
     p->row_bytes[PKV_KIND_VMETA] = p->row_bytes[PKV_KIND_KMETA];
   }
   const int64_t per_row_tokens = (int64_t)cfg->slab_blocks * kBlockTokens * cfg->n_kv_heads;
@@ -408,7 +413,7 @@ pkv_status pkv_write_block(pkv_pool* p, int layer, int n, const int32_t* rows, c
   if (((uintptr_t)k & 15u) != 0 || ((uintptr_t)v & 15u) != 0) return PKV_ERR_INVALID;
   cudaStream_t s = (cudaStream_t)stream;
   LayerView lv = layer_view(p, layer);
-  PKV_CUDA(launch_write(lv, p->cfg.format, p->cfg.head_dim, n, rows, slots, (const uint16_t*)k,
+  PKV_CUDA(launch_write(lv, p->cfg.format, p->cfg.head_dim, p->cfg.group_size, n, rows, slots, (const uint16_t*)k,
                         (const uint16_t*)v, p->signs_dev, p->inv_sqrt_d, s),
            "write_block launch");
   p->last_stream = s;
@@ -539,7 +544,8 @@ pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, con
   if (((uintptr_t)ws & 255u) != 0 || ((uintptr_t)q & 15u) != 0 || ((uintptr_t)out & 15u) != 0)
     return PKV_ERR_INVALID;
   DecodePlan plan;
-  if (!plan_decode(p->cfg.format, p->cfg.head_dim, G, hkv, B, &plan) || plan.smem_bytes > p->smem_optin)
+  if (!plan_decode(p->cfg.format, p->cfg.head_dim, G, hkv, B, p->cfg.group_size, &plan) ||
+      plan.smem_bytes > p->smem_optin)
     return PKV_ERR_INVALID;
   DecodeArgs a;
   a.lv = layer_view(p, layer);
@@ -562,6 +568,7 @@ pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, con
   a.tokens_per_stage = plan.tokens_per_stage;
   a.n_stages = plan.n_stages;
   a.dim_split = plan.dim_split;
+  a.group = p->cfg.group_size;
   a.smem_bytes = plan.smem_bytes;
   a.stream = (cudaStream_t)stream;
   cudaError_t e;

@@ -55,12 +55,13 @@ __global__ void __launch_bounds__(256) write_bf16_kernel(LayerView lv, int n, co
 }
 
 // Quantise E consecutive values per lane (lane owns dims [lane*E, lane*E+E)) to
-// `BITS`-bit codes with groups of 32 dims (32/E lanes per group) and store codes
+// `BITS`-bit codes with groups of GS dims (GS/E lanes per group) and store codes
 // and (scale, offset).  All arithmetic is IEEE single precision, one rounding per
 // operation, so the codes match a plain sequential CPU statement bit for bit.
-template <int E, int BITS>
+template <int E, int BITS, int GS>
 __device__ __forceinline__ void quantise_store(const float (&x)[E], uint8_t* code_row, float* meta_row, int lane) {
-  constexpr int LPG = 32 / E;  // lanes per group
+  constexpr int LPG = GS / E;  // lanes per group
+  static_assert(LPG >= 1 && LPG <= 32, "group geometry");
   float mn = x[0], mx = x[0];
 #pragma unroll
   for (int e = 1; e < E; ++e) {
@@ -103,7 +104,7 @@ __device__ __forceinline__ void quantise_store(const float (&x)[E], uint8_t* cod
 // bf16 rows whose binary-exponent spread is at most 45 - log2(D), so the order of
 // the butterflies does not matter), multiplied by 1/sqrt(D) in FP64 and rounded
 // once to FP32; V is quantised as stored.
-template <int D, int KBITS, int VBITS>
+template <int D, int KBITS, int VBITS, int GS>
 __global__ void __launch_bounds__(256) write_packed_kernel(LayerView lv, int n, const int32_t* __restrict__ rows,
                                                            const int32_t* __restrict__ slots,
                                                            const uint16_t* __restrict__ k,
@@ -152,14 +153,14 @@ __global__ void __launch_bounds__(256) write_packed_kernel(LayerView lv, int n, 
     xk[e] = __double2float_rn(__dmul_rn(xd[e], inv_sqrt_d));
     xv[e] = __uint_as_float((uint32_t)vr[e] << 16);
   }
-  quantise_store<E, KBITS>(xk, row_addr(lv, PKV_KIND_K, row, slot, h),
+  quantise_store<E, KBITS, GS>(xk, row_addr(lv, PKV_KIND_K, row, slot, h),
                            reinterpret_cast<float*>(row_addr(lv, PKV_KIND_KMETA, row, slot, h)), lane);
-  quantise_store<E, VBITS>(xv, row_addr(lv, PKV_KIND_V, row, slot, h),
+  quantise_store<E, VBITS, GS>(xv, row_addr(lv, PKV_KIND_V, row, slot, h),
                            reinterpret_cast<float*>(row_addr(lv, PKV_KIND_VMETA, row, slot, h)), lane);
 }
 
 template <int D>
-cudaError_t launch_write_d(const LayerView& lv, int fmt, int n, const int32_t* rows, const int32_t* slots,
+cudaError_t launch_write_d(const LayerView& lv, int fmt, int group, int n, const int32_t* rows, const int32_t* slots,
                            const uint16_t* k, const uint16_t* v, const float* signs, double inv, cudaStream_t s) {
   const int64_t warps = (int64_t)n * lv.hkv;
   // A step's write (a few tokens) runs one warp per CTA, so its warps spread over
@@ -168,9 +169,15 @@ cudaError_t launch_write_d(const LayerView& lv, int fmt, int n, const int32_t* r
   const unsigned grid = (unsigned)((warps * 32 + threads - 1) / threads);
   switch (fmt) {
     case PKV_FMT_BF16: write_bf16_kernel<D><<<grid, threads, 0, s>>>(lv, n, rows, slots, k, v); break;
-    case PKV_FMT_K4V4: write_packed_kernel<D, 4, 4><<<grid, threads, 0, s>>>(lv, n, rows, slots, k, v, signs, inv); break;
-    case PKV_FMT_K8V4: write_packed_kernel<D, 8, 4><<<grid, threads, 0, s>>>(lv, n, rows, slots, k, v, signs, inv); break;
-    default: write_packed_kernel<D, 8, 8><<<grid, threads, 0, s>>>(lv, n, rows, slots, k, v, signs, inv); break;
+    case PKV_FMT_K4V4:
+      if (D >= 128 && group == kGroupWide)
+        write_packed_kernel<D, 4, 4, (D >= 128 ? kGroupWide : kGroup)><<<grid, threads, 0, s>>>(lv, n, rows, slots, k,
+                                                                                               v, signs, inv);
+      else
+        write_packed_kernel<D, 4, 4, kGroup><<<grid, threads, 0, s>>>(lv, n, rows, slots, k, v, signs, inv);
+      break;
+    case PKV_FMT_K8V4: write_packed_kernel<D, 8, 4, kGroup><<<grid, threads, 0, s>>>(lv, n, rows, slots, k, v, signs, inv); break;
+    default: write_packed_kernel<D, 8, 8, kGroup><<<grid, threads, 0, s>>>(lv, n, rows, slots, k, v, signs, inv); break;
   }
   return cudaGetLastError();
 }
@@ -278,13 +285,13 @@ __global__ void gather_kernel(LayerView lv, const int32_t* __restrict__ bt_row, 
 
 }  // namespace
 
-cudaError_t launch_write(const LayerView& lv, int fmt, int D, int n, const int32_t* rows, const int32_t* slots,
-                         const uint16_t* k, const uint16_t* v, const float* signs, double inv_sqrt_d,
-                         cudaStream_t s) {
+cudaError_t launch_write(const LayerView& lv, int fmt, int D, int group, int n, const int32_t* rows,
+                         const int32_t* slots, const uint16_t* k, const uint16_t* v, const float* signs,
+                         double inv_sqrt_d, cudaStream_t s) {
   switch (D) {
-    case 64: return launch_write_d<64>(lv, fmt, n, rows, slots, k, v, signs, inv_sqrt_d, s);
-    case 128: return launch_write_d<128>(lv, fmt, n, rows, slots, k, v, signs, inv_sqrt_d, s);
-    default: return launch_write_d<256>(lv, fmt, n, rows, slots, k, v, signs, inv_sqrt_d, s);
+    case 64: return launch_write_d<64>(lv, fmt, group, n, rows, slots, k, v, signs, inv_sqrt_d, s);
+    case 128: return launch_write_d<128>(lv, fmt, group, n, rows, slots, k, v, signs, inv_sqrt_d, s);
+    default: return launch_write_d<256>(lv, fmt, group, n, rows, slots, k, v, signs, inv_sqrt_d, s);
   }
 }
 

@@ -142,6 +142,7 @@ class Workload:
     hadamard_seed: int
     seed: int
     outlier_frac: float = 0.0
+    group: int = 32  # values per affine group of the packed formats (64: the five-bit K4/V4 layout)
 
     @property
     def B(self) -> int:
@@ -197,6 +198,12 @@ def qwen3_1_7b_k4v4(seed: int = 2, B: int = 16, L: int = 16384) -> Workload:
     rows, used = interleaved_monotone_rows(nblk, rng_for(seed, 12))
     return Workload("qwen3-1.7b-k4v4", 1, 16, 8, 128, FMT_K4V4, [L] * B, rows, used,
                     1 / math.sqrt(128), 0x5EED, seed, outlier_frac=0.01)
+
+
+def qwen3_1_7b_k4v4_g64(seed: int = 2, B: int = 16, L: int = 16384) -> Workload:
+    """The Qwen3-1.7B K4/V4 workload stored with groups of 64 values (one FP32 scale/offset
+    pair per 64: five bits per value, the packed-formats PR's 3.2x)."""
+    return dataclasses.replace(qwen3_1_7b_k4v4(seed, B, L), name="qwen3-1.7b-k4v4-g64", group=64)
 
 
 def llama_1b(fmt: int = FMT_K8V4, seed: int = 3, B: int = 64, lo: int = 512, hi: int = 8192) -> Workload:

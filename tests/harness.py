@@ -33,10 +33,10 @@ def make_pools(w: wl.Workload, layers=None, oracle_layers=None, max_slabs=None):
     """GPU pool (all w.n_layers) and oracle pool (only `oracle_layers`, mapped 0..)."""
     rows = max(w.rows_used, 1)
     ms = max_slabs or (rows + 31) // 32 + 4
-    g = pkv.Pool(w.n_layers, w.Hkv, w.D, FMT[w.fmt], hadamard_seed=w.hadamard_seed, max_slabs=ms)
+    g = pkv.Pool(w.n_layers, w.Hkv, w.D, FMT[w.fmt], hadamard_seed=w.hadamard_seed, max_slabs=ms, group_size=w.group)
     g.reserve_rows(rows)
     ol = list(range(w.n_layers)) if oracle_layers is None else list(oracle_layers)
-    o = oracle.OraclePool(len(ol), w.Hkv, w.D, w.fmt, seed=w.hadamard_seed) if ol else None
+    o = oracle.OraclePool(len(ol), w.Hkv, w.D, w.fmt, seed=w.hadamard_seed, group_size=w.group) if ol else None
     if o is not None:
         o.reserve_rows(rows)
     return g, o, ol

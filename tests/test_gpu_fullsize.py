@@ -52,9 +52,9 @@ def _full_case(w, sample, layers):
     """Full pool of `w`; host data for `sample` in `layers`; all layers decoded with one
     shared workspace in layer order (the benchmark's step); sample compared."""
     g = pkv.Pool(w.n_layers, w.Hkv, w.D, FMT[w.fmt], hadamard_seed=w.hadamard_seed,
-                 max_slabs=(w.rows_used + 31) // 32 + 8)
+                 max_slabs=(w.rows_used + 31) // 32 + 8, group_size=w.group)
     g.reserve_rows(w.rows_used)
-    o = oracle.OraclePool(len(layers), w.Hkv, w.D, w.fmt, seed=w.hadamard_seed)
+    o = oracle.OraclePool(len(layers), w.Hkv, w.D, w.fmt, seed=w.hadamard_seed, group_size=w.group)
     o.reserve_rows(w.rows_used)
     for i, layer in enumerate(layers):
         _write_seqs(w, g, o, layer, i, sample)
@@ -89,6 +89,12 @@ def test_qwen3_1_7b_k4v4_full_size_sampled():
     """16 x 16384 K4/V4 with outliers: three sequences compared."""
     w = wl.qwen3_1_7b_k4v4()
     _full_case(w, sample=[0, 7, w.B - 1], layers=[0])
+
+
+def test_qwen3_1_7b_k4v4_groups_of_64_full_size_sampled():
+    """16 x 16384 in the five-bit K4/V4 layout: two sequences compared."""
+    w = wl.qwen3_1_7b_k4v4_g64()
+    _full_case(w, sample=[0, w.B - 1], layers=[0])
 
 
 @pytest.mark.parametrize("fmt", [wl.FMT_K8V4, wl.FMT_K8V8])

@@ -81,6 +81,42 @@ def test_qwen3_1_7b_k4v4_small():
     _check(w, g, o, ol)
 
 
+def test_qwen3_1_7b_k4v4_groups_of_64_small():
+    """The five-bit K4/V4 layout (one FP32 scale/offset pair per 64 values)."""
+    w = wl.qwen3_1_7b_k4v4_g64(B=3, L=2000)
+    g, o, ol = make_pools(w)
+    fill(w, g, o, ol)
+    assert g.row_bytes == [64, 64, 16, 16]
+    _check(w, g, o, ol)
+
+
+@pytest.mark.parametrize("D,Hkv,G", [(128, 4, 1), (128, 8, 2), (128, 2, 8), (256, 4, 2), (256, 2, 4), (256, 8, 1)])
+def test_groups_of_64_geometry_sweep(D, Hkv, G):
+    """Groups of 64 at both head dims: 64- and 128-byte metadata rows, the two-warp
+    split at D = 256 with 4 kv heads, ragged lengths incl. 0 and 1, several CTA counts."""
+    lens = [0, 1, 33, 95, 400, 1500]
+    rows, used = wl.fragmented_rows([wl.nblocks(L) for L in lens], wl.rng_for(9, D, G))
+    w = wl.Workload(f"g64-{D}-{Hkv}-{G}", 1, Hkv * G, Hkv, D, wl.FMT_K4V4, lens, rows, used, 1 / math.sqrt(D),
+                    0x64, 23 + D + G, group=64)
+    g, o, ol = make_pools(w)
+    fill(w, g, o, ol)
+    _check(w, g, o, ol)
+    ref = o.decode_attention(0, w.q(0), w.block_table(), w.ctx(), w.scale)
+    for ctas in [3, 41, 0]:
+        g.decode_set_ctas(ctas)
+        a = _decode(w, g, 0)
+        compare(a, ref, f"{w.name} ctas={ctas}")
+        assert not a[0].any()
+    assert g.check_errors() == 0
+
+
+def test_groups_of_64_only_for_k4v4_at_head_dim_128_and_256():
+    for fmt, D in [("k8v4", 128), ("k8v8", 256), ("k4v4", 64)]:
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.Pool(1, 4, D, fmt, hadamard_seed=1, group_size=64)
+        assert e.value.status == pkv.PKV_ERR_INVALID
+
+
 @pytest.mark.parametrize("fmt", [wl.FMT_K8V4, wl.FMT_K8V8])
 def test_llama_1b_small(fmt):
     w = wl.llama_1b(fmt, B=6, lo=20, hi=700)
