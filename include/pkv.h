@@ -73,7 +73,10 @@ typedef struct {
   int32_t head_dim;      /* 64, 128 or 256                                      */
   int32_t block_size;    /* tokens per block; must be 32                        */
   int32_t slab_blocks;   /* blocks per slab (POOL_SLAB_BLOCKS); 1..4096, 32 is the default */
-  int32_t group_size;    /* values per affine group; must be 32 (ignored for bf16) */
+  int32_t group_size;    /* values per affine group (ignored for bf16): 32, or 64 for K4/V4 with
+                          * head_dim 128 or 256 (one FP32 scale/offset pair per 64 values: five
+                          * bits per value, 3.2x against bf16)
+                          *   [mlx-swift-lm #142, Summary: "five effective bits per value"] */
   int32_t format;        /* pkv_format                                          */
   int32_t max_slabs;     /* capacity of the slab pointer table (>= 1)           */
   uint64_t hadamard_seed;/* signs s_i = -1 iff top bit of splitmix64(seed + i)  */
