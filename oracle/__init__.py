@@ -81,6 +81,8 @@ def _load():
         lib.oracle_read_block.restype = i32
         lib.oracle_read_slab.argtypes = [P, i32, i32, i32, P]
         lib.oracle_read_slab.restype = i32
+        lib.oracle_prefill_attention.argtypes = [P, i32, i32, i32, i32, P, P, i32, P, dbl, P]
+        lib.oracle_prefill_attention.restype = i32
         lib.oracle_record_bytes.argtypes = [P]
         lib.oracle_record_bytes.restype = ctypes.c_size_t
         lib.oracle_export_blocks.argtypes = [P, i32, P, P]
@@ -232,6 +234,17 @@ class OraclePool:
     def read_block(self, layer: int, kind: int, row: int) -> np.ndarray:
         out = np.zeros(self.block_size * self.n_kv_heads * self.row_bytes[kind], np.uint8)
         _check(self._lib.oracle_read_block(self._h, layer, kind, row, _ptr(out)), "read_block")
+        return out
+
+    def prefill_attention(self, layer: int, q_bf16: np.ndarray, bt: np.ndarray, ctx, scale: float) -> np.ndarray:
+        """[B, n_q, Hq, D] float64 causal attention of the last n_q tokens of each sequence."""
+        q = np.ascontiguousarray(q_bf16, np.uint16)
+        B, n_q, Hq, D = q.shape
+        bt = np.ascontiguousarray(bt, np.int32)
+        ctx = np.ascontiguousarray(ctx, np.int32)
+        out = np.zeros((B, n_q, Hq, D), np.float64)
+        _check(self._lib.oracle_prefill_attention(self._h, layer, B, n_q, Hq, _ptr(q), _ptr(bt), bt.shape[1],
+                                                  _ptr(ctx), float(scale), _ptr(out)), "prefill_attention")
         return out
 
     @property

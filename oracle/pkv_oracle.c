@@ -535,6 +535,37 @@ int oracle_decode_attention(const oracle_pool* p, int layer, int B, int Hq, cons
   return OR_OK;
 }
 
+/* Causal chunked-prefill attention [ATTN, Proposed Solution: attend = update the
+ * storage, then attention over it; the survey's prefill-over-paged-slabs row].
+ * Sequence b holds ctx[b] tokens, the last n_q of which are the chunk's new tokens
+ * (already written); query i of the chunk (position ctx[b] - n_q + i) attends to
+ * tokens [0, ctx[b] - n_q + i] of its sequence, with the same softmax(q K^T scale) V
+ * as decode.  q: [B, n_q, Hq, D] bf16; out: [B, n_q, Hq, D] FP64.  A sequence with
+ * fewer than n_q tokens is an argument error. */
+int oracle_prefill_attention(const oracle_pool* p, int layer, int B, int n_q, int Hq, const uint16_t* q,
+                             const int32_t* bt, int max_blocks, const int32_t* ctx, double scale, double* out) {
+  if (layer < 0 || layer >= p->n_layers || B < 0 || n_q <= 0 || Hq <= 0 || Hq % p->n_kv_heads) return OR_ERR_ARG;
+  const int D = p->head_dim, G = Hq / p->n_kv_heads;
+  for (int b = 0; b < B; ++b) {
+    if (ctx[b] < n_q || ctx[b] > max_blocks * p->block_size) return OR_ERR_RANGE;
+    for (int j = 0; j < (ctx[b] + p->block_size - 1) / p->block_size; ++j)
+      if (!row_ok(p, bt[(size_t)b * max_blocks + j])) return OR_ERR_RANGE;
+  }
+  for (int b = 0; b < B; ++b)
+    for (int i = 0; i < n_q; ++i) {
+      const int visible = ctx[b] - n_q + i + 1;
+      for (int h = 0; h < Hq; ++h) {
+        double qd[512], qr[512];
+        const size_t row = (((size_t)b * n_q + i) * Hq + h) * D;
+        for (int d = 0; d < D; ++d) qd[d] = bf16_to_double(q[row + d]);
+        if (p->format == OR_FMT_BF16) memcpy(qr, qd, sizeof(double) * (size_t)D);
+        else oracle_rotate_q(qd, D, p->signs, qr);
+        attend_one(p, layer, qr, bt + (size_t)b * max_blocks, visible, h / G, scale, out + row);
+      }
+    }
+  return OR_OK;
+}
+
 /* Block record [SLAB, touch point 6 (serde block content, restore path); PACK,
  * Summary (complete checkpoints preserve packed bytes)]: every stored byte of one
  * block, for each layer in order and, within a layer, for each stored tensor in
