@@ -803,6 +803,150 @@ def run_gpu_blocks(args, rank, world, local):
     return res
 
 
+PREFILL = "prefill-qwen3-0.6b"
+PREFILL_NQ = 8  # new tokens per sequence in the chunk
+
+
+def prefill_oracle_sample(budget_s: float = 10.0, n_seqs: int = 2):
+    """The oracle's chunked prefill on one layer of the Qwen3-0.6B-shaped workload,
+    sequences 0..n_seqs-1, all host cores it may use."""
+    import oracle
+    oracle.build()
+    w = wl.qwen3_0_6b(n_layers=1)
+    o = oracle.OraclePool(1, w.Hkv, w.D, w.fmt, seed=w.hadamard_seed)
+    o.reserve_rows(w.rows_used)
+    for b in range(n_seqs):
+        k, v = w.kv(0, b)
+        r, sl = w.token_placement(b)
+        o.write_block(0, r, sl, k, v)
+    q = wl.bf16_normal(wl.rng_for(91), (n_seqs, PREFILL_NQ, w.Hq, w.D))
+    bt = w.block_table()[:n_seqs]
+    ctx = w.ctx()[:n_seqs]
+    times, t_end = [], time.perf_counter() + budget_s
+    while time.perf_counter() < t_end or len(times) < 2:
+        t0 = time.perf_counter()
+        o.prefill_attention(0, q, bt, ctx, w.scale)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    nbytes = int(ctx.sum()) * w.Hkv * token_head_bytes(w.fmt, w.D) + 2 * n_seqs * PREFILL_NQ * w.Hq * w.D * 2
+    return {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"1 of 28 layers, {n_seqs} of 8 sequences, chunk of {PREFILL_NQ} queries; median of {len(times)} runs",
+            "seconds_per_sample": t}
+
+
+def run_gpu_prefill(args, rank, world, local):
+    """Chunked prefill: the Qwen3-0.6B-shaped pool (28 layers, 8 x 4096 tokens), the last
+    PREFILL_NQ tokens of every sequence being the chunk; a step is one causal prefill
+    attention call per layer.  Bytes are the decode's (K/V of every visible token once,
+    q and out of every query, block-table entries, context lengths)."""
+    import torch
+    import paged_kv_cache_split_gb300 as pkv
+
+    torch.cuda.set_device(local)
+    w = wl.qwen3_0_6b(n_layers=args.layers) if args.layers else wl.qwen3_0_6b()
+    n_q = PREFILL_NQ
+    dev = torch.device("cuda", local)
+    pool = pkv.Pool(w.n_layers, w.Hkv, w.D, pkv.FORMAT_NAMES[w.fmt], hadamard_seed=w.hadamard_seed,
+                    max_slabs=(w.rows_used + 31) // 32 + 8)
+    pool.reserve_rows(w.rows_used)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000 + rank)
+    rows = np.concatenate([w.token_placement(b)[0] for b in range(w.B)])
+    slots = np.concatenate([w.token_placement(b)[1] for b in range(w.B)])
+    rows_d, slots_d = torch.from_numpy(rows).to(dev), torch.from_numpy(slots).to(dev)
+    for layer in range(w.n_layers):
+        k = torch.randn((rows.size, w.Hkv, w.D), generator=gen, device=dev).to(torch.bfloat16)
+        v = torch.randn((rows.size, w.Hkv, w.D), generator=gen, device=dev).to(torch.bfloat16)
+        pool.write_block(layer, rows_d, slots_d, k, v)
+        del k, v
+    q = torch.randn((w.n_layers, w.B, n_q, w.Hq, w.D), generator=gen, device=dev).to(torch.bfloat16)
+    bt = torch.from_numpy(w.block_table()).to(dev)
+    ctx = torch.from_numpy(w.ctx()).to(dev)
+    out = torch.empty_like(q)
+    ws = torch.zeros(pool.prefill_workspace_bytes(w.B, n_q, w.Hq, int(bt.shape[1])), dtype=torch.uint8, device=dev)
+    max_ctx = max(w.lens)
+
+    def step():
+        for layer in range(w.n_layers):
+            pool.paged_prefill_attention(layer, q[layer], bt, ctx, w.scale, max_ctx=max_ctx, out=out[layer], workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    q_h, out_h = q.cpu().pin_memory(), torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    q_e = torch.empty_like(q)
+
+    def e2e_step():
+        q_e.copy_(q_h, non_blocking=True)
+        for layer in range(w.n_layers):
+            pool.paged_prefill_attention(layer, q_e[layer], bt, ctx, w.scale, max_ctx=max_ctx, out=out[layer], workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+
+    sampler = ClockSampler(local)
+    with sampler:
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        ms_step = t0.elapsed_time(t1) / args.steps
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        ms_e2e = e0.elapsed_time(e1) / args.steps
+    if pool.check_errors():
+        raise SystemExit("device error word set during the timed region")
+    ms_step, ms_e2e = dist_max(ms_step, world), dist_max(ms_e2e, world)
+    kv = sum(w.lens) * w.Hkv * token_head_bytes(w.fmt, w.D)
+    qo = 2 * w.B * n_q * w.Hq * w.D * 2
+    bytes_layer = kv + qo + sum(wl.nblocks(L) for L in w.lens) * 4 + 4 * w.B
+    bytes_step = bytes_layer * w.n_layers
+    value = bytes_step * world / (ms_step * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    launch_us = ms_step * 1e3 / w.n_layers
+    res = {"metric": "chunked prefill attention: achieved HBM GB/s (K/V of the visible context once), query tokens/s",
+           "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f32", "data": "synthetic (seeded N(0,1) bf16 K/V and q; no model weights)",
+           "config": {"workload": f"chunked prefill: {describe(w)}; the last {n_q} tokens of each sequence are the chunk",
+                      "global_batch": w.B * world, "seq_len": max(w.lens), "layers": w.n_layers,
+                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                      "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB per step vs 129 MB L2)", "cuda_graph": True},
+           "query_tokens_per_s": round(w.B * n_q * w.n_layers * world / (ms_step * 1e-3), 1),
+           "roofline": {"bound": "hbm", "achieved": round(bytes_layer / (launch_us * 1e-6) / 1e9, 1), "peak": peak,
+                        "unit": "GB/s", "frac": round(bytes_layer / (launch_us * 1e-6) / 1e9 / peak, 4), "traffic": None,
+                        "per_launch_bytes": bytes_layer, "avg_launch_us": round(launch_us, 3), "peak_source": peak_src,
+                        "kernel": "expansion + decode attention + combine kernels per layer"},
+           "e2e": {"value": round(bytes_step * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+                   "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": int(q.numel() * 2),
+                   "d2h_bytes_per_step": int(out.numel() * 2)},
+           "gpu_launches": 3 * w.n_layers * args.steps, "clocks": sampler.summary()}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -837,6 +981,32 @@ def main():
                "e2e": {"value": round(cb["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                        "d2h_bytes_per_step": 0}}
         print(json.dumps(res), flush=True)
+        return
+
+    if args.workload == PREFILL:
+        if args.impl == "reference":
+            if rank == 0:
+                cb = prefill_oracle_sample(budget_s=max(2.0, 0.05 * (args.warmup + args.steps)))
+                print(json.dumps({"impl": "reference", "metric": "chunked prefill attention: achieved HBM GB/s "
+                                  "(K/V of the visible context once), query tokens/s", "value": round(cb["value"], 4),
+                                  "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                                  "ms_per_step": round(cb["seconds_per_sample"] * 1e3, 3), "higher_is_better": True,
+                                  "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                                  "data": "synthetic (seeded N(0,1) bf16 K/V and q; no model weights)",
+                                  "config": {"workload": "chunked prefill (oracle sample)", "parallelism": "host cores"},
+                                  "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                                  "e2e": {"value": round(cb["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                          "d2h_bytes_per_step": 0}}), flush=True)
+            return
+        res = run_gpu_prefill(args, rank, world, local)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                cb = prefill_oracle_sample(budget_s=10.0)
+                res["cpu_baseline"] = {k: (round(v, 5) if isinstance(v, float) else v) for k, v in cb.items()}
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
 
     if args.workload == BLOCKS:

@@ -237,6 +237,31 @@ pkv_status pkv_slab_address(const pkv_pool* pool, int layer, int kind, int slab,
  *   [mlx-swift-lm #142, Summary: reject incompatible storage identities] */
 pkv_status pkv_pool_check_identity(const pkv_pool* pool, const pkv_pool_config* cfg);
 
+/* Workspace bytes for pkv_paged_prefill_attention with B sequences, n_q new tokens
+ * each, Hq query heads and block tables of max_blocks entries.  B * n_q <= 4096.
+ * Synchronous, host only. */
+pkv_status pkv_prefill_workspace_bytes(const pkv_pool* pool, int B, int n_q, int Hq, int max_blocks, size_t* bytes);
+
+/* Causal chunked-prefill attention over the pool: sequence b holds ctx_lens[b]
+ * tokens (its chunk of n_q new tokens already written with pkv_write_block, as the
+ * last n_q), and query i of the chunk attends to tokens [0, ctx_lens[b] - n_q + i].
+ * q_bf16: [B, n_q, Hq, head_dim] bf16, un-rotated (packed formats rotate q
+ * internally); out_bf16: [B, n_q, Hq, head_dim]; block_table, ctx_lens and the GQA
+ * mapping as for pkv_paged_decode_attention.  The workspace (caller-owned, 256-byte
+ * aligned, pkv_prefill_workspace_bytes) holds each query's view of its sequence
+ * (the same block-table row, a causal context length) and the split-K partials;
+ * each query then runs the decode kernels, so the chunk's K/V blocks are read once
+ * from HBM and again from L2 by the chunk's later queries.  A sequence with fewer
+ * than n_q tokens sets the device error word (bit 2) and its rows are zero.
+ * Errors as for pkv_paged_decode_attention; PKV_ERR_INVALID when B * n_q > 4096.
+ * Asynchronous.
+ *   [mlxcel #2171, Proposed Solution: attend = update the storage, then attention;
+ *    mlx-swift-lm #142, Summary: direct attention consumes packed pages] */
+pkv_status pkv_paged_prefill_attention(pkv_pool* pool, int layer, int B, int n_q, int Hq, const void* q_bf16,
+                                       const int32_t* block_table, int max_blocks, const int32_t* ctx_lens,
+                                       int max_ctx, float scale, void* out_bf16, void* workspace, size_t ws_bytes,
+                                       void* stream);
+
 /* The pool's configuration (its storage identity plus n_layers and max_slabs), for
  * a checkpoint header.  Synchronous, host only. */
 pkv_status pkv_pool_get_config(const pkv_pool* pool, pkv_pool_config* out);

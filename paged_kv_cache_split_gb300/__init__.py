@@ -87,6 +87,8 @@ SIGNATURES = {
     "pkv_pool_check_identity": ([_P, ctypes.POINTER(PoolConfig)], _I),
     "pkv_pool_check_errors": ([_P, _P, ctypes.POINTER(ctypes.c_int32)], _I),
     "pkv_pool_get_config": ([_P, ctypes.POINTER(PoolConfig)], _I),
+    "pkv_prefill_workspace_bytes": ([_P, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
+    "pkv_paged_prefill_attention": ([_P, _I, _I, _I, _I, _P, _P, _I, _P, _I, _F, _P, _P, _SZ, _P], _I),
     "pkv_block_record_bytes": ([_P, ctypes.POINTER(_SZ)], _I),
     "pkv_export_blocks": ([_P, _I, _P, _P, _SZ, _P], _I),
     "pkv_import_blocks": ([_P, ctypes.POINTER(PoolConfig), _I, _P, _P, _SZ, _P], _I),
@@ -323,6 +325,34 @@ class Pool:
             int(block_table.shape[1]), _dev(ctx_lens, torch.int32, "ctx_lens", (B,)), int(max_ctx), float(scale),
             _dev(out, torch.bfloat16, "out", (B, Hq, D)), workspace.data_ptr(), int(workspace.numel()),
             _stream(stream)), "paged_decode_attention")
+        return out
+
+    def prefill_workspace_bytes(self, B: int, n_q: int, Hq: int, max_blocks: int) -> int:
+        n = _SZ()
+        _check(self._lib.pkv_prefill_workspace_bytes(self._h, B, n_q, Hq, max_blocks, ctypes.byref(n)),
+               "prefill_workspace_bytes")
+        return int(n.value)
+
+    def paged_prefill_attention(self, layer: int, q, block_table, ctx_lens, scale: float, max_ctx: int = 0,
+                                out=None, workspace=None, stream=None):
+        """Causal attention of the last n_q tokens of each sequence: q [B, n_q, Hq, D] bf16."""
+        torch = _torch()
+        B, n_q, Hq, D = q.shape
+        if D != self.head_dim:
+            raise ValueError(f"q head_dim {D} != pool head_dim {self.head_dim}")
+        if block_table.dim() != 2 or block_table.shape[0] != B:
+            raise ValueError("block_table must be [B, max_blocks]")
+        if out is None:
+            out = torch.empty_like(q)
+        mb = int(block_table.shape[1])
+        if workspace is None:
+            n = self.prefill_workspace_bytes(B, n_q, Hq, mb)
+            workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+        _check(self._lib.pkv_paged_prefill_attention(
+            self._h, layer, B, n_q, Hq, _dev(q, torch.bfloat16, "q"), _dev(block_table, torch.int32, "block_table"), mb,
+            _dev(ctx_lens, torch.int32, "ctx_lens", (B,)), int(max_ctx), float(scale),
+            _dev(out, torch.bfloat16, "out", (B, n_q, Hq, D)), workspace.data_ptr(), int(workspace.numel()),
+            _stream(stream)), "paged_prefill_attention")
         return out
 
     def paged_decode_attention_noalloc(self, layer: int, q, block_table, ctx_lens, scale: float,

@@ -561,6 +561,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams P, int 
   }
 }
 
+// Opt `kern` in to the largest dynamic shared memory a block may use (227 KB).  The
+// attribute belongs to the current device, so it is set once per device; `done` is
+// the caller's record for this kernel (bit d: set on device d).
+template <typename Kern>
+inline cudaError_t allow_max_dynamic_smem(Kern kern, unsigned long long& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && ((done >> dev) & 1ull)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  if (e == cudaSuccess && dev < 64) done |= 1ull << dev;
+  return e;
+}
+
 // Launch `kern` with programmatic stream serialization enabled (see above).
 template <typename Kern>
 inline cudaError_t launch_with_pdl(Kern kern, int grid, int threads, size_t smem, cudaStream_t stream,

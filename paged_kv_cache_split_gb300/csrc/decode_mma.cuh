@@ -297,11 +297,10 @@ cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
   P.NS = a.n_stages;
   P.stage_bytes = 2 * P.T * (a.lv.hkv * D * 2) + ((a.Hq * D * 2 + 1023) & ~1023);
   auto kern = decode_bf16_mma_kernel<D, G>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  {
+    static unsigned long long smem_done = 0;  // this kernel (one per template instantiation)
+    cudaError_t e = allow_max_dynamic_smem(kern, smem_done);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   cudaError_t e = launch_with_pdl(kern, a.grid, (a.lv.hkv + 1) * 32, a.smem_bytes, a.stream, P);
   if (e != cudaSuccess) return e;

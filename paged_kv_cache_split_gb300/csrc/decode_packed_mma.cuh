@@ -765,11 +765,10 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   const int hkv = a.lv.hkv;
   P.stage_bytes = packed_stage_bytes(P.T, hkv * Tr::KB, hkv * Tr::VB, hkv * Tr::MB, a.Hq * D * 2);
   auto kern = decode_packed_mma_kernel<FMT, D, G, W128, RS, DS, GS>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  {
+    static unsigned long long smem_done = 0;  // this kernel (one per template instantiation)
+    cudaError_t e = allow_max_dynamic_smem(kern, smem_done);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const int ncons = DS ? 2 * hkv : hkv;
   const int threads = RS ? 128 * (((ncons + 3) >> 2) + 1) : (ncons + kProducerWarps) * 32;

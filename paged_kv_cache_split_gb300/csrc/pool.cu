@@ -57,6 +57,8 @@ static thread_local std::string g_last_error;
 
 namespace pkv {
 // Defined in write.cu.
+cudaError_t launch_expand_prefill(int B, int n_q, int max_blocks, const int32_t* bt, const int32_t* ctx,
+                                  int32_t* bt_out, int32_t* ctx_out, int32_t* err, cudaStream_t s);
 cudaError_t launch_serde_blocks(const uint8_t* const* table, int n_layers, int n_kinds, const int64_t* block_bytes,
                                int slab_blocks, int64_t rows_capacity, int n, const int32_t* rows, uint8_t* buf,
                                int64_t rec_bytes, int to_pool, int32_t* err, cudaStream_t s);
@@ -581,6 +583,54 @@ pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, con
   if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attention launch");
   p->last_stream = (cudaStream_t)stream;
   return PKV_OK;
+}
+
+// Chunked prefill: the expanded block table and context lengths, then the decode
+// workspace of B * n_q virtual sequences.
+static void prefill_layout(const pkv_pool* p, int B, int n_q, int Hq, int max_blocks, size_t* bt_off, size_t* ctx_off,
+                           size_t* dec_off, size_t* total) {
+  const size_t nv = (size_t)B * (size_t)n_q;
+  *bt_off = 0;
+  *ctx_off = align_up(nv * (size_t)(max_blocks > 0 ? max_blocks : 1) * sizeof(int32_t), 256);
+  *dec_off = *ctx_off + align_up(nv * sizeof(int32_t), 256);
+  *total = *dec_off + workspace_bytes(p, (int)nv, Hq);
+}
+
+pkv_status pkv_prefill_workspace_bytes(const pkv_pool* p, int B, int n_q, int Hq, int max_blocks, size_t* bytes) {
+  if (!p || !bytes || B < 0 || n_q < 1 || Hq < 1 || max_blocks < 0 || (int64_t)B * n_q > 4096)
+    return PKV_ERR_INVALID;
+  size_t a, b, c;
+  prefill_layout(p, B, n_q, Hq, max_blocks, &a, &b, &c, bytes);
+  return PKV_OK;
+}
+
+pkv_status pkv_paged_prefill_attention(pkv_pool* p, int layer, int B, int n_q, int Hq, const void* q,
+                                       const int32_t* bt, int max_blocks, const int32_t* ctx, int max_ctx,
+                                       float scale, void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!p || layer < 0 || layer >= p->cfg.n_layers || B < 0 || n_q < 1 || Hq < 1 || max_blocks < 0 ||
+      (int64_t)B * n_q > 4096)
+    return PKV_ERR_INVALID;
+  if (B == 0) return PKV_OK;
+  if (Hq % p->cfg.n_kv_heads) return PKV_ERR_INVALID;
+  const int G = Hq / p->cfg.n_kv_heads;
+  if (!(G == 1 || G == 2 || G == 4 || G == 8)) return PKV_ERR_INVALID;
+  if (!q || !bt || !ctx || !out || !ws || !std::isfinite(scale)) return PKV_ERR_INVALID;
+  if (((uintptr_t)ws & 255u) != 0 || ((uintptr_t)q & 15u) != 0 || ((uintptr_t)out & 15u) != 0)
+    return PKV_ERR_INVALID;
+  size_t bt_off, ctx_off, dec_off, total;
+  prefill_layout(p, B, n_q, Hq, max_blocks, &bt_off, &ctx_off, &dec_off, &total);
+  if (ws_bytes < total) return PKV_ERR_INVALID;
+  DecodePlan plan;
+  if (!plan_decode(p->cfg.format, p->cfg.head_dim, G, p->cfg.n_kv_heads, B * n_q, p->cfg.group_size, &plan) ||
+      plan.smem_bytes > p->smem_optin)
+    return PKV_ERR_INVALID;
+  int32_t* bt2 = (int32_t*)((uint8_t*)ws + bt_off);
+  int32_t* ctx2 = (int32_t*)((uint8_t*)ws + ctx_off);
+  PKV_CUDA(launch_expand_prefill(B, n_q, max_blocks, bt, ctx, bt2, ctx2, p->err_dev, (cudaStream_t)stream),
+           "prefill expansion launch");
+  // q [B, n_q, Hq, D] and out [B, n_q, Hq, D] are [B * n_q, Hq, D]: decode of the virtual sequences.
+  return pkv_paged_decode_attention(p, layer, B * n_q, Hq, q, bt2, max_blocks, ctx2, max_ctx, scale, out,
+                                    (uint8_t*)ws + dec_off, ws_bytes - dec_off, stream);
 }
 
 pkv_status pkv_pool_stats(const pkv_pool* p, pkv_stats* out) {
