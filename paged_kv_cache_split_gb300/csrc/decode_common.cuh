@@ -26,6 +26,7 @@ struct DecodeParams {
   int T;            // tokens per unit / stage
   int NS;           // stages in the ring
   int stage_bytes;  // bytes of one stage
+  int kv_reuse;     // 1: K/V are read again soon (chunked prefill): normal L2 priority, else evict-first
 };
 
 constexpr int kMaxConsumerWarps = 8;

@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   // a zero probability.  A unit that starts a CTA's segment of a sequence also
   // brings that sequence's q.
   auto issue = [&](uint64_t* bar, uint8_t* st, const uint8_t* map, int y0, int ok, const uint8_t* qsrc) {
-    const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once
+    const uint64_t kv_policy = P.kv_reuse ? l2_policy_evict_normal() : l2_policy_evict_first();
     mbar_arrive_expect_tx(bar, (ok ? (uint32_t)(2 * T * ROW) : 0u) + (qsrc ? (uint32_t)QB : 0u));
     if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, bar);
     if (ok) {
@@ -293,6 +293,7 @@ cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
   P.out = a.out;
   P.counters = a.counters;
   P.partials = a.partials;
+  P.kv_reuse = a.kv_reuse;
   P.T = a.tokens_per_stage;
   P.NS = a.n_stages;
   P.stage_bytes = 2 * P.T * (a.lv.hkv * D * 2) + ((a.Hq * D * 2 + 1023) & ~1023);

@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   // Producers: one 3-D tensor copy per 16 tokens and stored tensor, plus q when the
   // unit starts a CTA's segment of a sequence, all counted on barrier `bar`.
   auto issue = [&](uint64_t* bar, uint8_t* st, const uint8_t* map, int y0, int ok, const uint8_t* qsrc) {
-    const uint64_t kv_policy = l2_policy_evict_first();
+    const uint64_t kv_policy = P.kv_reuse ? l2_policy_evict_normal() : l2_policy_evict_first();
     mbar_arrive_expect_tx(bar, (ok ? (uint32_t)(T * (KR + VR + 2 * MR)) : 0u) + (qsrc ? (uint32_t)QB : 0u));
     if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, bar);
     if (ok) {
@@ -760,6 +760,7 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   P.out = a.out;
   P.counters = a.counters;
   P.partials = a.partials;
+  P.kv_reuse = a.kv_reuse;
   P.T = a.tokens_per_stage;
   P.NS = a.n_stages;
   const int hkv = a.lv.hkv;

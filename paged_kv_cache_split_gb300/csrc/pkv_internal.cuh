@@ -196,6 +196,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return p;
 }
 
+// L2 policy: lines fetched under it are kept like ordinary loads.
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -239,6 +246,7 @@ struct DecodeArgs {
   cudaStream_t stream;
   int dim_split;        // see DecodePlan
   int group;            // values per affine group of the packed formats: 32 or 64 (K4/V4)
+  int kv_reuse;         // 1: K/V blocks are read again soon (chunked prefill): keep them in L2
 };
 
 // Returns cudaSuccess or the launch error.  Defined per format in decode_*.cu.

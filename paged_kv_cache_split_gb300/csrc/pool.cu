@@ -529,10 +529,9 @@ pkv_status pkv_decode_set_ctas(pkv_pool* p, int n_ctas) {
   return PKV_OK;
 }
 
-pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, const void* q,
-                                      const int32_t* bt, int max_blocks, const int32_t* ctx, int max_ctx,
-                                      float scale, void* out, void* ws, size_t ws_bytes, void* stream) {
-  (void)max_ctx;
+static pkv_status decode_impl(pkv_pool* p, int layer, int B, int Hq, const void* q, const int32_t* bt,
+                              int max_blocks, const int32_t* ctx, float scale, void* out, void* ws, size_t ws_bytes,
+                              void* stream, int kv_reuse) {
   if (!p || layer < 0 || layer >= p->cfg.n_layers || B < 0 || Hq < 1 || max_blocks < 0)
     return PKV_ERR_INVALID;
   if (B == 0) return PKV_OK;
@@ -571,6 +570,7 @@ pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, con
   a.n_stages = plan.n_stages;
   a.dim_split = plan.dim_split;
   a.group = p->cfg.group_size;
+  a.kv_reuse = kv_reuse;
   a.smem_bytes = plan.smem_bytes;
   a.stream = (cudaStream_t)stream;
   cudaError_t e;
@@ -583,6 +583,13 @@ pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, con
   if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attention launch");
   p->last_stream = (cudaStream_t)stream;
   return PKV_OK;
+}
+
+pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, const void* q,
+                                      const int32_t* bt, int max_blocks, const int32_t* ctx, int max_ctx,
+                                      float scale, void* out, void* ws, size_t ws_bytes, void* stream) {
+  (void)max_ctx;
+  return decode_impl(p, layer, B, Hq, q, bt, max_blocks, ctx, scale, out, ws, ws_bytes, stream, 0);
 }
 
 // Chunked prefill: the expanded block table and context lengths, then the decode
@@ -629,8 +636,10 @@ pkv_status pkv_paged_prefill_attention(pkv_pool* p, int layer, int B, int n_q, i
   PKV_CUDA(launch_expand_prefill(B, n_q, max_blocks, bt, ctx, bt2, ctx2, p->err_dev, (cudaStream_t)stream),
            "prefill expansion launch");
   // q [B, n_q, Hq, D] and out [B, n_q, Hq, D] are [B * n_q, Hq, D]: decode of the virtual sequences.
-  return pkv_paged_decode_attention(p, layer, B * n_q, Hq, q, bt2, max_blocks, ctx2, max_ctx, scale, out,
-                                    (uint8_t*)ws + dec_off, ws_bytes - dec_off, stream);
+  // K/V blocks of a sequence are read by all n_q of its queries: normal L2 priority.
+  (void)max_ctx;
+  return decode_impl(p, layer, B * n_q, Hq, q, bt2, max_blocks, ctx2, scale, out, (uint8_t*)ws + dec_off,
+                     ws_bytes - dec_off, stream, 1);
 }
 
 pkv_status pkv_pool_stats(const pkv_pool* p, pkv_stats* out) {
