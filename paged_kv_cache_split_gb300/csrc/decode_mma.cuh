@@ -56,9 +56,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int D, int G>
+// NQ > 1 (chunked prefill): a virtual sequence carries NQ consecutive queries of one
+// sequence's chunk, and the S tile's rows are (query, head) pairs, query-major: row
+// r is query r / G and head r % G of the kv head, so up to 8 rows serve NQ queries
+// at the cost of one decode.  Query j of NQ sees the sequence's first
+// L - (NQ - 1 - j) tokens (causal); P.Hq counts the NQ queries' heads.
+template <int D, int G, int NQ = 1>
 __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const DecodeParams P) {
   static_assert(G >= 1 && G <= 8 && D % 16 == 0, "geometry");
+  static_assert(NQ >= 1 && NQ * G <= 8, "query rows of one kv head fit the tile's first 8 rows");
+  constexpr int R = NQ * G;  // rows in use
   extern __shared__ __align__(128) uint8_t smem[];
   const int hkv = P.lv.hkv;
   const int NC = hkv;
@@ -118,6 +125,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   // ------------------------------ consumers ---------------------------------
   const int h = warp;
   const int g = lane >> 2, t = lane & 3;
+  // q head (within the virtual sequence's P.Hq) of row r
+  auto qhead = [&](int r) -> size_t {
+    if constexpr (NQ == 1) return (size_t)h * G + r;
+    else return (size_t)(r / G) * (size_t)(P.Hq / NQ) + (size_t)h * G + (size_t)(r % G);
+  };
   // ldmatrix row owned by this lane: matrix mi = lane/8, row ri = lane%8 covers
   // token 8*(mi/2)+ri and dims 8*(mi%2) .. +7 of the current 16-token x 16-dim tile.
   const int ld_tok = 8 * ((lane >> 3) >> 1) + (lane & 7);
@@ -153,17 +165,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
 
     const int32_t tok0 = (u - UP[b]) * T;
     const int nv = min(T, LS[b] - tok0);
+    // tokens of this unit visible to the lane's row (its query's causal limit)
+    const int nvr = NQ == 1 ? nv : min(T, LS[b] - tok0 - (NQ - 1 - (g < R ? g / G : NQ - 1)));
     if (!dead && !mbar_wait_bounded(&full[s], phase, err)) dead = true;
     dead = __shfl_sync(0xffffffffu, dead, 0);
     if (!dead && seg_start) {
       // A fragments of Q (rows = query heads of kv head h; rows >= G are zero),
       // from the copy of q that arrived with this stage.
       const uint32_t* qrow = reinterpret_cast<const uint32_t*>(stages + (size_t)s * P.stage_bytes + offQ +
-                                                               ((size_t)h * G + (g < G ? g : 0)) * D * 2);
+                                                               qhead(g < R ? g : 0) * D * 2);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        qa[kk][0] = g < G ? qrow[(16 * kk + 2 * t) / 2] : 0u;
-        qa[kk][1] = g < G ? qrow[(16 * kk + 2 * t + 8) / 2] : 0u;
+        qa[kk][0] = g < R ? qrow[(16 * kk + 2 * t) / 2] : 0u;
+        qa[kk][1] = g < R ? qrow[(16 * kk + 2 * t + 8) / 2] : 0u;
       }
     }
     if (!dead) {
@@ -184,10 +198,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
         }
         // ---- online softmax for head g (row g), tokens 2t, 2t+1, 8+2t, 9+2t ----
         const int tb = kc * 16 + 2 * t;
-        float x0 = tb < nv ? sacc[0][0] * P.scale_log2 : -INFINITY;
-        float x1 = tb + 1 < nv ? sacc[0][1] * P.scale_log2 : -INFINITY;
-        float x2 = tb + 8 < nv ? sacc[1][0] * P.scale_log2 : -INFINITY;
-        float x3 = tb + 9 < nv ? sacc[1][1] * P.scale_log2 : -INFINITY;
+        float x0 = tb < nvr ? sacc[0][0] * P.scale_log2 : -INFINITY;
+        float x1 = tb + 1 < nvr ? sacc[0][1] * P.scale_log2 : -INFINITY;
+        float x2 = tb + 8 < nvr ? sacc[1][0] * P.scale_log2 : -INFINITY;
+        float x3 = tb + 9 < nvr ? sacc[1][1] * P.scale_log2 : -INFINITY;
         float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -208,8 +222,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
             o[mt][3] *= ao;
           }
         }
-        const float p0 = exp2f(x0 - m_run), p1 = exp2f(x1 - m_run);
-        const float p2 = exp2f(x2 - m_run), p3 = exp2f(x3 - m_run);
+        float p0 = exp2f(x0 - m_run), p1 = exp2f(x1 - m_run);
+        float p2 = exp2f(x2 - m_run), p3 = exp2f(x3 - m_run);
+        if constexpr (NQ > 1) {
+          // a row with no visible token yet in this segment keeps m_run = -inf
+          if (m_run == -INFINITY) p0 = p1 = p2 = p3 = 0.f;
+        }
         l_run += (p0 + p1) + (p2 + p3);
         const uint32_t pb0 = pack_bf16x2(p0, p1), pb1 = pack_bf16x2(p2, p3);
         // ---- O^T += V^T P^T over these 16 tokens ----
@@ -234,23 +252,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
       const int32_t c_lo = UP[b] / C, c_hi = (UP[b + 1] - 1) / C;
       if (c_lo == c_hi) {
         const float ie = 1.0f / le, io = 1.0f / lo;
-        uint16_t* oe = P.out + ((size_t)b * P.Hq + (size_t)h * G + he) * D;
-        uint16_t* oo = P.out + ((size_t)b * P.Hq + (size_t)h * G + ho) * D;
+        uint16_t* oe = P.out + ((size_t)b * P.Hq + qhead(he < R ? he : 0)) * D;
+        uint16_t* oo = P.out + ((size_t)b * P.Hq + qhead(ho < R ? ho : 0)) * D;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-          if (he < G) {
+          if (he < R) {
             oe[16 * mt + g] = f2bf(o[mt][0] * ie);
             oe[16 * mt + g + 8] = f2bf(o[mt][2] * ie);
           }
-          if (ho < G) {
+          if (ho < R) {
             oo[16 * mt + g] = f2bf(o[mt][1] * io);
             oo[16 * mt + g + 8] = f2bf(o[mt][3] * io);
           }
         }
       } else {
-        float* pe = partial_ptr(P, D, (size_t)blockIdx.x, b, (size_t)h * G + he);
-        float* po = partial_ptr(P, D, (size_t)blockIdx.x, b, (size_t)h * G + ho);
-        if (he < G) {
+        float* pe = partial_ptr(P, D, (size_t)blockIdx.x, b, qhead(he < R ? he : 0));
+        float* po = partial_ptr(P, D, (size_t)blockIdx.x, b, qhead(ho < R ? ho : 0));
+        if (he < R) {
           if (g == 0) {
             pe[0] = me;
             pe[1] = le;
@@ -261,7 +279,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
             pe[kPartialHeader + 16 * mt + g + 8] = o[mt][2];
           }
         }
-        if (ho < G) {
+        if (ho < R) {
           if (g == 0) {
             po[0] = mo;
             po[1] = lo;
@@ -277,7 +295,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   }
 }
 
-template <int D, int G>
+template <int D, int G, int NQ = 1>
 cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
   DecodeParams P;
   P.lv = a.lv;
@@ -297,7 +315,7 @@ cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
   P.T = a.tokens_per_stage;
   P.NS = a.n_stages;
   P.stage_bytes = 2 * P.T * (a.lv.hkv * D * 2) + ((a.Hq * D * 2 + 1023) & ~1023);
-  auto kern = decode_bf16_mma_kernel<D, G>;
+  auto kern = decode_bf16_mma_kernel<D, G, NQ>;
   {
     static unsigned long long smem_done = 0;  // this kernel (one per template instantiation)
     cudaError_t e = allow_max_dynamic_smem(kern, smem_done);
@@ -308,14 +326,5 @@ cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
   return launch_combine<D>(P, a.grid, a.stream);
 }
 
-inline cudaError_t launch_decode_bf16_mma(const DecodeArgs& a) {
-#define PKV_CASE(DD, GG) \
-  if (a.D == DD && a.G == GG) return launch_decode_bf16_mma_t<DD, GG>(a);
-  PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
-  PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
-  PKV_CASE(256, 1) PKV_CASE(256, 2) PKV_CASE(256, 4) PKV_CASE(256, 8)
-#undef PKV_CASE
-  return cudaErrorInvalidValue;
-}
 
 }  // namespace pkv

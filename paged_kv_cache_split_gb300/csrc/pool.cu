@@ -57,7 +57,7 @@ static thread_local std::string g_last_error;
 
 namespace pkv {
 // Defined in write.cu.
-cudaError_t launch_expand_prefill(int B, int n_q, int max_blocks, const int32_t* bt, const int32_t* ctx,
+cudaError_t launch_expand_prefill(int B, int n_q, int nq, int max_blocks, const int32_t* bt, const int32_t* ctx,
                                   int32_t* bt_out, int32_t* ctx_out, int32_t* err, cudaStream_t s);
 cudaError_t launch_serde_blocks(const uint8_t* const* table, int n_layers, int n_kinds, const int64_t* block_bytes,
                                int slab_blocks, int64_t rows_capacity, int n, const int32_t* rows, uint8_t* buf,
@@ -531,7 +531,7 @@ pkv_status pkv_decode_set_ctas(pkv_pool* p, int n_ctas) {
 
 static pkv_status decode_impl(pkv_pool* p, int layer, int B, int Hq, const void* q, const int32_t* bt,
                               int max_blocks, const int32_t* ctx, float scale, void* out, void* ws, size_t ws_bytes,
-                              void* stream, int kv_reuse) {
+                              void* stream, int kv_reuse, int nq) {
   if (!p || layer < 0 || layer >= p->cfg.n_layers || B < 0 || Hq < 1 || max_blocks < 0)
     return PKV_ERR_INVALID;
   if (B == 0) return PKV_OK;
@@ -571,6 +571,7 @@ static pkv_status decode_impl(pkv_pool* p, int layer, int B, int Hq, const void*
   a.dim_split = plan.dim_split;
   a.group = p->cfg.group_size;
   a.kv_reuse = kv_reuse;
+  a.nq = nq;
   a.smem_bytes = plan.smem_bytes;
   a.stream = (cudaStream_t)stream;
   cudaError_t e;
@@ -589,18 +590,30 @@ pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, con
                                       const int32_t* bt, int max_blocks, const int32_t* ctx, int max_ctx,
                                       float scale, void* out, void* ws, size_t ws_bytes, void* stream) {
   (void)max_ctx;
-  return decode_impl(p, layer, B, Hq, q, bt, max_blocks, ctx, scale, out, ws, ws_bytes, stream, 0);
+  return decode_impl(p, layer, B, Hq, q, bt, max_blocks, ctx, scale, out, ws, ws_bytes, stream, 0, 1);
 }
 
-// Chunked prefill: the expanded block table and context lengths, then the decode
-// workspace of B * n_q virtual sequences.
+// Chunked prefill: queries per virtual sequence.  The bf16 kernel serves nq
+// queries of one sequence per tile when nq x (query heads per kv head) <= 8 and nq
+// divides the chunk; the packed kernels take one query per virtual sequence.
+static int prefill_nq(const pkv_pool* p, int n_q, int Hq) {
+  if (p->cfg.format != PKV_FMT_BF16 || Hq % p->cfg.n_kv_heads) return 1;
+  const int G = Hq / p->cfg.n_kv_heads;
+  for (int nq = 8; nq > 1; nq >>= 1)
+    if (nq * G <= 8 && n_q % nq == 0) return nq;
+  return 1;
+}
+
+// The expanded block table and context lengths, then the decode workspace of the
+// B * n_q / nq virtual sequences (nq queries' heads each).
 static void prefill_layout(const pkv_pool* p, int B, int n_q, int Hq, int max_blocks, size_t* bt_off, size_t* ctx_off,
                            size_t* dec_off, size_t* total) {
-  const size_t nv = (size_t)B * (size_t)n_q;
+  const int nq = prefill_nq(p, n_q, Hq);
+  const size_t nv = (size_t)B * (size_t)(n_q / nq);
   *bt_off = 0;
   *ctx_off = align_up(nv * (size_t)(max_blocks > 0 ? max_blocks : 1) * sizeof(int32_t), 256);
   *dec_off = *ctx_off + align_up(nv * sizeof(int32_t), 256);
-  *total = *dec_off + workspace_bytes(p, (int)nv, Hq);
+  *total = *dec_off + workspace_bytes(p, (int)nv, Hq * nq);
 }
 
 pkv_status pkv_prefill_workspace_bytes(const pkv_pool* p, int B, int n_q, int Hq, int max_blocks, size_t* bytes) {
@@ -614,6 +627,7 @@ pkv_status pkv_prefill_workspace_bytes(const pkv_pool* p, int B, int n_q, int Hq
 pkv_status pkv_paged_prefill_attention(pkv_pool* p, int layer, int B, int n_q, int Hq, const void* q,
                                        const int32_t* bt, int max_blocks, const int32_t* ctx, int max_ctx,
                                        float scale, void* out, void* ws, size_t ws_bytes, void* stream) {
+  (void)max_ctx;
   if (!p || layer < 0 || layer >= p->cfg.n_layers || B < 0 || n_q < 1 || Hq < 1 || max_blocks < 0 ||
       (int64_t)B * n_q > 4096)
     return PKV_ERR_INVALID;
@@ -624,22 +638,24 @@ pkv_status pkv_paged_prefill_attention(pkv_pool* p, int layer, int B, int n_q, i
   if (!q || !bt || !ctx || !out || !ws || !std::isfinite(scale)) return PKV_ERR_INVALID;
   if (((uintptr_t)ws & 255u) != 0 || ((uintptr_t)q & 15u) != 0 || ((uintptr_t)out & 15u) != 0)
     return PKV_ERR_INVALID;
+  const int nq = prefill_nq(p, n_q, Hq);
+  const int Bv = B * (n_q / nq);
   size_t bt_off, ctx_off, dec_off, total;
   prefill_layout(p, B, n_q, Hq, max_blocks, &bt_off, &ctx_off, &dec_off, &total);
   if (ws_bytes < total) return PKV_ERR_INVALID;
   DecodePlan plan;
-  if (!plan_decode(p->cfg.format, p->cfg.head_dim, G, p->cfg.n_kv_heads, B * n_q, p->cfg.group_size, &plan) ||
+  if (!plan_decode(p->cfg.format, p->cfg.head_dim, G * nq, p->cfg.n_kv_heads, Bv, p->cfg.group_size, &plan) ||
       plan.smem_bytes > p->smem_optin)
     return PKV_ERR_INVALID;
   int32_t* bt2 = (int32_t*)((uint8_t*)ws + bt_off);
   int32_t* ctx2 = (int32_t*)((uint8_t*)ws + ctx_off);
-  PKV_CUDA(launch_expand_prefill(B, n_q, max_blocks, bt, ctx, bt2, ctx2, p->err_dev, (cudaStream_t)stream),
+  PKV_CUDA(launch_expand_prefill(B, n_q, nq, max_blocks, bt, ctx, bt2, ctx2, p->err_dev, (cudaStream_t)stream),
            "prefill expansion launch");
-  // q [B, n_q, Hq, D] and out [B, n_q, Hq, D] are [B * n_q, Hq, D]: decode of the virtual sequences.
-  // K/V blocks of a sequence are read by all n_q of its queries: normal L2 priority.
-  (void)max_ctx;
-  return decode_impl(p, layer, B * n_q, Hq, q, bt2, max_blocks, ctx2, scale, out, (uint8_t*)ws + dec_off,
-                     ws_bytes - dec_off, stream, 1);
+  // q [B, n_q, Hq, D] and out [B, n_q, Hq, D] are [Bv, nq * Hq, D]: virtual sequence v
+  // holds queries nq * (v mod (n_q / nq)) .. + nq - 1 of its sequence.  The K/V blocks
+  // of a sequence are read by all of its virtual sequences: normal L2 priority.
+  return decode_impl(p, layer, Bv, Hq * nq, q, bt2, max_blocks, ctx2, scale, out, (uint8_t*)ws + dec_off,
+                     ws_bytes - dec_off, stream, 1, nq);
 }
 
 pkv_status pkv_pool_stats(const pkv_pool* p, pkv_stats* out) {

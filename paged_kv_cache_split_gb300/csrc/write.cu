@@ -260,25 +260,27 @@ __global__ void __launch_bounds__(256) serde_blocks_kernel(const uint8_t* const*
   }
 }
 
-// Chunked prefill as decode of virtual sequences: query i of sequence b's chunk
-// of n_q new tokens becomes virtual sequence b * n_q + i, holding the first
-// ctx[b] - n_q + i + 1 tokens of b (causal) through b's block-table row.  A
-// sequence with fewer than n_q tokens sets the error word (context bit) and its
+// Chunked prefill as decode of virtual sequences: queries nq s .. nq s + nq - 1 of
+// sequence b's chunk of n_q new tokens become virtual sequence b * (n_q / nq) + s,
+// holding the first ctx[b] - n_q + nq (s + 1) tokens of b through b's block-table
+// row (the last of those queries' causal limit; the kernel masks the earlier ones).
+// A sequence with fewer than n_q tokens sets the error word (context bit) and its
 // queries see no token.
-__global__ void expand_prefill_kernel(int B, int n_q, int max_blocks, const int32_t* __restrict__ bt,
+__global__ void expand_prefill_kernel(int B, int n_q, int nq, int max_blocks, const int32_t* __restrict__ bt,
                                       const int32_t* __restrict__ ctx, int32_t* __restrict__ bt_out,
                                       int32_t* __restrict__ ctx_out, int32_t* err) {
-  const int64_t nv = (int64_t)B * n_q;
+  const int S = n_q / nq;  // virtual sequences per sequence
+  const int64_t nv = (int64_t)B * S;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (int64_t idx = first; idx < nv * max_blocks; idx += stride) {
     const int64_t v = idx / max_blocks, j = idx - v * max_blocks;
-    bt_out[idx] = bt[(v / n_q) * max_blocks + j];
+    bt_out[idx] = bt[(v / S) * max_blocks + j];
   }
   for (int64_t v = first; v < nv; v += stride) {
-    const int b = (int)(v / n_q), i = (int)(v - (int64_t)b * n_q);
+    const int b = (int)(v / S), sub = (int)(v - (int64_t)b * S);
     const int32_t L = ctx[b];
-    int32_t vis = L - n_q + i + 1;
+    int32_t vis = L - n_q + nq * (sub + 1);
     if (L < n_q) {
       atomicOr(err, ERR_CTX);
       vis = 0;
@@ -353,13 +355,13 @@ cudaError_t launch_serde_blocks(const uint8_t* const* table, int n_layers, int n
   return cudaGetLastError();
 }
 
-cudaError_t launch_expand_prefill(int B, int n_q, int max_blocks, const int32_t* bt, const int32_t* ctx,
+cudaError_t launch_expand_prefill(int B, int n_q, int nq, int max_blocks, const int32_t* bt, const int32_t* ctx,
                                   int32_t* bt_out, int32_t* ctx_out, int32_t* err, cudaStream_t s) {
-  const int64_t work = (int64_t)B * n_q * (max_blocks > 1 ? max_blocks : 1);
+  const int64_t work = (int64_t)B * (n_q / nq) * (max_blocks > 1 ? max_blocks : 1);
   int64_t grid = (work + 255) / 256;
   if (grid > 8LL * sm_count()) grid = 8LL * sm_count();
   if (grid < 1) grid = 1;
-  expand_prefill_kernel<<<(unsigned)grid, 256, 0, s>>>(B, n_q, max_blocks, bt, ctx, bt_out, ctx_out, err);
+  expand_prefill_kernel<<<(unsigned)grid, 256, 0, s>>>(B, n_q, nq, max_blocks, bt, ctx, bt_out, ctx_out, err);
   return cudaGetLastError();
 }
 

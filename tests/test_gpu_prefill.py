@@ -65,3 +65,25 @@ def test_prefill_rejects_too_many_queries():
     with pytest.raises(pkv.PkvError) as e:
         g.prefill_workspace_bytes(1, 4097, 2, 2)
     assert e.value.status == pkv.PKV_ERR_INVALID
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("G,n_q", [(1, 8), (2, 4), (4, 2), (2, 8), (1, 16)])
+def test_prefill_several_queries_per_tile_bf16(D, G, n_q):
+    """bf16 chunks served n_q' = 8 / G queries per tile (several tiles per chunk when
+    n_q is larger), with CTA counts that start split-K segments inside the chunk, so
+    some rows see no token of their segment."""
+    lens = [n_q, n_q + 1, 33, 47, 64, 500, 1031]
+    w = _case(wl.FMT_BF16, D, 2, G, lens, 91 + G + n_q)
+    g, o, ol = make_pools(w)
+    fill(w, g, o, ol)
+    q = wl.bf16_normal(wl.rng_for(92, n_q), (w.B, n_q, w.Hq, D))
+    bt = w.block_table()
+    ref = o.prefill_attention(0, q, bt, w.ctx(), w.scale)
+    for ctas in [5, 97, 0]:
+        g.decode_set_ctas(ctas)
+        out = g.paged_prefill_attention(0, to_dev_bf16(q), to_dev_i32(bt), to_dev_i32(w.ctx()), w.scale)
+        got = bf16_dev_to_f64(out)
+        assert np.isfinite(got).all()
+        compare(got.reshape(-1, D), ref.reshape(-1, D), f"prefill {w.name} n_q={n_q} ctas={ctas}")
+    assert g.check_errors() == 0
