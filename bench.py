@@ -937,7 +937,7 @@ def run_gpu_prefill(args, rank, world, local):
                       "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB per step vs 129 MB L2)", "cuda_graph": True},
            "query_tokens_per_s": round(w.B * n_q * w.n_layers * world / (ms_step * 1e-3), 1),
            "roofline": {"bound": "hbm", "achieved": round(bytes_layer / (launch_us * 1e-6) / 1e9, 1), "peak": peak,
-                        "unit": "GB/s", "frac": round(bytes_layer / (launch_us * 1e-6) / 1e9 / peak, 4), "traffic": None,
+                        "unit": "GB/s", "frac": round(bytes_layer / (launch_us * 1e-6) / 1e9 / peak, 4), "traffic": ncu_traffic(PREFILL),
                         "per_launch_bytes": bytes_layer, "avg_launch_us": round(launch_us, 3), "peak_source": peak_src,
                         "kernel": "expansion + decode attention + combine kernels per layer"},
            "e2e": {"value": round(bytes_step * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
