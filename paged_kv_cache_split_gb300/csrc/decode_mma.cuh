@@ -58,14 +58,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // NQ > 1 (chunked prefill): a virtual sequence carries NQ consecutive queries of one
 // sequence's chunk, and the S tile's rows are (query, head) pairs, query-major: row
-// r is query r / G and head r % G of the kv head, so up to 8 rows serve NQ queries
-// at the cost of one decode.  Query j of NQ sees the sequence's first
-// L - (NQ - 1 - j) tokens (causal); P.Hq counts the NQ queries' heads.
+// r is query r / G and head r % G of the kv head.  Up to 8 rows ride in the rows
+// decode leaves empty; with more (up to 16, head dims up to 128) rows 8..15 get a
+// second softmax state and a second PV product per lane.  Query j of NQ sees the
+// sequence's first L - (NQ - 1 - j) tokens (causal); P.Hq counts the NQ queries' heads.
 template <int D, int G, int NQ = 1>
 __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const DecodeParams P) {
   static_assert(G >= 1 && G <= 8 && D % 16 == 0, "geometry");
-  static_assert(NQ >= 1 && NQ * G <= 8, "query rows of one kv head fit the tile's first 8 rows");
-  constexpr int R = NQ * G;  // rows in use
+  static_assert(NQ >= 1 && NQ * G <= 16 && (NQ * G <= 8 || D <= 128), "query rows of one kv head fit the tile");
+  constexpr int R = NQ * G;      // rows in use
+  constexpr bool TWO = R > 8;    // rows 8..15 in use
   extern __shared__ __align__(128) uint8_t smem[];
   const int hkv = P.lv.hkv;
   const int NC = hkv;
@@ -144,6 +146,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   uint32_t qa[D / 16][2];
   float o[D / 16][4];
   float m_run = -INFINITY, l_run = 0.f;
+  uint32_t qa8[D / 16][2];  // rows g + 8 (TWO only)
+  float o8[D / 16][4];
+  float m_run8 = -INFINITY, l_run8 = 0.f;
   bool dead = false;
   const uint32_t smem_base = smem_u32(stages);
 
@@ -161,12 +166,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
         for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
       m_run = -INFINITY;
       l_run = 0.f;
+      if constexpr (TWO) {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o8[mt][i] = 0.f;
+        m_run8 = -INFINITY;
+        l_run8 = 0.f;
+      }
     }
 
     const int32_t tok0 = (u - UP[b]) * T;
     const int nv = min(T, LS[b] - tok0);
     // tokens of this unit visible to the lane's row (its query's causal limit)
     const int nvr = NQ == 1 ? nv : min(T, LS[b] - tok0 - (NQ - 1 - (g < R ? g / G : NQ - 1)));
+    const int nvr8 = TWO ? min(T, LS[b] - tok0 - (NQ - 1 - (g + 8 < R ? (g + 8) / G : NQ - 1))) : 0;
     if (!dead && !mbar_wait_bounded(&full[s], phase, err)) dead = true;
     dead = __shfl_sync(0xffffffffu, dead, 0);
     if (!dead && seg_start) {
@@ -178,6 +192,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
       for (int kk = 0; kk < D / 16; ++kk) {
         qa[kk][0] = g < R ? qrow[(16 * kk + 2 * t) / 2] : 0u;
         qa[kk][1] = g < R ? qrow[(16 * kk + 2 * t + 8) / 2] : 0u;
+      }
+      if constexpr (TWO) {
+        const uint32_t* qrow8 = reinterpret_cast<const uint32_t*>(stages + (size_t)s * P.stage_bytes + offQ +
+                                                                  qhead(g + 8 < R ? g + 8 : 0) * D * 2);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          qa8[kk][0] = g + 8 < R ? qrow8[(16 * kk + 2 * t) / 2] : 0u;
+          qa8[kk][1] = g + 8 < R ? qrow8[(16 * kk + 2 * t + 8) / 2] : 0u;
+        }
       }
     }
     if (!dead) {
@@ -193,8 +216,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
         for (int kk = 0; kk < D / 16; ++kk) {
           uint32_t r0, r1, r2, r3;
           ldsm_x4(kaddr + (kk >> 2) * 2048 + ld_chunk[kk & 3], r0, r1, r2, r3);
-          mma_bf16_16816(sacc[0], qa[kk][0], 0u, qa[kk][1], 0u, r0, r1);
-          mma_bf16_16816(sacc[1], qa[kk][0], 0u, qa[kk][1], 0u, r2, r3);
+          if constexpr (TWO) {
+            mma_bf16_16816(sacc[0], qa[kk][0], qa8[kk][0], qa[kk][1], qa8[kk][1], r0, r1);
+            mma_bf16_16816(sacc[1], qa[kk][0], qa8[kk][0], qa[kk][1], qa8[kk][1], r2, r3);
+          } else {
+            mma_bf16_16816(sacc[0], qa[kk][0], 0u, qa[kk][1], 0u, r0, r1);
+            mma_bf16_16816(sacc[1], qa[kk][0], 0u, qa[kk][1], 0u, r2, r3);
+          }
         }
         // ---- online softmax for head g (row g), tokens 2t, 2t+1, 8+2t, 9+2t ----
         const int tb = kc * 16 + 2 * t;
@@ -230,6 +258,38 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
         }
         l_run += (p0 + p1) + (p2 + p3);
         const uint32_t pb0 = pack_bf16x2(p0, p1), pb1 = pack_bf16x2(p2, p3);
+        uint32_t pb2 = 0u, pb3 = 0u;
+        if constexpr (TWO) {
+          // ---- the same for rows g + 8 (fragment elements 2 and 3) ----
+          const float y0 = tb < nvr8 ? sacc[0][2] * P.scale_log2 : -INFINITY;
+          const float y1 = tb + 1 < nvr8 ? sacc[0][3] * P.scale_log2 : -INFINITY;
+          const float y2 = tb + 8 < nvr8 ? sacc[1][2] * P.scale_log2 : -INFINITY;
+          const float y3 = tb + 9 < nvr8 ? sacc[1][3] * P.scale_log2 : -INFINITY;
+          float my = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
+          my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
+          my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
+          const bool grow8 = my > m_run8;
+          if (__any_sync(0xffffffffu, grow8)) {
+            const float alpha = grow8 ? exp2f(m_run8 - my) : 1.0f;
+            if (grow8) m_run8 = my;
+            l_run8 *= alpha;
+            const float ae = __shfl_sync(0xffffffffu, alpha, 8 * t);
+            const float ao = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              o8[mt][0] *= ae;
+              o8[mt][2] *= ae;
+              o8[mt][1] *= ao;
+              o8[mt][3] *= ao;
+            }
+          }
+          float q0 = exp2f(y0 - m_run8), q1 = exp2f(y1 - m_run8);
+          float q2 = exp2f(y2 - m_run8), q3 = exp2f(y3 - m_run8);
+          if (m_run8 == -INFINITY) q0 = q1 = q2 = q3 = 0.f;
+          l_run8 += (q0 + q1) + (q2 + q3);
+          pb2 = pack_bf16x2(q0, q1);
+          pb3 = pack_bf16x2(q2, q3);
+        }
         // ---- O^T += V^T P^T over these 16 tokens ----
         const uint32_t vaddr = vst + (uint32_t)(kc * NX * 2048) + ld_base;
 #pragma unroll
@@ -237,6 +297,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
           uint32_t a0, a1, a2, a3;
           ldsm_x4_t(vaddr + (mt >> 2) * 2048 + ld_chunk[mt & 3], a0, a1, a2, a3);
           mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+          if constexpr (TWO) mma_bf16_16816(o8[mt], a0, a1, a2, a3, pb2, pb3);
         }
       }
       __syncwarp();
@@ -244,53 +305,58 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
     }
 
     if (seg_end) {
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-      const float me = __shfl_sync(0xffffffffu, m_run, 8 * t), mo = __shfl_sync(0xffffffffu, m_run, 8 * t + 4);
-      const float le = __shfl_sync(0xffffffffu, l_run, 8 * t), lo = __shfl_sync(0xffffffffu, l_run, 8 * t + 4);
-      const int he = 2 * t, ho = 2 * t + 1;
-      const int32_t c_lo = UP[b] / C, c_hi = (UP[b + 1] - 1) / C;
-      if (c_lo == c_hi) {
-        const float ie = 1.0f / le, io = 1.0f / lo;
-        uint16_t* oe = P.out + ((size_t)b * P.Hq + qhead(he < R ? he : 0)) * D;
-        uint16_t* oo = P.out + ((size_t)b * P.Hq + qhead(ho < R ? ho : 0)) * D;
+      // rows rb + 2t and rb + 2t + 1 of the tile (this lane's O^T columns)
+      auto finish = [&](const float (&ov)[D / 16][4], float mv, float lv, const int rb) {
+        lv += __shfl_xor_sync(0xffffffffu, lv, 1);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 2);
+        const float me = __shfl_sync(0xffffffffu, mv, 8 * t), mo = __shfl_sync(0xffffffffu, mv, 8 * t + 4);
+        const float le = __shfl_sync(0xffffffffu, lv, 8 * t), lo = __shfl_sync(0xffffffffu, lv, 8 * t + 4);
+        const int he = rb + 2 * t, ho = rb + 2 * t + 1;
+        const int32_t c_lo = UP[b] / C, c_hi = (UP[b + 1] - 1) / C;
+        if (c_lo == c_hi) {
+          const float ie = 1.0f / le, io = 1.0f / lo;
+          uint16_t* oe = P.out + ((size_t)b * P.Hq + qhead(he < R ? he : 0)) * D;
+          uint16_t* oo = P.out + ((size_t)b * P.Hq + qhead(ho < R ? ho : 0)) * D;
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
+          for (int mt = 0; mt < D / 16; ++mt) {
+            if (he < R) {
+              oe[16 * mt + g] = f2bf(ov[mt][0] * ie);
+              oe[16 * mt + g + 8] = f2bf(ov[mt][2] * ie);
+            }
+            if (ho < R) {
+              oo[16 * mt + g] = f2bf(ov[mt][1] * io);
+              oo[16 * mt + g + 8] = f2bf(ov[mt][3] * io);
+            }
+          }
+        } else {
+          float* pe = partial_ptr(P, D, (size_t)blockIdx.x, b, qhead(he < R ? he : 0));
+          float* po = partial_ptr(P, D, (size_t)blockIdx.x, b, qhead(ho < R ? ho : 0));
           if (he < R) {
-            oe[16 * mt + g] = f2bf(o[mt][0] * ie);
-            oe[16 * mt + g + 8] = f2bf(o[mt][2] * ie);
+            if (g == 0) {
+              pe[0] = me;
+              pe[1] = le;
+            }
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              pe[kPartialHeader + 16 * mt + g] = ov[mt][0];
+              pe[kPartialHeader + 16 * mt + g + 8] = ov[mt][2];
+            }
           }
           if (ho < R) {
-            oo[16 * mt + g] = f2bf(o[mt][1] * io);
-            oo[16 * mt + g + 8] = f2bf(o[mt][3] * io);
-          }
-        }
-      } else {
-        float* pe = partial_ptr(P, D, (size_t)blockIdx.x, b, qhead(he < R ? he : 0));
-        float* po = partial_ptr(P, D, (size_t)blockIdx.x, b, qhead(ho < R ? ho : 0));
-        if (he < R) {
-          if (g == 0) {
-            pe[0] = me;
-            pe[1] = le;
-          }
+            if (g == 0) {
+              po[0] = mo;
+              po[1] = lo;
+            }
 #pragma unroll
-          for (int mt = 0; mt < D / 16; ++mt) {
-            pe[kPartialHeader + 16 * mt + g] = o[mt][0];
-            pe[kPartialHeader + 16 * mt + g + 8] = o[mt][2];
+            for (int mt = 0; mt < D / 16; ++mt) {
+              po[kPartialHeader + 16 * mt + g] = ov[mt][1];
+              po[kPartialHeader + 16 * mt + g + 8] = ov[mt][3];
+            }
           }
         }
-        if (ho < R) {
-          if (g == 0) {
-            po[0] = mo;
-            po[1] = lo;
-          }
-#pragma unroll
-          for (int mt = 0; mt < D / 16; ++mt) {
-            po[kPartialHeader + 16 * mt + g] = o[mt][1];
-            po[kPartialHeader + 16 * mt + g + 8] = o[mt][3];
-          }
-        }
-      }
+      };
+      finish(o, m_run, l_run, 0);
+      if constexpr (TWO) finish(o8, m_run8, l_run8, 8);
     }
   }
 }

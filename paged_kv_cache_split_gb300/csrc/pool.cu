@@ -537,8 +537,8 @@ static pkv_status decode_impl(pkv_pool* p, int layer, int B, int Hq, const void*
   if (B == 0) return PKV_OK;
   const int hkv = p->cfg.n_kv_heads;
   if (Hq % hkv) return PKV_ERR_INVALID;
-  const int G = Hq / hkv;
-  if (!(G == 1 || G == 2 || G == 4 || G == 8)) return PKV_ERR_INVALID;
+  const int G = Hq / hkv;  // with nq > 1: rows of the tile per kv head (nq x heads per kv head)
+  if (!(G == 1 || G == 2 || G == 4 || G == 8 || (nq > 1 && G == 16))) return PKV_ERR_INVALID;
   if (!q || !bt || !ctx || !out || !ws) return PKV_ERR_INVALID;
   if (!std::isfinite(scale)) return PKV_ERR_INVALID;
   if (ws_bytes < workspace_bytes(p, B, Hq)) return PKV_ERR_INVALID;
@@ -594,13 +594,15 @@ pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, con
 }
 
 // Chunked prefill: queries per virtual sequence.  The bf16 kernel serves nq
-// queries of one sequence per tile when nq x (query heads per kv head) <= 8 and nq
-// divides the chunk; the packed kernels take one query per virtual sequence.
+// queries of one sequence per tile when nq x (query heads per kv head) fits the
+// tile's 16 rows (8 at head_dim 256) and nq divides the chunk; the packed kernels
+// take one query per virtual sequence.
 static int prefill_nq(const pkv_pool* p, int n_q, int Hq) {
   if (p->cfg.format != PKV_FMT_BF16 || Hq % p->cfg.n_kv_heads) return 1;
   const int G = Hq / p->cfg.n_kv_heads;
-  for (int nq = 8; nq > 1; nq >>= 1)
-    if (nq * G <= 8 && n_q % nq == 0) return nq;
+  const int rows = p->cfg.head_dim <= 128 ? 16 : 8;
+  for (int nq = 16; nq > 1; nq >>= 1)
+    if (nq * G <= rows && n_q % nq == 0) return nq;
   return 1;
 }
 

@@ -68,11 +68,12 @@ def test_prefill_rejects_too_many_queries():
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("G,n_q", [(1, 8), (2, 4), (4, 2), (2, 8), (1, 16)])
+@pytest.mark.parametrize("G,n_q", [(1, 8), (2, 4), (4, 2), (2, 8), (1, 16), (4, 4), (8, 2)])
 def test_prefill_several_queries_per_tile_bf16(D, G, n_q):
-    """bf16 chunks served n_q' = 8 / G queries per tile (several tiles per chunk when
-    n_q is larger), with CTA counts that start split-K segments inside the chunk, so
-    some rows see no token of their segment."""
+    """bf16 chunks served several queries per tile (up to 16 rows of (query, head)
+    pairs at head dims 64/128, 8 at 256; several tiles per chunk when n_q is larger),
+    with CTA counts that start split-K segments inside the chunk, so some rows see no
+    token of their segment."""
     lens = [n_q, n_q + 1, 33, 47, 64, 500, 1031]
     w = _case(wl.FMT_BF16, D, 2, G, lens, 91 + G + n_q)
     g, o, ol = make_pools(w)
