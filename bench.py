@@ -804,6 +804,7 @@ def run_gpu_blocks(args, rank, world, local):
 
 
 PREFILL = "prefill-qwen3-0.6b"
+PREFILL_PACKED = "prefill-qwen3-1.7b-k4v4"
 PREFILL_NQ = 8  # new tokens per sequence in the chunk
 
 
@@ -843,7 +844,10 @@ def run_gpu_prefill(args, rank, world, local):
     import paged_kv_cache_split_gb300 as pkv
 
     torch.cuda.set_device(local)
-    w = wl.qwen3_0_6b(n_layers=args.layers) if args.layers else wl.qwen3_0_6b()
+    if args.workload == PREFILL_PACKED:
+        w = wl.qwen3_1_7b_k4v4()
+    else:
+        w = wl.qwen3_0_6b(n_layers=args.layers) if args.layers else wl.qwen3_0_6b()
     n_q = PREFILL_NQ
     dev = torch.device("cuda", local)
     pool = pkv.Pool(w.n_layers, w.Hkv, w.D, pkv.FORMAT_NAMES[w.fmt], hadamard_seed=w.hadamard_seed,
@@ -937,9 +941,9 @@ def run_gpu_prefill(args, rank, world, local):
                       "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB per step vs 129 MB L2)", "cuda_graph": True},
            "query_tokens_per_s": round(w.B * n_q * w.n_layers * world / (ms_step * 1e-3), 1),
            "roofline": {"bound": "hbm", "achieved": round(bytes_layer / (launch_us * 1e-6) / 1e9, 1), "peak": peak,
-                        "unit": "GB/s", "frac": round(bytes_layer / (launch_us * 1e-6) / 1e9 / peak, 4), "traffic": ncu_traffic(PREFILL),
+                        "unit": "GB/s", "frac": round(bytes_layer / (launch_us * 1e-6) / 1e9 / peak, 4), "traffic": ncu_traffic(args.workload),
                         "per_launch_bytes": bytes_layer, "avg_launch_us": round(launch_us, 3), "peak_source": peak_src,
-                        "kernel": "expansion + decode attention + combine kernels per layer"},
+                        "kernel": "expansion + attention + combine kernels per layer"},
            "e2e": {"value": round(bytes_step * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
                    "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": int(q.numel() * 2),
                    "d2h_bytes_per_step": int(out.numel() * 2)},
@@ -983,7 +987,7 @@ def main():
         print(json.dumps(res), flush=True)
         return
 
-    if args.workload == PREFILL:
+    if args.workload in (PREFILL, PREFILL_PACKED):
         if args.impl == "reference":
             if rank == 0:
                 cb = prefill_oracle_sample(budget_s=max(2.0, 0.05 * (args.warmup + args.steps)))

@@ -2,5 +2,8 @@
 #include "decode_packed_mma.cuh"
 
 namespace pkv {
-cudaError_t launch_decode_k8v4(const DecodeArgs& a) { return launch_decode_packed_mma<PKV_FMT_K8V4>(a); }
+cudaError_t launch_decode_k8v4(const DecodeArgs& a) {
+  if (a.nq > 1) return launch_decode_k8v4_mq(a);
+  return launch_decode_packed_mma<PKV_FMT_K8V4>(a);
+}
 }  // namespace pkv

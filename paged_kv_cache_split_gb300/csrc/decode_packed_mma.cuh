@@ -179,7 +179,11 @@ constexpr int kProdRegs = 56;
 // the output).  Per 16-token chunk the two halves of every logit are exchanged
 // through shared memory and added in a fixed order, so both warps run the same
 // softmax; each keeps the state of its own dims.
-template <int FMT, int D, int G, bool W128, bool RS, bool DS, int GS>
+// NQ > 1 (chunked prefill): the S tile's rows are (query, head) pairs of NQ
+// consecutive queries of one sequence, query-major (row r: query r / G, head r % G
+// of the kv head; NQ x G <= 8), each masked at its query's causal limit; P.Hq counts
+// the NQ queries' heads.
+template <int FMT, int D, int G, bool W128, bool RS, bool DS, int GS, int NQ = 1>
 __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packed_mma_kernel(const DecodeParams P) {
   using Tr = PackedTraits<FMT, D, GS>;
   static_assert(G >= 1 && G <= 8 && D % 32 == 0, "geometry");
@@ -188,6 +192,8 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   extern __shared__ __align__(128) uint8_t smem[];
   const int hkv = P.lv.hkv;
   const int NC = DS ? 2 * hkv : hkv;  // consumer warps
+  constexpr int RW = NQ * G;          // tile rows in use
+  static_assert(RW <= 8, "query rows of one kv head fit the tile's first 8 rows");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NCW = (NC + 3) >> 2;                // consumer warpgroups (register split)
   const int PW = RS ? 4 * NCW : NC;             // the first of the two producer warps
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   float* qscr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(LS + B) + 15) & ~uintptr_t(15));
   // dim split: per kv head, each half's partial logits (up to 32 tokens) of the last two exchanges, and
   // one mbarrier per kv head that pairs the two warps (bounded waits)
-  float4* xbuf = reinterpret_cast<float4*>(qscr + (size_t)hkv * G * D);
+  float4* xbuf = reinterpret_cast<float4*>(qscr + (size_t)hkv * RW * D);
   uint64_t* pbar = reinterpret_cast<uint64_t*>(xbuf + (size_t)hkv * 2 * 2 * 2 * 32);
   // the producers' issue token, one barrier per batch parity (after the dim-split
   // buffers, or where they would start)
@@ -284,7 +290,12 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   const int half = DS ? warp / hkv : 0;
   const int gofs = half * NGL;
   const int g = lane >> 2, t = lane & 3;
-  float* qs = qscr + (size_t)h * G * D;  // dim split: shared by the pair, written by half 0
+  float* qs = qscr + (size_t)h * RW * D;  // dim split: shared by the pair, written by half 0
+  // q head (within the virtual sequence's P.Hq) of tile row r
+  auto qhead = [&](int r) -> size_t {
+    if constexpr (NQ == 1) return (size_t)h * G + r;
+    else return (size_t)(r / G) * (size_t)(P.Hq / NQ) + (size_t)h * G + (size_t)(r % G);
+  };
   uint32_t qa[NGL][2][2];  // A fragments per group, k-step, register (rows g; rows g+8 zero)
   float qsum[NGL];         // 2^-24 * sum over the group of the q~ values the MMA sees
   float o[NGL][2][4];      // O^T accumulators, in units of 2^-24: group, M tile, fragment
@@ -481,6 +492,12 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     for (int jj = 0; jj < NT; ++jj)
 #pragma unroll
       for (int e = 0; e < 2; ++e) p[jj][e] = ex2(x[jj][e] - m_run);
+    if constexpr (NQ > 1) {
+      // a row with no visible token yet in this segment keeps m_run = -inf
+      if (m_run == -INFINITY)
+#pragma unroll
+        for (int jj = 0; jj < NT; ++jj) p[jj][0] = p[jj][1] = 0.f;
+    }
     float ls = p[0][0] + p[0][1];
 #pragma unroll
     for (int jj = 1; jj < NT; ++jj) ls += p[jj][0] + p[jj][1];
@@ -582,15 +599,16 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
           // Hadamard transform with lane l holding dims l + 32 r of one head (butterfly
           // spans 1..16 across lanes, 32.. in registers), written to the head's scratch.
           constexpr int R = D / 32;
-          const uint16_t* qsm = reinterpret_cast<const uint16_t*>(st + offQ) + (size_t)h * G * D;
+          const uint16_t* qsm0 = reinterpret_cast<const uint16_t*>(st + offQ);
           float sg[R];
 #pragma unroll
           for (int r = 0; r < R; ++r) sg[r] = P.signs[lane + 32 * r];
 #pragma unroll 1
-          for (int gg = 0; gg < G; ++gg) {
+          for (int gg = 0; gg < RW; ++gg) {
+            const uint16_t* qsm = qsm0 + qhead(gg) * D;
             float v[R];
 #pragma unroll
-            for (int r = 0; r < R; ++r) v[r] = __uint_as_float((uint32_t)qsm[gg * D + lane + 32 * r] << 16) * sg[r];
+            for (int r = 0; r < R; ++r) v[r] = __uint_as_float((uint32_t)qsm[lane + 32 * r] << 16) * sg[r];
 #pragma unroll
             for (int hs = 1; hs < 32; hs <<= 1) {
               const float sgn = (lane & hs) ? -1.f : 1.f;  // upper element: x - y; lower: x + y
@@ -627,7 +645,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
                 const int dd = 32 * (gofs + grp) + k_dim<Tr::KBITS>(t, ks, r, hh, d16);
-                const float qv = g < G ? qs[g * D + dd] * P.inv_sqrt_d : 0.f;
+                const float qv = g < RW ? qs[g * D + dd] * P.inv_sqrt_d : 0.f;
                 v[hh] = d16 ? qv * 0.0625f : qv;
               }
               qa[grp][ks][r] = pack_f16x2(v[0], v[1]);
@@ -641,7 +659,9 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
         __syncwarp();
       }
       const int nv = min(T, Lb - (u - UP[b]) * T);
-      if (kUnit32 && T == 32 && nv == 32) {
+      // tokens of this unit visible to the lane's row (its query's causal limit)
+      const int nvr = NQ == 1 ? nv : min(T, Lb - (u - UP[b]) * T - (NQ - 1 - (g < RW ? g / G : NQ - 1)));
+      if (kUnit32 && T == 32 && nv == 32 && (NQ == 1 || Lb - (u - UP[b]) * T - (NQ - 1) >= 32)) {
         float x[4][2], p[4][2];
         if (!logits(std::integral_constant<int, 4>{}, sb, 0, x)) return;
 #pragma unroll
@@ -659,8 +679,8 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const int tk = kc * 16 + 8 * j + 2 * t;
-            x[j][0] = tk < nv ? x[j][0] * scale24 : -INFINITY;
-            x[j][1] = tk + 1 < nv ? x[j][1] * scale24 : -INFINITY;
+            x[j][0] = tk < nvr ? x[j][0] * scale24 : -INFINITY;
+            x[j][1] = tk + 1 < nvr ? x[j][1] * scale24 : -INFINITY;
           }
           softmax(std::integral_constant<int, 2>{}, x, p);
           pv(sb, kc, p, 0);
@@ -696,30 +716,30 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
       const int32_t c_lo = UP[b] / C, c_hi = (UP[b + 1] - 1) / C;
       if (c_lo == c_hi) {
         const float ie = 1.0f / le, io = 1.0f / lo;
-        uint16_t* oe = P.out + ((size_t)b * P.Hq + (size_t)h * G + he) * D;
-        uint16_t* oo = P.out + ((size_t)b * P.Hq + (size_t)h * G + ho) * D;
+        uint16_t* oe = P.out + ((size_t)b * P.Hq + qhead(he < RW ? he : 0)) * D;
+        uint16_t* oo = P.out + ((size_t)b * P.Hq + qhead(ho < RW ? ho : 0)) * D;
 #pragma unroll
         for (int grp = 0; grp < NGL; ++grp)
 #pragma unroll
           for (int mi = 0; mi < 2; ++mi) {
             const int d0 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 0, g), d1 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 1, g);
-            if (he < G) {
+            if (he < RW) {
               oe[d0] = f2bf(fmaf(o[grp][mi][0], fs[mi], ce[grp]) * ie);
               oe[d1] = f2bf(fmaf(o[grp][mi][2], fs[mi], ce[grp]) * ie);
             }
-            if (ho < G) {
+            if (ho < RW) {
               oo[d0] = f2bf(fmaf(o[grp][mi][1], fs[mi], co[grp]) * io);
               oo[d1] = f2bf(fmaf(o[grp][mi][3], fs[mi], co[grp]) * io);
             }
           }
       } else {
-        float* pe = partial_ptr(P, D, (size_t)blockIdx.x, b, (size_t)h * G + he);
-        float* po = partial_ptr(P, D, (size_t)blockIdx.x, b, (size_t)h * G + ho);
-        if (he < G && g == 0 && half == 0) {
+        float* pe = partial_ptr(P, D, (size_t)blockIdx.x, b, qhead(he < RW ? he : 0));
+        float* po = partial_ptr(P, D, (size_t)blockIdx.x, b, qhead(ho < RW ? ho : 0));
+        if (he < RW && g == 0 && half == 0) {
           pe[0] = me;
           pe[1] = le;
         }
-        if (ho < G && g == 0 && half == 0) {
+        if (ho < RW && g == 0 && half == 0) {
           po[0] = mo;
           po[1] = lo;
         }
@@ -728,11 +748,11 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 #pragma unroll
           for (int mi = 0; mi < 2; ++mi) {
             const int d0 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 0, g), d1 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 1, g);
-            if (he < G) {
+            if (he < RW) {
               pe[kPartialHeader + d0] = fmaf(o[grp][mi][0], fs[mi], ce[grp]);
               pe[kPartialHeader + d1] = fmaf(o[grp][mi][2], fs[mi], ce[grp]);
             }
-            if (ho < G) {
+            if (ho < RW) {
               po[kPartialHeader + d0] = fmaf(o[grp][mi][1], fs[mi], co[grp]);
               po[kPartialHeader + d1] = fmaf(o[grp][mi][3], fs[mi], co[grp]);
             }
@@ -743,7 +763,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   }
 }
 
-template <int FMT, int D, int G, bool W128, bool RS, bool DS, int GS>
+template <int FMT, int D, int G, bool W128, bool RS, bool DS, int GS, int NQ = 1>
 cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   using Tr = PackedTraits<FMT, D, GS>;
   DecodeParams P;
@@ -765,7 +785,7 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   P.NS = a.n_stages;
   const int hkv = a.lv.hkv;
   P.stage_bytes = packed_stage_bytes(P.T, hkv * Tr::KB, hkv * Tr::VB, hkv * Tr::MB, a.Hq * D * 2);
-  auto kern = decode_packed_mma_kernel<FMT, D, G, W128, RS, DS, GS>;
+  auto kern = decode_packed_mma_kernel<FMT, D, G, W128, RS, DS, GS, NQ>;
   {
     static unsigned long long smem_done = 0;  // this kernel (one per template instantiation)
     cudaError_t e = allow_max_dynamic_smem(kern, smem_done);
@@ -814,6 +834,30 @@ cudaError_t launch_decode_packed_mma(const DecodeArgs& a) {
   PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
   PKV_CASE(256, 1) PKV_CASE(256, 2) PKV_CASE(256, 4) PKV_CASE(256, 8)
 #undef PKV_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv
+
+namespace pkv {
+
+// Chunked prefill in the packed formats: NQ = 8 / G queries per tile (the plain
+// variants: no register split, no dim split).
+template <int FMT, int GS = kGroup>
+cudaError_t launch_decode_packed_mma_mq(const DecodeArgs& a) {
+  const bool w128 = a.lv.box_bytes[0] == 128 && a.lv.box_bytes[1] == 128 && a.lv.box_bytes[2] == 128 &&
+                    a.lv.box_bytes[3] == 128;
+  const int G = a.G / a.nq;
+#define PKV_MQ(DD, GG)                                                                           \
+  if (a.D == DD && G == GG && a.nq == 8 / GG)                                                    \
+    return w128 ? launch_decode_packed_mma_t<FMT, DD, GG, true, false, false, GS, 8 / GG>(a)      \
+                : launch_decode_packed_mma_t<FMT, DD, GG, false, false, false, GS, 8 / GG>(a);
+  if constexpr (GS == kGroup) {
+    PKV_MQ(64, 1) PKV_MQ(64, 2) PKV_MQ(64, 4)
+  }
+  PKV_MQ(128, 1) PKV_MQ(128, 2) PKV_MQ(128, 4)
+  PKV_MQ(256, 1) PKV_MQ(256, 2) PKV_MQ(256, 4)
+#undef PKV_MQ
   return cudaErrorInvalidValue;
 }
 

@@ -256,6 +256,11 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a);
 cudaError_t launch_decode_bf16_mq(const DecodeArgs& a);  // nq > 1 (decode_bf16_mq.cu)
 cudaError_t launch_decode_k4v4(const DecodeArgs& a);
 cudaError_t launch_decode_k4v4_g64(const DecodeArgs& a);  // groups of 64 (decode_k4v4g64.cu)
+// nq > 1 (chunked prefill), per format: decode_*_mq.cu
+cudaError_t launch_decode_k4v4_mq(const DecodeArgs& a);
+cudaError_t launch_decode_k4v4_g64_mq(const DecodeArgs& a);
+cudaError_t launch_decode_k8v4_mq(const DecodeArgs& a);
+cudaError_t launch_decode_k8v8_mq(const DecodeArgs& a);
 cudaError_t launch_decode_k8v4(const DecodeArgs& a);
 cudaError_t launch_decode_k8v8(const DecodeArgs& a);
 

@@ -596,10 +596,15 @@ pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, con
 // Chunked prefill: queries per virtual sequence.  The bf16 kernel serves nq
 // queries of one sequence per tile when nq x (query heads per kv head) fits the
 // tile's 16 rows (8 at head_dim 256) and nq divides the chunk; the packed kernels
-// take one query per virtual sequence.
+// serve 8 / (query heads per kv head) when that divides the chunk.
 static int prefill_nq(const pkv_pool* p, int n_q, int Hq) {
-  if (p->cfg.format != PKV_FMT_BF16 || Hq % p->cfg.n_kv_heads) return 1;
+  if (Hq % p->cfg.n_kv_heads) return 1;
   const int G = Hq / p->cfg.n_kv_heads;
+  if (p->cfg.format != PKV_FMT_BF16) {
+    // packed kernels: 8 / G queries per tile (8 rows)
+    const int nq = 8 / G;
+    return (nq > 1 && n_q % nq == 0) ? nq : 1;
+  }
   const int rows = p->cfg.head_dim <= 128 ? 16 : 8;
   for (int nq = 16; nq > 1; nq >>= 1)
     if (nq * G <= rows && n_q % nq == 0) return nq;

@@ -88,3 +88,25 @@ def test_prefill_several_queries_per_tile_bf16(D, G, n_q):
         assert np.isfinite(got).all()
         compare(got.reshape(-1, D), ref.reshape(-1, D), f"prefill {w.name} n_q={n_q} ctas={ctas}")
     assert g.check_errors() == 0
+
+
+@pytest.mark.parametrize("fmt,D,group", [(wl.FMT_K4V4, 128, 32), (wl.FMT_K8V4, 64, 32), (wl.FMT_K8V8, 128, 32),
+                                         (wl.FMT_K4V4, 256, 64)])
+@pytest.mark.parametrize("G,n_q", [(1, 8), (2, 8), (4, 2)])
+def test_prefill_several_queries_per_tile_packed(fmt, D, group, G, n_q):
+    """Packed chunks served 8 / G queries per tile, with CTA counts that start split-K
+    segments inside the chunk."""
+    lens = [n_q, n_q + 1, 33, 64, 500, 1031]
+    w = _case(fmt, D, 2, G, lens, 101 + G + n_q, group)
+    g, o, ol = make_pools(w)
+    fill(w, g, o, ol)
+    q = wl.bf16_normal(wl.rng_for(102, n_q), (w.B, n_q, w.Hq, D))
+    bt = w.block_table()
+    ref = o.prefill_attention(0, q, bt, w.ctx(), w.scale)
+    for ctas in [5, 97, 0]:
+        g.decode_set_ctas(ctas)
+        out = g.paged_prefill_attention(0, to_dev_bf16(q), to_dev_i32(bt), to_dev_i32(w.ctx()), w.scale)
+        got = bf16_dev_to_f64(out)
+        assert np.isfinite(got).all()
+        compare(got.reshape(-1, D), ref.reshape(-1, D), f"prefill {w.name} n_q={n_q} ctas={ctas}")
+    assert g.check_errors() == 0
