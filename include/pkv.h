@@ -248,11 +248,14 @@ pkv_status pkv_prefill_workspace_bytes(const pkv_pool* pool, int B, int n_q, int
  * q_bf16: [B, n_q, Hq, head_dim] bf16, un-rotated (packed formats rotate q
  * internally); out_bf16: [B, n_q, Hq, head_dim]; block_table, ctx_lens and the GQA
  * mapping as for pkv_paged_decode_attention.  The workspace (caller-owned, 256-byte
- * aligned, pkv_prefill_workspace_bytes) holds each query's view of its sequence
- * (the same block-table row, a causal context length) and the split-K partials;
- * each query then runs the decode kernels, so the chunk's K/V blocks are read once
- * from HBM and again from L2 by the chunk's later queries.  A sequence with fewer
- * than n_q tokens sets the device error word (bit 2) and its rows are zero.
+ * aligned, pkv_prefill_workspace_bytes) holds, for each run of NQ consecutive
+ * queries of a sequence, a view of the sequence (the same block-table row, the
+ * last of those queries' causal length) and the split-K partials.  The attention
+ * kernels serve the NQ queries in one tensor-core tile, each masked at its own
+ * causal limit: bf16 up to 16 (query, head) rows per kv head at head_dim <= 128 and
+ * 8 at 256, the packed formats 8; NQ is the largest such count dividing n_q, else 1.
+ * A sequence with fewer than n_q tokens sets the device error word (bit 2) and its
+ * rows are zero.
  * Errors as for pkv_paged_decode_attention; PKV_ERR_INVALID when B * n_q > 4096.
  * Asynchronous.
  *   [mlxcel #2171, Proposed Solution: attend = update the storage, then attention;
