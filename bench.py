@@ -517,8 +517,31 @@ class MixedRun:
             steps.append(per_pool)
         self.steps_host = steps
         self.steps_dev = [[{k: self._dev(v) for k, v in h.items()} for h in sp] for sp in steps]
-        self.steps_pin = [[{k: self._pin(v) for k, v in h.items()} for h in sp] for sp in steps]
-        self.steps_e2e = [[{k: torch.empty_like(v) for k, v in h.items()} for h in sp] for sp in self.steps_dev]
+        # end-to-end arm: each step's inputs of both pools packed in one pinned host buffer
+        # (256-byte aligned segments), copied in with one copy, used through device views
+        self.step_in_h, self.step_in_e, self.steps_e2e = [], [], []
+        for sp in steps:
+            hosts = [self._host(v) for h in sp for v in h.values()]
+            offs, total = [], 0
+            for t in hosts:
+                offs.append(total)
+                total += (t.numel() * t.element_size() + 255) // 256 * 256
+            buf_h = torch.zeros(max(total, 256), dtype=torch.uint8, pin_memory=True)
+            buf_e = torch.empty(buf_h.shape, dtype=torch.uint8, device=self.dev)
+            views, j = [], 0
+            for h in sp:
+                vh = {}
+                for key in h:
+                    t, off = hosts[j], offs[j]
+                    n = t.numel() * t.element_size()
+                    if n:
+                        buf_h[off:off + n].copy_(t.reshape(-1).view(torch.uint8))
+                    vh[key] = buf_e[off:off + n].view(t.dtype).view(t.shape)
+                    j += 1
+                views.append(vh)
+            self.step_in_h.append(buf_h)
+            self.step_in_e.append(buf_e)
+            self.steps_e2e.append(views)
         self.out_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in self.outs]
         torch.cuda.synchronize()
         self.m = m
@@ -530,18 +553,14 @@ class MixedRun:
         t = x if isinstance(x, self.torch.Tensor) else self.torch.from_numpy(np.ascontiguousarray(x))
         return t.to(self.dev)
 
-    def _pin(self, x):
-        t = x if isinstance(x, self.torch.Tensor) else self.torch.from_numpy(np.ascontiguousarray(x))
-        return t.pin_memory()
+    def _host(self, x):
+        return (x if isinstance(x, self.torch.Tensor) else self.torch.from_numpy(np.ascontiguousarray(x))).contiguous()
 
     def run_step(self, i: int, e2e: bool = False):
+        if e2e:
+            self.step_in_e[i].copy_(self.step_in_h[i], non_blocking=True)
         for pi, pool in enumerate(self.pools):
-            d = self.steps_dev[i][pi]
-            if e2e:
-                e, h = self.steps_e2e[i][pi], self.steps_pin[i][pi]
-                for key in e:
-                    e[key].copy_(h[key], non_blocking=True)
-                d = e
+            d = self.steps_e2e[i][pi] if e2e else self.steps_dev[i][pi]
             if d["cow_src"].numel():
                 pool.copy_on_write_block(d["cow_src"], d["cow_dst"])
             pool.write_block(0, d["rows"], d["slots"], d["k"], d["v"])
@@ -568,7 +587,7 @@ class MixedRun:
                    for pi in range(len(self.pools)))
 
     def h2d_d2h(self, i: int):
-        h2d = sum(int(t.numel() * t.element_size()) for sp in self.steps_pin[i] for t in sp.values())
+        h2d = int(self.step_in_h[i].numel())
         d2h = sum(int(o.numel() * o.element_size()) for o in self.outs)
         return h2d, d2h
 
