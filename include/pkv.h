@@ -182,6 +182,10 @@ pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int Hq, int m
  *   out_bf16_dev:    [B, Hq, head_dim] bf16
  *   workspace_dev:   ws_bytes >= pkv_decode_workspace_bytes(B, Hq), zeroed once
  * Deterministic: bitwise identical results for identical inputs on one device.
+ * B = 0 returns PKV_OK with no device work.  PKV_ERR_INVALID, before any work,
+ * when Hq is not n_kv_heads x G with G in {1, 2, 4, 8}, scale is not finite, the
+ * workspace is smaller than pkv_decode_workspace_bytes or not 256-byte aligned,
+ * or q / out are not 16-byte aligned.
  *   [mlxcel issue #2171, "one KV storage abstraction": Proposed Solution
  *    (KVCache::attend -> paged_batch_decode_attention) and Edge cases (single
  *    token, no mask); mlx-swift-lm #142: "direct attention consumes packed pages
