@@ -48,3 +48,9 @@ def test_partial_last_block_not_rounded_up():
     qo = 2 * 3 * 32 * 64 * 2
     bt = sum(math.ceil(L / 32) for L in lens) * 4
     assert got == kv + qo + bt + 4 * 3
+
+
+def test_mixed_row_bytes_is_one_block_of_every_stored_tensor():
+    # one 32-token block of one layer: bf16 K and V, or codes plus (scale, offset) pairs
+    assert bench.mixed_row_bytes(wl.FMT_BF16, 4, 256) == 32 * 4 * 2 * 256 * 2
+    assert bench.mixed_row_bytes(wl.FMT_K4V4, 4, 256) == 32 * 4 * (128 + 128 + 2 * 8 * 8)
