@@ -59,3 +59,20 @@ def test_invalid_config_rejected_before_device_use(lib):
     h = ctypes.c_void_p()
     assert lib.pkv_pool_create(ctypes.byref(cfg), None, None, ctypes.byref(h)) == pkv.PKV_ERR_INVALID
     assert not h.value
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(pkv, "_lib_handle", None)
+    monkeypatch.setattr(pkv, "LIB_PATH", str(tmp_path / "libpkv.so"))
+    with pytest.raises(RuntimeError, match="is missing"):
+        pkv.lib()
+    with pytest.raises(RuntimeError, match="is missing"):
+        pkv.Pool(1, 1, 64, "bf16")
+
+
+def test_no_cpu_path_without_a_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    with pytest.raises(RuntimeError):  # PkvError is a RuntimeError too
+        pkv.Pool(1, 1, 64, "bf16")
