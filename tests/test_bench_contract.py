@@ -3,6 +3,7 @@ with the contract's keys, for every workload, and under a two-rank launch only r
 prints it."""
 import json
 import os
+import socket
 import subprocess
 import sys
 
@@ -36,8 +37,14 @@ def test_reference_arm_prints_one_contract_line(workload):
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 
+def _free_port():
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
 def test_reference_arm_under_two_ranks_prints_once():
     out = _lines([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
-                  "--master-addr", "127.0.0.1", "--master-port", "29531", "bench.py", "--impl", "reference",
+                  "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
                   "--gpus", "2", "--steps", "3", "--warmup", "3"])
     assert len(out) == 1 and out[0]["impl"] == "reference"
