@@ -56,6 +56,13 @@ def bf16_normal(rng: np.random.Generator, shape, outlier_frac: float = 0.0,
     return f32_to_bf16_bits(x)
 
 
+def scale_pow2(bits: np.ndarray, e) -> np.ndarray:
+    """bf16 bits times 2^e (e broadcast against bits): exact while the results stay
+    normal bf16 numbers, which the magnitude plans here keep to."""
+    x = bf16_bits_to_f32(bits).astype(np.float64) * np.exp2(np.asarray(e, np.float64))
+    return f32_to_bf16_bits(x.astype(np.float32)).reshape(np.shape(bits))
+
+
 # ---------------------------------------------------------------------------
 # Row planning (which pool row holds each logical block of each sequence)
 # ---------------------------------------------------------------------------
@@ -143,6 +150,18 @@ class Workload:
     seed: int
     outlier_frac: float = 0.0
     group: int = 32  # values per affine group of the packed formats (64: the five-bit K4/V4 layout)
+    # Magnitude plan (powers of two, so every value stays an exact bf16 and a row's
+    # exponent spread is unchanged): q, K and V are multiplied by 2^q_exp, 2^k_exp and
+    # 2^v_exp; a seeded 1/boost_every of each sequence's tokens has K multiplied by
+    # 2^k_boost and V by 2^v_boost; the second half of each sequence's tokens has V
+    # multiplied by 2^v_ramp.
+    q_exp: int = 0
+    k_exp: int = 0
+    v_exp: int = 0
+    boost_every: int = 64
+    k_boost: int = 0
+    v_boost: int = 0
+    v_ramp: int = 0
 
     @property
     def B(self) -> int:
@@ -161,12 +180,25 @@ class Workload:
     def kv(self, layer: int, b: int):
         """K and V of sequence b at `layer`: two [L_b, Hkv, D] bf16 bit arrays."""
         r = rng_for(self.seed, 1, layer, b)
-        shape = (self.lens[b], self.Hkv, self.D)
-        return (bf16_normal(r, shape, self.outlier_frac), bf16_normal(r, shape, self.outlier_frac))
+        L = self.lens[b]
+        shape = (L, self.Hkv, self.D)
+        k = bf16_normal(r, shape, self.outlier_frac)
+        v = bf16_normal(r, shape, self.outlier_frac)
+        if self.k_exp or self.v_exp or self.k_boost or self.v_boost or self.v_ramp:
+            ke = np.full(L, self.k_exp, np.int32)
+            ve = np.full(L, self.v_exp, np.int32)
+            if self.k_boost or self.v_boost:
+                hit = rng_for(self.seed, 3, layer, b).integers(0, self.boost_every, size=L) == 0
+                ke[hit] += self.k_boost
+                ve[hit] += self.v_boost
+            ve[L // 2:] += self.v_ramp
+            k, v = scale_pow2(k, ke[:, None, None]), scale_pow2(v, ve[:, None, None])
+        return k, v
 
     def q(self, layer: int) -> np.ndarray:
         """[B, Hq, D] bf16 bits."""
-        return bf16_normal(rng_for(self.seed, 2, layer), (self.B, self.Hq, self.D))
+        q = bf16_normal(rng_for(self.seed, 2, layer), (self.B, self.Hq, self.D))
+        return scale_pow2(q, self.q_exp) if self.q_exp else q
 
     def token_placement(self, b: int):
         """(rows, slots) of the tokens of sequence b in logical order."""
