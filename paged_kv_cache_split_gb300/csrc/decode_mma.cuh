@@ -25,6 +25,8 @@
 //    the PV product while the denominator sums the fp32 probabilities.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_common.cuh"
 
 namespace pkv {
@@ -291,14 +293,37 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
           pb3 = pack_bf16x2(q2, q3);
         }
         // ---- O^T += V^T P^T over these 16 tokens ----
+        // The lane's A fragments hold V of tokens tb, tb + 1 (a0, a1) and tb + 8,
+        // tb + 9 (a2, a3).  In a chunk that ends past the context those tokens' slots
+        // may hold stale bytes (an earlier owner of the row, an imported record): their
+        // probability is 0, but 0 times a non-finite value is not, so their V halves
+        // are replaced by zeros.
         const uint32_t vaddr = vst + (uint32_t)(kc * NX * 2048) + ld_base;
+        auto pv_tile = [&](auto masked_c) {
+          constexpr bool MASKED = decltype(masked_c)::value;
+          uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
+          if constexpr (MASKED) {
+            m01 = (tb < nv ? 0x0000ffffu : 0u) | (tb + 1 < nv ? 0xffff0000u : 0u);
+            m89 = (tb + 8 < nv ? 0x0000ffffu : 0u) | (tb + 9 < nv ? 0xffff0000u : 0u);
+          }
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(vaddr + (mt >> 2) * 2048 + ld_chunk[mt & 3], a0, a1, a2, a3);
-          mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
-          if constexpr (TWO) mma_bf16_16816(o8[mt], a0, a1, a2, a3, pb2, pb3);
-        }
+          for (int mt = 0; mt < D / 16; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vaddr + (mt >> 2) * 2048 + ld_chunk[mt & 3], a0, a1, a2, a3);
+            if constexpr (MASKED) {
+              a0 &= m01;
+              a1 &= m01;
+              a2 &= m89;
+              a3 &= m89;
+            }
+            mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+            if constexpr (TWO) mma_bf16_16816(o8[mt], a0, a1, a2, a3, pb2, pb3);
+          }
+        };
+        if (kc * 16 + 16 > nv)
+          pv_tile(std::true_type{});
+        else
+          pv_tile(std::false_type{});
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);

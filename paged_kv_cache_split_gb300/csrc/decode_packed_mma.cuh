@@ -36,6 +36,23 @@
 //    16-row M tile covers 16 dims of one group; the order of dims inside a group
 //    follows the ldmatrix.trans fragment (a lane's two dims per token come from one
 //    half-word of codes) and the output store undoes the permutation.
+//
+// fp16 range.  The stored scales and offsets are FP32 (mlx-swift-lm PR #142,
+// Summary), so q, K and V may have any magnitude; only the two operands rounded to
+// fp16 need care, and both are kept in range by powers of two that are undone in
+// fp32 (exact, so no rounding is added):
+//  * q~ of each tile row is multiplied by 2^e, with e chosen once per sequence
+//    segment so that the row's largest |q~| lies in [2^14, 2^15); the logits' fp32
+//    scale carries 2^-e.
+//  * p s uses an exponent f shared by all of a warp's groups: the softmax works
+//    with the reference max m - f, so every probability (and with it the running
+//    denominator and both accumulators) carries 2^f.  f is set from the first chunk
+//    with a nonzero V scale, so that its largest s 2^f lies in [2^4, 2^5), and is
+//    lowered (the state multiplied by the matching power of two) when a chunk's
+//    products would reach 2^15.  Partial records store the state with 2^f removed.
+// A token past the context (in the last unit of a sequence) gets probability 0
+// and its V scale and offset are replaced by 0 before they meet it, so stale
+// non-finite bytes in unused slots of a block never reach the output.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -160,6 +177,30 @@ __device__ __forceinline__ int swz(const SwzRegion& z, int tok, int b) {
 }
 
 __device__ __forceinline__ int ilog2i(int v) { return 31 - __clz(v); }
+
+// 2^n as a float, for n in [-126, 127].
+__device__ __forceinline__ float pow2i(int n) { return __int_as_float((n + 127) << 23); }
+
+// floor(log2 x) of a positive float, read from its exponent field (fp32 subnormals
+// give -127).
+__device__ __forceinline__ int exponent_of(float x) { return (int)((__float_as_uint(x) >> 23) & 0xffu) - 127; }
+
+// The p s exponent for a largest V scale smax > 0: smax 2^f lands in [2^4, 2^5).
+__device__ __forceinline__ int v_exponent_for(float smax) {
+  const int f = 4 - exponent_of(smax);
+  return f < -40 ? -40 : (f > 80 ? 80 : f);
+}
+
+__device__ __forceinline__ uint32_t hmax2u(uint32_t a, uint32_t b) {
+  const __half2 r = __hmax2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Either half of a packed non-negative fp16 pair at or above 2^15 (or NaN).
+__device__ __forceinline__ bool f16x2_reaches_2p15(uint32_t a) {
+  const __half2 h = *reinterpret_cast<const __half2*>(&a);
+  return !__hblt2(h, __float2half2_rn(32768.0f));
+}
 
 // Register split (RS): the block is laid out in warpgroups, ceil(Hkv / 4) of consumer
 // warps and one whose first two warps are the producers.  At the role branch the producer warpgroup
@@ -303,6 +344,10 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   uint32_t pphase = 0;     // dim split: phase of the pair barrier
   int xpar = 0;            // dim split: which partial-logit buffer this chunk uses
   float m_run = -INFINITY, l_run = 0.f;
+  float m_eff = -INFINITY;  // m_run - vf: the reference of the probabilities (which carry 2^vf)
+  int vf = 0;               // p s exponent of this warp's groups (warp-uniform)
+  bool vset = false;        // vf chosen for this segment
+  float s24 = 0.f;          // this row's logit scale: scale * log2(e) * 2^24 * 2^-(q~ exponent)
   // dim split: every lane of both warps of the pair arrives, then waits (bounded) for
   // the other warp.  False when the wait gave up: the warp then stops (returns), so
   // its partner gives up at its next wait and no wait is ever repeated.
@@ -315,7 +360,6 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     }
     return true;
   };
-  const float scale24 = P.scale_log2 * 16777216.0f;
 
   // Shared-memory addresses.  ldmatrix: lane 8i + r gives row r of matrix i.  K codes
   // (non-transposed) and V codes (transposed) are read as 8 tokens x one 16-byte
@@ -473,6 +517,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     if (__any_sync(0xffffffffu, grow)) {
       const float alpha = grow ? ex2(m_run - mx) : 1.0f;
       if (grow) m_run = mx;
+      m_eff = m_run - (float)vf;
       l_run *= alpha;
 #pragma unroll
       for (int grp = 0; grp < NGL; ++grp) corr[grp] *= alpha;
@@ -491,7 +536,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 #pragma unroll
     for (int jj = 0; jj < NT; ++jj)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) p[jj][e] = ex2(x[jj][e] - m_run);
+      for (int e = 0; e < 2; ++e) p[jj][e] = ex2(x[jj][e] - m_eff);
     if constexpr (NQ > 1) {
       // a row with no visible token yet in this segment keeps m_run = -inf
       if (m_run == -INFINITY)
@@ -503,8 +548,32 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     for (int jj = 1; jj < NT; ++jj) ls += p[jj][0] + p[jj][1];
     l_run += ls;
   };
+  // The p s exponent moves by d: the state (both accumulators, the denominator and
+  // the probabilities in flight) is multiplied by 2^d, exactly.
+  auto v_rescale = [&](int d, float (&p)[4][2]) {
+    const float a = pow2i(d);
+#pragma unroll
+    for (int grp = 0; grp < NGL; ++grp) {
+      corr[grp] *= a;
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[grp][mi][i] *= a;
+    }
+    l_run *= a;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      p[jj][0] *= a;
+      p[jj][1] *= a;
+    }
+    vf += d;
+    m_eff = m_run - (float)vf;
+  };
   // O^T += V^T (P S)^T over the 16 tokens of chunk kc (tiles p[jp], p[jp + 1]); offsets into corr.
-  auto pv = [&](const uint32_t sb, const int kc, const float (&p)[4][2], const int jp) {
+  // MASK: only the chunk's first nvc tokens hold data (the last unit of a sequence);
+  // the others' scale and offset are taken as 0.
+  auto pv = [&](auto mask_c, const uint32_t sb, const int kc, float (&p)[4][2], const int jp, const int nvc) {
+    constexpr bool MASK = decltype(mask_c)::value;
     uint32_t vx[2][NVC];  // half-word g of tokens 16kc + 8pp + 2t, +1; chunk c
     if constexpr (NVC == 2) {
       uint32_t r4[4];
@@ -524,30 +593,78 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
           for (int m = 0; m < 4; ++m) vx[pp][4 * cs + m] = r4[m];
         }
     }
+    auto tok_ok = [&](int pp, int e) { return !MASK || 8 * pp + 2 * t + e < nvc; };
+    if (!vset) {
+      // the segment's first chunk with a nonzero V scale sets the exponent (lanes of
+      // one t hold the same tokens, so two shuffles give the warp's maximum)
+      float sm = 0.f;
+#pragma unroll
+      for (int cm = 0; cm < NMC; ++cm)
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (tok_ok(pp, e)) {
+              const float4 mv = lds128(m_addr(sb, 3, kc, pp, e, cm));
+              sm = fmaxf(sm, fmaxf(mv.x, mv.z));
+            }
+      sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 1));
+      sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 2));
+      if (sm > 0.f) {
+        v_rescale(v_exponent_for(sm) - vf, p);
+        vset = true;
+      }
+    }
 #pragma unroll
     for (int cm = 0; cm < NMC; ++cm) {
       float4 mv[2][2];  // token 8pp + 2t + e
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) mv[pp][e] = lds128(m_addr(sb, 3, kc, pp, e, cm));
+        for (int e = 0; e < 2; ++e) {
+          mv[pp][e] = lds128(m_addr(sb, 3, kc, pp, e, cm));
+          if (!tok_ok(pp, e)) mv[pp][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      const float* p0 = p[jp];
+      const float* p1 = p[jp + 1];
+      uint32_t pbs[Tr::SPC][2];
+      auto make_pb = [&]() {
+#pragma unroll
+        for (int q = 0; q < Tr::SPC; ++q) {
+          const bool q2 = q >= Tr::SPP;  // second pair of the chunk
+          pbs[q][0] = pack_f16x2(p0[0] * (q2 ? mv[0][0].z : mv[0][0].x), p0[1] * (q2 ? mv[0][1].z : mv[0][1].x));
+          pbs[q][1] = pack_f16x2(p1[0] * (q2 ? mv[1][0].z : mv[1][0].x), p1[1] * (q2 ? mv[1][1].z : mv[1][1].x));
+        }
+      };
+      make_pb();
+      {
+        uint32_t hm = hmax2u(pbs[0][0], pbs[0][1]);
+#pragma unroll
+        for (int q = 1; q < Tr::SPC; ++q) hm = hmax2u(hm, hmax2u(pbs[q][0], pbs[q][1]));
+        if (__any_sync(0xffffffffu, f16x2_reaches_2p15(hm))) {
+          // this chunk's scales outgrew the exponent: lower it to fit them
+          float sm = 0.f;
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) sm = fmaxf(sm, fmaxf(mv[pp][e].x, mv[pp][e].z));
+          sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 1));
+          sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 2));
+          const int nf = sm > 0.f ? v_exponent_for(sm) : vf;
+          if (nf < vf) {
+            v_rescale(nf - vf, p);
+            make_pb();
+          }
+        }
+      }
 #pragma unroll
       for (int q = 0; q < Tr::SPC; ++q) {
         const int grp = Tr::SPC * cm + q;
         const bool q2 = q >= Tr::SPP;  // second pair of the chunk
-        float sv[2][2], ov[2][2];
-#pragma unroll
-        for (int pp = 0; pp < 2; ++pp)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            sv[pp][e] = q2 ? mv[pp][e].z : mv[pp][e].x;
-            ov[pp][e] = q2 ? mv[pp][e].w : mv[pp][e].y;
-          }
-        const float* p0 = p[jp];
-        const float* p1 = p[jp + 1];
-        const uint32_t pb0 = pack_f16x2(p0[0] * sv[0][0], p0[1] * sv[0][1]);
-        const uint32_t pb1 = pack_f16x2(p1[0] * sv[1][0], p1[1] * sv[1][1]);
-        corr[grp] = fmaf(p0[0], ov[0][0], fmaf(p0[1], ov[0][1], fmaf(p1[0], ov[1][0], fmaf(p1[1], ov[1][1], corr[grp]))));
+        const uint32_t pb0 = pbs[q][0], pb1 = pbs[q][1];
+        const float ov00 = q2 ? mv[0][0].w : mv[0][0].y, ov01 = q2 ? mv[0][1].w : mv[0][1].y;
+        const float ov10 = q2 ? mv[1][0].w : mv[1][0].y, ov11 = q2 ? mv[1][1].w : mv[1][1].y;
+        corr[grp] = fmaf(p0[0], ov00, fmaf(p0[1], ov01, fmaf(p1[0], ov10, fmaf(p1[1], ov11, corr[grp]))));
         if constexpr (Tr::VBITS == 4) {
           const uint32_t x01 = vx[0][grp], x23 = vx[1][grp];
           const uint32_t y01 = x01 >> 8, y23 = x23 >> 8;
@@ -585,7 +702,10 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
         for (int i = 0; i < 4; ++i) o[grp][mi][i] = 0.f;
     }
     m_run = -INFINITY;
+    m_eff = -INFINITY;
     l_run = 0.f;
+    vf = 0;
+    vset = false;
     for (int32_t u = ua; u < ue; ++u) {
       {
         const bool ok = mbar_wait_bounded(&full[s], phase, err);
@@ -633,6 +753,27 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
         // exchange since)
         if (!pair_sync()) return;
         __syncwarp();
+        // the row's q~ exponent: its largest |q~| times 2^e lands in [2^14, 2^15)
+        // (lanes 4g..4g+3 read a quarter of row g each; rows >= RW are zero)
+        float qm = 0.f;
+        if (g < RW) {
+          const float4* qr = reinterpret_cast<const float4*>(qs + g * D) + t * (D / 16);
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i) {
+            const float4 v4 = qr[i];
+            qm = fmaxf(qm, fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w))));
+          }
+        }
+        qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 1));
+        qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 2));
+        qm *= P.inv_sqrt_d;
+        int qe = 0;
+        if (qm > 0.f) {
+          qe = 14 - exponent_of(qm);
+          qe = qe < -100 ? -100 : (qe > 126 ? 126 : qe);
+        }
+        const float qf = P.inv_sqrt_d * pow2i(qe);
+        s24 = P.scale_log2 * pow2i(-qe) * 16777216.0f;
 #pragma unroll
         for (int grp = 0; grp < NGL; ++grp) {
           float tsum = 0.f;
@@ -645,7 +786,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
                 const int dd = 32 * (gofs + grp) + k_dim<Tr::KBITS>(t, ks, r, hh, d16);
-                const float qv = g < RW ? qs[g * D + dd] * P.inv_sqrt_d : 0.f;
+                const float qv = g < RW ? qs[g * D + dd] * qf : 0.f;
                 v[hh] = d16 ? qv * 0.0625f : qv;
               }
               qa[grp][ks][r] = pack_f16x2(v[0], v[1]);
@@ -666,24 +807,24 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
         if (!logits(std::integral_constant<int, 4>{}, sb, 0, x)) return;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          x[jj][0] *= scale24;
-          x[jj][1] *= scale24;
+          x[jj][0] *= s24;
+          x[jj][1] *= s24;
         }
         softmax(std::integral_constant<int, 4>{}, x, p);
-        pv(sb, 0, p, 0);
-        pv(sb, 1, p, 2);
+        pv(std::false_type{}, sb, 0, p, 0, 16);
+        pv(std::false_type{}, sb, 1, p, 2, 16);
       } else {
         for (int kc = 0; kc * 16 < nv; ++kc) {
-          float x[4][2], p[4][2];
+          float x[4][2], p[4][2] = {};
           if (!logits(std::integral_constant<int, 2>{}, sb, kc, x)) return;
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const int tk = kc * 16 + 8 * j + 2 * t;
-            x[j][0] = tk < nvr ? x[j][0] * scale24 : -INFINITY;
-            x[j][1] = tk + 1 < nvr ? x[j][1] * scale24 : -INFINITY;
+            x[j][0] = tk < nvr ? x[j][0] * s24 : -INFINITY;
+            x[j][1] = tk + 1 < nvr ? x[j][1] * s24 : -INFINITY;
           }
           softmax(std::integral_constant<int, 2>{}, x, p);
-          pv(sb, kc, p, 0);
+          pv(std::true_type{}, sb, kc, p, 0, nv - 16 * kc);
         }
       }
       mbar_arrive(&empty[s]);  // every lane: its reads of the stage are done
@@ -733,30 +874,36 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
             }
           }
       } else {
+        // the record holds the state without the p s exponent's 2^vf (exact), so the
+        // two warps of a dim-split pair, each with its own exponent, agree
+        const float iv = pow2i(-vf);
+        const float fsv[2] = {fs[0] * iv, fs[1] * iv};
         float* pe = partial_ptr(P, D, (size_t)blockIdx.x, b, qhead(he < RW ? he : 0));
         float* po = partial_ptr(P, D, (size_t)blockIdx.x, b, qhead(ho < RW ? ho : 0));
         if (he < RW && g == 0 && half == 0) {
           pe[0] = me;
-          pe[1] = le;
+          pe[1] = le * iv;
         }
         if (ho < RW && g == 0 && half == 0) {
           po[0] = mo;
-          po[1] = lo;
+          po[1] = lo * iv;
         }
 #pragma unroll
-        for (int grp = 0; grp < NGL; ++grp)
+        for (int grp = 0; grp < NGL; ++grp) {
+          const float cev = ce[grp] * iv, cov = co[grp] * iv;
 #pragma unroll
           for (int mi = 0; mi < 2; ++mi) {
             const int d0 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 0, g), d1 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 1, g);
             if (he < RW) {
-              pe[kPartialHeader + d0] = fmaf(o[grp][mi][0], fs[mi], ce[grp]);
-              pe[kPartialHeader + d1] = fmaf(o[grp][mi][2], fs[mi], ce[grp]);
+              pe[kPartialHeader + d0] = fmaf(o[grp][mi][0], fsv[mi], cev);
+              pe[kPartialHeader + d1] = fmaf(o[grp][mi][2], fsv[mi], cev);
             }
             if (ho < RW) {
-              po[kPartialHeader + d0] = fmaf(o[grp][mi][1], fs[mi], co[grp]);
-              po[kPartialHeader + d1] = fmaf(o[grp][mi][3], fs[mi], co[grp]);
+              po[kPartialHeader + d0] = fmaf(o[grp][mi][1], fsv[mi], cov);
+              po[kPartialHeader + d1] = fmaf(o[grp][mi][3], fsv[mi], cov);
             }
           }
+        }
       }
     }
     ua = ue;
