@@ -76,7 +76,8 @@ typedef struct {
   int32_t group_size;    /* values per affine group (ignored for bf16): 32, or 64 for K4/V4 with
                           * head_dim 128 or 256 (one FP32 scale/offset pair per 64 values: five
                           * bits per value, 3.2x against bf16)
-                          *   [mlx-swift-lm #142, Summary: "five effective bits per value"] */
+                          *   [mlx-swift-lm #142, Summary: K4/V4 at five bits per value,
+                          *    metadata included] */
   int32_t format;        /* pkv_format                                          */
   int32_t max_slabs;     /* capacity of the slab pointer table (>= 1)           */
   uint64_t hadamard_seed;/* signs s_i = -1 iff top bit of splitmix64(seed + i)  */
@@ -100,13 +101,22 @@ typedef struct {
   int64_t row_bytes[4];       /* bytes of one (token, head) row per tensor kind    */
 } pkv_stats;
 
-/* Create a pool with no slabs.  The allocator struct is copied.  Errors:
- * PKV_ERR_INVALID for an unsupported configuration, PKV_ERR_CUDA if the device
- * cannot be used.  Synchronous. */
+/* Create a pool with no slabs on the current device: per layer and stored tensor an
+ * empty vector of slabs, the pointer table for up to max_slabs of them, the row
+ * allocator and the device error word.  The allocator struct is copied.  *out
+ * receives the pool (owned by the caller until pkv_pool_destroy).  Errors:
+ * PKV_ERR_INVALID for an unsupported configuration (n_kv_heads outside 1..8,
+ * head_dim not 64/128/256, block_size not 32, group_size not allowed for the
+ * format), PKV_ERR_CUDA if the device cannot be used.  Synchronous.
+ *   [mlxcel #235, Proposed solution, bullet 1: the single pool tensor of a layer
+ *    becomes a vector of fixed-size slabs] */
 pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_allocator* alloc, void* stream,
                            pkv_pool** out);
 
-/* Synchronise `stream` of the last call, release every slab and the pool. */
+/* Wait for the device, then release every slab (through the pool's allocator) and
+ * the pool itself.  NULL is ignored.  Slabs are freed only here, never while the
+ * pool lives.
+ *   [mlxcel #235, Proposed solution, bullet 2: growth never frees a slab] */
 void pkv_pool_destroy(pkv_pool* pool);
 
 /* Append n_slabs fresh zeroed slabs to every layer and tensor, in one step
@@ -118,7 +128,8 @@ pkv_status pkv_append_slab(pkv_pool* pool, int n_slabs, void* stream);
 /* Take n rows from the free list (LIFO reuse of released rows, then rows of
  * appended slabs in ascending order), appending slabs when it is empty.  Each
  * returned row has reference count 1.  rows_host: n int32.
- *   [mlxcel #235, Behavioral invariants: block ids, refcounts, free-row reuse] */
+ *   [mlxcel #235, Behavioral invariants: block identities, reference counts and the
+ *    reuse of freed rows remain row-level bookkeeping] */
 pkv_status pkv_alloc_rows(pkv_pool* pool, int n, int32_t* rows_host, void* stream);
 
 /* Reference counting of rows (host bookkeeping only).  retain requires a live
@@ -166,7 +177,10 @@ pkv_status pkv_gather_visible(pkv_pool* pool, int layer, const int32_t* bt_row_d
  * sequences with Hq query heads (max_ctx is the caller's bound on any context
  * length; it is accepted for interface stability and does not change the size).
  * The workspace holds the split-K partials and per-sequence arrival counters; it
- * must be zero-filled once before its first use (the kernel leaves it reusable). */
+ * must be zero-filled once before its first use (the kernel leaves it reusable).
+ * Host only; PKV_ERR_INVALID for a NULL pool or bytes, B < 0 or Hq < 1.
+ *   [mlx-swift-lm #142, Summary: the workspace a step is guaranteed is priced on
+ *    its own, apart from storage] */
 pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int Hq, int max_ctx,
                                       size_t* bytes);
 
@@ -182,14 +196,23 @@ pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int Hq, int m
  *   out_bf16_dev:    [B, Hq, head_dim] bf16
  *   workspace_dev:   ws_bytes >= pkv_decode_workspace_bytes(B, Hq), zeroed once
  * Deterministic: bitwise identical results for identical inputs on one device.
+ * Limits: 1 <= B <= 4096 (the batch's unit prefix is staged in shared memory);
+ * n_kv_heads <= 8 (one consumer warp per kv head, fixed at pool creation);
+ * G = Hq / n_kv_heads in {1, 2, 4, 8}.
+ * Range: any finite q, K and V whose magnitudes stay within about 2^-60..2^40 (and
+ * whose logits scale * q.k are finite) are handled at the same accuracy as values
+ * near 1: the packed kernels keep their two fp16 operands (the rotated q, and the
+ * probability times the V scale) in range with power-of-two exponents that are
+ * removed exactly in fp32.  Slots of a block past a sequence's context are never
+ * read into the result, whatever bytes they hold.
  * B = 0 returns PKV_OK with no device work.  PKV_ERR_INVALID, before any work,
- * when Hq is not n_kv_heads x G with G in {1, 2, 4, 8}, scale is not finite, the
- * workspace is smaller than pkv_decode_workspace_bytes or not 256-byte aligned,
- * or q / out are not 16-byte aligned.
+ * when B > 4096, Hq is not n_kv_heads x G with G in {1, 2, 4, 8}, scale is not
+ * finite, the workspace is smaller than pkv_decode_workspace_bytes or not 256-byte
+ * aligned, or q / out are not 16-byte aligned.
  *   [mlxcel issue #2171, "one KV storage abstraction": Proposed Solution
- *    (KVCache::attend -> paged_batch_decode_attention) and Edge cases (single
- *    token, no mask); mlx-swift-lm #142: "direct attention consumes packed pages
- *    without expanding the history"] */
+ *    (KVCache::attend -> paged_batch_decode_attention) and Implementation Notes,
+ *    edge cases (single token, no mask); mlx-swift-lm #142, Summary: packed pages
+ *    are attended to directly, with no expanded copy of the history] */
 pkv_status pkv_paged_decode_attention(pkv_pool* pool, int layer, int B, int Hq,
                                       const void* q_bf16_dev, const int32_t* block_table_dev,
                                       int max_blocks, const int32_t* ctx_lens_dev, int max_ctx,
@@ -225,20 +248,82 @@ pkv_status pkv_paged_decode_attention_noalloc(pkv_pool* pool, int layer, int B, 
 
 /* Number of CTAs a decode launch uses (0 = one per SM, the default).  Changing it
  * changes the split-K partition (results agree to rounding) and the workspace
- * size.  PKV_ERR_INVALID for n < 0. */
+ * size.  PKV_ERR_INVALID for n < 0.  Host only.  (A tuning and test knob; the
+ * pages have no counterpart.) */
 pkv_status pkv_decode_set_ctas(pkv_pool* pool, int n_ctas);
 
-/* Pool statistics (host bookkeeping; no device access). */
+/* Pool statistics (host bookkeeping; no device access): slab count, the
+ * slab-append counter (one per appended slab; no slab is ever copied), row
+ * capacity and rows in use, and bytes_reserved as the sum over every slab of every
+ * layer and tensor.  PKV_ERR_INVALID for NULL arguments.
+ *   [mlxcel #235, Proposed solution, bullet 2 (the growth counter counts slab
+ *    appends) and touch point 5 (reserved bytes summed over slabs)] */
 pkv_status pkv_pool_stats(const pkv_pool* pool, pkv_stats* out);
 
-/* Device base address of slab `slab` of (layer, kind); PKV_ERR_RANGE if absent. */
+/* Device base address of slab `slab` of (layer, kind); PKV_ERR_RANGE if absent.
+ * Host only.
+ *   [mlxcel #235, touch point 4: per-slab base pointers] */
 pkv_status pkv_slab_address(const pkv_pool* pool, int layer, int kind, int slab, void** addr);
+
+/* A request's price for admission into a step: the three costs that an admission
+ * policy weighs separately.  Host only; nothing is allocated or changed.
+ *   in  new_blocks:  blocks (rows) the request needs that it does not share with a
+ *                    sequence already in the pool (e.g. ceil(tokens / 32) minus the
+ *                    blocks of a shared prefix); >= 0
+ *   in  B, Hq, n_q:  the step it joins: sequences (the request included), query
+ *                    heads, queries per sequence (1 for decode, > 1 for a chunked
+ *                    prefill of n_q tokens)
+ *   in  max_blocks:  block-table width of that step
+ *   out slabs_to_append: slabs pkv_alloc_rows(new_blocks) would append now (0
+ *                    while the free list holds enough rows), the same count
+ *                    pkv_append_slab(n) takes to presize for the span
+ *   out free_rows:   rows on the free list now
+ *   out storage_bytes: growing storage: the bytes the allocator is asked for by
+ *                    those appends (every layer and tensor of each slab, plus the
+ *                    slab's 128-byte tensor maps)
+ *   out page_bytes:  page cost: the stored bytes of the request's new blocks, every
+ *                    layer and tensor (pkv_block_record_bytes x new_blocks); this is
+ *                    space inside the pool's capacity, not a further allocation
+ *   out fixed_bytes: fixed per-request cost of a step: its block-table row
+ *                    (max_blocks int32), context length (int32), and q and output
+ *                    rows (n_q x Hq x head_dim bf16 each)
+ *   out workspace_bytes: the step's guaranteed workspace for (B, Hq, n_q,
+ *                    max_blocks): pkv_decode_workspace_bytes(B, Hq) when n_q == 1,
+ *                    else pkv_prefill_workspace_bytes(B, n_q, Hq, max_blocks)
+ * A request fits a device budget of free bytes F when storage_bytes + fixed_bytes
+ * plus the growth of the step's workspace over what the caller already holds is at
+ * most F.  Errors: PKV_ERR_INVALID for NULL pointers, negative or zero sizes, Hq
+ * not a multiple of n_kv_heads or B * n_q > 4096 with n_q > 1; PKV_ERR_RANGE when
+ * the slabs to append would exceed max_slabs (the pool can never hold the request).
+ *   [mlx-swift-lm #142, Summary: admission prices the growth of storage, the page
+ *    and fixed costs and the step's guaranteed workspace each on its own; After:
+ *    admission = storage plus guaranteed workspace; mlxcel #235, Proposed
+ *    solution, bullet 2: presize_for_span appends the slabs a span needs at once] */
+typedef struct {
+  int32_t new_blocks;
+  int32_t B;
+  int32_t Hq;
+  int32_t n_q;
+  int32_t max_blocks;
+} pkv_request;
+
+typedef struct {
+  int32_t slabs_to_append;
+  int64_t free_rows;
+  uint64_t storage_bytes;
+  uint64_t page_bytes;
+  uint64_t fixed_bytes;
+  uint64_t workspace_bytes;
+} pkv_price;
+
+pkv_status pkv_price_request(const pkv_pool* pool, const pkv_request* req, pkv_price* out);
 
 /* Storage identity check: PKV_OK if cfg describes the same stored layout as the
  * pool (format, head_dim, n_kv_heads, block_size, slab_blocks, group_size and,
  * for packed formats, hadamard_seed), else PKV_ERR_FORMAT.  Used to reject an
  * incompatible storage identity before any allocation or copy.
- *   [mlx-swift-lm #142, Summary: reject incompatible storage identities] */
+ *   [mlx-swift-lm #142, Summary: a checkpoint of another storage identity is
+ *    refused before anything is allocated] */
 pkv_status pkv_pool_check_identity(const pkv_pool* pool, const pkv_pool_config* cfg);
 
 /* Workspace bytes for pkv_paged_prefill_attention with B sequences, n_q new tokens
@@ -263,14 +348,15 @@ pkv_status pkv_prefill_workspace_bytes(const pkv_pool* pool, int B, int n_q, int
  * Errors as for pkv_paged_decode_attention; PKV_ERR_INVALID when B * n_q > 4096.
  * Asynchronous.
  *   [mlxcel #2171, Proposed Solution: attend = update the storage, then attention;
- *    mlx-swift-lm #142, Summary: direct attention consumes packed pages] */
+ *    mlx-swift-lm #142, Summary: packed pages are attended to directly] */
 pkv_status pkv_paged_prefill_attention(pkv_pool* pool, int layer, int B, int n_q, int Hq, const void* q_bf16,
                                        const int32_t* block_table, int max_blocks, const int32_t* ctx_lens,
                                        int max_ctx, float scale, void* out_bf16, void* workspace, size_t ws_bytes,
                                        void* stream);
 
 /* The pool's configuration (its storage identity plus n_layers and max_slabs), for
- * a checkpoint header.  Synchronous, host only. */
+ * a checkpoint header.  Synchronous, host only.
+ *   [mlx-swift-lm #142, After: a packed checkpoint carries its format identity] */
 pkv_status pkv_pool_get_config(const pkv_pool* pool, pkv_pool_config* out);
 
 /* Bytes of one block record: every stored byte of one block (row) of every layer,
@@ -287,9 +373,9 @@ pkv_status pkv_block_record_bytes(const pkv_pool* pool, size_t* bytes);
  * (out_bytes).  Errors: PKV_ERR_INVALID for null or misaligned pointers,
  * PKV_ERR_RANGE when out_bytes is too small; a row outside the pool sets the
  * device error word (bit 1) and its record is left unwritten.  Asynchronous.
- *   [mlxcel #235, touch point 6: serde block-content extraction localised to the
- *    row's slab by the mapping helper; mlx-swift-lm #142, Summary: complete
- *    checkpoints preserve packed bytes] */
+ *   [mlxcel #235, touch point 6: a block's content is read from the slab that holds
+ *    its row, through the shared mapping helper; mlx-swift-lm #142, Summary: a full
+ *    checkpoint keeps the packed bytes as they are] */
 pkv_status pkv_export_blocks(pkv_pool* pool, int n, const int32_t* rows_dev, void* out_dev, size_t out_bytes,
                              void* stream);
 
@@ -300,19 +386,23 @@ pkv_status pkv_export_blocks(pkv_pool* pool, int n, const int32_t* rows_dev, voi
  * n_layers differs from this pool's, PKV_ERR_FORMAT is returned before any device
  * work, so an incompatible checkpoint is rejected before anything is written.
  * Other errors as for export.  Asynchronous.
- *   [mlxcel #235, touch point 6: restore path; mlx-swift-lm #142, Summary: reject
- *    incompatible storage identities before allocation; After: exact packed
- *    checkpoint with format identity] */
+ *   [mlxcel #235, touch point 6: restore path; mlx-swift-lm #142, Summary: a
+ *    checkpoint of another storage identity is refused before anything is
+ *    allocated; After: the packed checkpoint is exact and carries its format] */
 pkv_status pkv_import_blocks(pkv_pool* pool, const pkv_pool_config* identity, int n, const int32_t* rows_dev,
                              const void* in_dev, size_t in_bytes, void* stream);
 
 /* Synchronise `stream`, read and clear the device error word.  PKV_ERR_DEVICE if it
  * was set (bits: 1 row out of range, 2 context too long, 4 slot out of range,
- * 8 wait limit reached); *word_out (optional) receives the bits. */
+ * 8 wait limit reached); *word_out (optional) receives the bits.  The kernels record
+ * errors on the device instead of returning them, so that a decode step needs no
+ * host synchronisation; the caller checks when it chooses.
+ *   [mlxcel #2171, Implementation Notes: a decode step adds no host sync] */
 pkv_status pkv_pool_check_errors(pkv_pool* pool, void* stream, int32_t* word_out);
 
 /* Static description of a status code, and the last CUDA error message seen by
- * this thread (empty if none). */
+ * this thread (empty if none).  Never NULL; the strings belong to the library.
+ * (C-ABI conveniences with no counterpart on the pages.) */
 const char* pkv_status_string(pkv_status status);
 const char* pkv_last_error(void);
 

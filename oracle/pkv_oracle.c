@@ -536,7 +536,8 @@ int oracle_decode_attention(const oracle_pool* p, int layer, int B, int Hq, cons
 }
 
 /* Causal chunked-prefill attention [ATTN, Proposed Solution: attend = update the
- * storage, then attention over it; the survey's prefill-over-paged-slabs row].
+ * storage, then attention over it; Implementation Notes, edge cases: a masked
+ * (prefill) step runs attention with a causal mask, not the single-token path].
  * Sequence b holds ctx[b] tokens, the last n_q of which are the chunk's new tokens
  * (already written); query i of the chunk (position ctx[b] - n_q + i) attends to
  * tokens [0, ctx[b] - n_q + i] of its sequence, with the same softmax(q K^T scale) V
@@ -567,7 +568,7 @@ int oracle_prefill_attention(const oracle_pool* p, int layer, int B, int n_q, in
 }
 
 /* Block record [SLAB, touch point 6 (serde block content, restore path); PACK,
- * Summary (complete checkpoints preserve packed bytes)]: every stored byte of one
+ * Summary (a full checkpoint keeps the packed bytes unchanged)]: every stored byte of one
  * block, for each layer in order and, within a layer, for each stored tensor in
  * the order K, V, K meta, V meta, the block's [block_size][n_kv_heads][row]
  * bytes as stored.  Nothing is converted. */

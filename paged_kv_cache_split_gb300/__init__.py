@@ -61,6 +61,20 @@ ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, c
 RELEASE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p)
 
 
+class Request(ctypes.Structure):
+    _fields_ = [("new_blocks", ctypes.c_int32), ("B", ctypes.c_int32), ("Hq", ctypes.c_int32),
+                ("n_q", ctypes.c_int32), ("max_blocks", ctypes.c_int32)]
+
+
+class Price(ctypes.Structure):
+    _fields_ = [("slabs_to_append", ctypes.c_int32), ("free_rows", ctypes.c_int64),
+                ("storage_bytes", ctypes.c_uint64), ("page_bytes", ctypes.c_uint64),
+                ("fixed_bytes", ctypes.c_uint64), ("workspace_bytes", ctypes.c_uint64)]
+
+    def as_dict(self):
+        return {k: int(getattr(self, k)) for k, _ in self._fields_}
+
+
 class Allocator(ctypes.Structure):
     _fields_ = [("alloc", ALLOC_FN), ("release", RELEASE_FN), ("ctx", ctypes.c_void_p)]
 
@@ -85,6 +99,7 @@ SIGNATURES = {
     "pkv_pool_stats": ([_P, ctypes.POINTER(Stats)], _I),
     "pkv_slab_address": ([_P, _I, _I, _I, ctypes.POINTER(_P)], _I),
     "pkv_pool_check_identity": ([_P, ctypes.POINTER(PoolConfig)], _I),
+    "pkv_price_request": ([_P, ctypes.POINTER(Request), ctypes.POINTER(Price)], _I),
     "pkv_pool_check_errors": ([_P, _P, ctypes.POINTER(ctypes.c_int32)], _I),
     "pkv_pool_get_config": ([_P, ctypes.POINTER(PoolConfig)], _I),
     "pkv_prefill_workspace_bytes": ([_P, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
@@ -379,6 +394,14 @@ class Pool:
         a = _P()
         _check(self._lib.pkv_slab_address(self._h, layer, kind, slab, ctypes.byref(a)), "slab_address")
         return int(a.value or 0)
+
+    def price_request(self, new_blocks: int, B: int, Hq: int, n_q: int = 1, max_blocks: int = 0) -> dict:
+        """Admission price of a request (see pkv_price_request): slabs to append, free
+        rows, and the storage, page, fixed and workspace bytes."""
+        req = Request(int(new_blocks), int(B), int(Hq), int(n_q), int(max_blocks))
+        out = Price()
+        _check(self._lib.pkv_price_request(self._h, ctypes.byref(req), ctypes.byref(out)), "price_request")
+        return out.as_dict()
 
     def check_identity(self, cfg: PoolConfig) -> bool:
         st = self._lib.pkv_pool_check_identity(self._h, ctypes.byref(cfg))

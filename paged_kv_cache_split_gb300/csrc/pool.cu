@@ -246,7 +246,8 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_allocator* allo
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaMemset(error word)"));
 
   // Fixed signed Hadamard basis: s_i = -1 iff the top bit of splitmix64(seed + i)
-  // is set (mlx-swift-lm #142, Summary: "fixed signed Hadamard basis for Q/K").
+  // is set (mlx-swift-lm #142, Summary: Q and K share one signed Hadamard basis that
+  // never changes).
   std::vector<float> signs((size_t)D);
   for (int i = 0; i < D; ++i) signs[i] = (splitmix64(cfg->hadamard_seed + (uint64_t)i) >> 63) ? -1.f : 1.f;
   e = cudaMalloc((void**)&p->signs_dev, sizeof(float) * (size_t)D);
@@ -663,6 +664,34 @@ pkv_status pkv_paged_prefill_attention(pkv_pool* p, int layer, int B, int n_q, i
   // of a sequence are read by all of its virtual sequences: normal L2 priority.
   return decode_impl(p, layer, Bv, Hq * nq, q, bt2, max_blocks, ctx2, scale, out, (uint8_t*)ws + dec_off,
                      ws_bytes - dec_off, stream, 1, nq);
+}
+
+pkv_status pkv_price_request(const pkv_pool* p, const pkv_request* r, pkv_price* out) {
+  if (!p || !r || !out || r->new_blocks < 0 || r->B < 1 || r->Hq < 1 || r->n_q < 1 || r->max_blocks < 0)
+    return PKV_ERR_INVALID;
+  if (r->Hq % p->cfg.n_kv_heads) return PKV_ERR_INVALID;
+  if (r->n_q > 1 && (int64_t)r->B * r->n_q > 4096) return PKV_ERR_INVALID;
+  const int64_t free_rows = (int64_t)p->free_rows.size();
+  const int64_t deficit = r->new_blocks > free_rows ? r->new_blocks - free_rows : 0;
+  const int64_t slabs = (deficit + p->cfg.slab_blocks - 1) / p->cfg.slab_blocks;
+  if ((int64_t)p->groups.size() + slabs > p->cfg.max_slabs) return PKV_ERR_RANGE;
+  int64_t block_bytes = 0;  // one block of one layer, every stored tensor
+  for (int k = 0; k < p->n_kinds; ++k) block_bytes += p->row_bytes[k] * kBlockTokens * p->cfg.n_kv_heads;
+  memset(out, 0, sizeof *out);
+  out->slabs_to_append = (int32_t)slabs;
+  out->free_rows = free_rows;
+  out->storage_bytes = (uint64_t)slabs * (uint64_t)p->group_bytes;
+  out->page_bytes = (uint64_t)r->new_blocks * (uint64_t)block_bytes * (uint64_t)p->cfg.n_layers;
+  out->fixed_bytes = (uint64_t)r->max_blocks * 4u + 4u + 2ull * (uint64_t)r->n_q * (uint64_t)r->Hq *
+                                                          (uint64_t)p->cfg.head_dim * 2u;
+  if (r->n_q == 1) {
+    out->workspace_bytes = workspace_bytes(p, r->B, r->Hq);
+  } else {
+    size_t a, b, c, t;
+    prefill_layout(p, r->B, r->n_q, r->Hq, r->max_blocks, &a, &b, &c, &t);
+    out->workspace_bytes = t;
+  }
+  return PKV_OK;
 }
 
 pkv_status pkv_pool_stats(const pkv_pool* p, pkv_stats* out) {

@@ -151,3 +151,64 @@ def test_device_error_word_reports_and_skips():
     out = p.paged_decode_attention(0, q, to_dev_i32([[1, 2]]), to_dev_i32([65]), 0.125)
     assert p.check_errors() & pkv.ERR_CTX
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("fmt,D,hkv,gs", [("bf16", 128, 8, 32), ("k4v4", 128, 8, 32), ("k8v4", 64, 8, 32),
+                                          ("k8v8", 256, 4, 32), ("k4v4", 256, 4, 64)])
+def test_price_request_closed_forms_and_growth(fmt, D, hkv, gs):
+    """The admission price (mlx-swift-lm PR #142, Summary: storage growth, page and
+    fixed costs and the step's guaranteed workspace priced apart): each figure
+    against its closed form, and the predicted growth against what alloc_rows then
+    asks of the allocator."""
+    requested = []
+
+    def alloc(ctx, n, stream):
+        t = torch.empty(n, dtype=torch.uint8, device="cuda")
+        requested.append(n)
+        keep[t.data_ptr()] = t
+        return t.data_ptr()
+
+    def release(ctx, ptr, stream):
+        keep.pop(ptr, None)
+
+    keep = {}
+    a = pkv.Allocator(pkv.ALLOC_FN(alloc), pkv.RELEASE_FN(release), None)
+    L, Hq = 3, 2 * hkv
+    g = pkv.Pool(L, hkv, D, fmt, hadamard_seed=1, max_slabs=6, allocator=a, group_size=gs)
+    rb = g.row_bytes
+    block = sum(32 * hkv * r for r in rb)          # one block of one layer, every tensor
+    slab_data = 32 * block * L                     # 32 blocks per slab, every layer
+    group = -(-slab_data // 128) * 128 + L * len(rb) * 128  # + one 128-byte tensor map per (layer, tensor)
+    pr = g.price_request(40, B=4, Hq=Hq, n_q=1, max_blocks=64)
+    assert pr["slabs_to_append"] == 2 and pr["free_rows"] == 0
+    assert pr["storage_bytes"] == 2 * group
+    assert pr["page_bytes"] == 40 * block * L == 40 * g.block_record_bytes()
+    assert pr["fixed_bytes"] == 64 * 4 + 4 + 2 * Hq * D * 2
+    assert pr["workspace_bytes"] == g.decode_workspace_bytes(4, Hq)
+    before = g.stats()
+    g.alloc_rows(40)
+    after = g.stats()
+    assert after["n_slabs"] - before["n_slabs"] == 2
+    assert sum(requested) == pr["storage_bytes"]
+    assert after["bytes_reserved"] - before["bytes_reserved"] == 2 * slab_data
+    # 24 rows left on the free list
+    p20 = g.price_request(20, B=4, Hq=Hq)
+    assert p20["slabs_to_append"] == 0 and p20["storage_bytes"] == 0 and p20["free_rows"] == 24
+    p30 = g.price_request(30, B=4, Hq=Hq)
+    assert p30["slabs_to_append"] == 1 and p30["storage_bytes"] == group
+    # a chunked-prefill step prices the prefill workspace
+    pp = g.price_request(10, B=2, Hq=Hq, n_q=8, max_blocks=16)
+    assert pp["workspace_bytes"] == g.prefill_workspace_bytes(2, 8, Hq, 16)
+    assert pp["fixed_bytes"] == 16 * 4 + 4 + 2 * 8 * Hq * D * 2
+    # more slabs than the table holds: the pool can never take the request
+    with pytest.raises(pkv.PkvError) as e:
+        g.price_request(24 + 4 * 32 + 1, B=1, Hq=Hq)
+    assert e.value.status == pkv.PKV_ERR_RANGE
+    g.price_request(24 + 4 * 32, B=1, Hq=Hq)
+    for bad in (dict(new_blocks=-1, B=1, Hq=Hq), dict(new_blocks=1, B=0, Hq=Hq),
+                dict(new_blocks=1, B=1, Hq=Hq + 1), dict(new_blocks=1, B=1024, Hq=Hq, n_q=8)):
+        with pytest.raises(pkv.PkvError) as e:
+            g.price_request(**bad)
+        assert e.value.status == pkv.PKV_ERR_INVALID
+    assert g.stats()["n_slabs"] == 2  # pricing changes nothing
+    g.close()

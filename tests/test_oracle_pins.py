@@ -233,8 +233,9 @@ def _fill(pool, layer, rows_per_seq, lens, data):
 
 @pytest.mark.parametrize("fmt", [FMT_BF16, FMT_K4V4, FMT_K8V4, FMT_K8V8])
 def test_fragmented_equals_contiguous(fmt):
-    """Acceptance criterion of mlxcel #235: gather over an interleaved (fragmented) block
-    table is byte-identical to the contiguous layout, for spans crossing slabs."""
+    """Acceptance criteria of mlxcel #235: a gather through a fragmented block table
+    (freed rows reused, sequences interleaved) gives the same bytes as the contiguous
+    layout, for spans crossing slabs."""
     H, D = 2, 64
     lens = [700, 1500, 33]
     rng = wl.rng_for(11, fmt)

@@ -1,8 +1,9 @@
 """Pins of the oracle's block records (export / import), CPU only.
 
 The record layout is fixed by the serde touch point of the chunked-slab issue
-(block content localised to the row's slab) and the packed-formats PR's "complete
-checkpoints preserve packed bytes": a record is every stored byte of one block,
+(a block's content is read and written within the slab that holds its row) and
+the packed-formats PR's Summary (a full checkpoint keeps the packed bytes as they
+are): a record is every stored byte of one block,
 layer-major, then K, V, K meta, V meta.  The pins tie the oracle's export to its
 already-pinned per-block reads and gathers, and check the size by closed form.
 """
