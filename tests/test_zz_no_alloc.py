@@ -4,9 +4,11 @@ Some callers cannot allocate device memory for the decode workspace (a serving l
 that reserved all of its memory at start-up, a plugin whose host framework owns the
 allocator).  pkv_paged_decode_attention_noalloc serves them from a fixed scratch
 array inside the library.  This file checks, through the C ABI, that two calls in a
-row give the same results as the regular entry point with a caller workspace, within
-the parity tolerance used everywhere else, and that oversize requests are refused.
-It is named so that pytest collects it last."""
+row give the same results as the regular entry point with a caller workspace, and
+that oversize requests are refused.  Both entry points run the same kernel over the
+same split-K partition, and decode is deterministic, so the outputs must agree bit
+for bit (a stale counter or partial left over from the first call would show up as
+a difference).  It is named so that pytest collects it last."""
 import ctypes
 
 import numpy as np
@@ -14,7 +16,7 @@ import pytest
 
 import paged_kv_cache_split_gb300 as pkv
 from paged_kv_cache_split_gb300 import workloads as wl
-from tests.harness import bf16_dev_to_f64, compare, fill, make_pools, to_dev_bf16, to_dev_i32
+from tests.harness import fill, make_pools, to_dev_bf16, to_dev_i32
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -47,11 +49,12 @@ def test_noalloc_matches_workspace_entry_point(make):
     ctx = to_dev_i32(w.ctx())
     for layer in range(w.n_layers):
         q = to_dev_bf16(w.q(layer))
-        ref = bf16_dev_to_f64(g.paged_decode_attention(layer, q, bt, ctx, w.scale, max_ctx=max(w.lens)))
-        first = bf16_dev_to_f64(_noalloc(g, layer, q, bt, ctx, w.scale, max(w.lens)))
-        second = bf16_dev_to_f64(_noalloc(g, layer, q, bt, ctx, w.scale, max(w.lens)))
-        compare(first, ref, f"{w.name} layer {layer}, first call")
-        compare(second, ref, f"{w.name} layer {layer}, second call")
+        ref = g.paged_decode_attention(layer, q, bt, ctx, w.scale, max_ctx=max(w.lens))
+        first = _noalloc(g, layer, q, bt, ctx, w.scale, max(w.lens))
+        second = _noalloc(g, layer, q, bt, ctx, w.scale, max(w.lens))
+        torch.cuda.synchronize()
+        assert torch.equal(first.view(torch.int16), ref.view(torch.int16)), f"{w.name} layer {layer}, first call"
+        assert torch.equal(second.view(torch.int16), ref.view(torch.int16)), f"{w.name} layer {layer}, second call"
     assert g.check_errors() == 0
 
 
