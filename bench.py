@@ -123,6 +123,28 @@ def dist_barrier(world: int):
         dist.barrier()
 
 
+def timed_steps(run, steps: int, stream):
+    """Run `steps` steps on `stream` with a CUDA event after each.  Returns the total
+    time (first event to last) and the per-step times, in ms."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        run()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return ev[0].elapsed_time(ev[steps]), [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+
+
+def step_stats(per_ms):
+    """Distribution of per-step times (ms): median, 10th and 90th percentiles."""
+    a = np.asarray(per_ms, np.float64)
+    if a.size == 0:
+        return None
+    return {"median": round(float(np.median(a)), 5), "p10": round(float(np.percentile(a, 10)), 5),
+            "p90": round(float(np.percentile(a, 90)), 5), "n": int(a.size)}
+
+
 # ---------------------------------------------------------------------------
 # clocks (nvidia-smi sampled in the background during the timed region)
 # ---------------------------------------------------------------------------
@@ -224,11 +246,11 @@ def ncu_traffic(workload: str):
 
 class OracleRun:
     """The oracle on one layer of the workload (sequences 0..n-1), using every core of
-    this process's affinity."""
+    this process's affinity (or `threads` of them)."""
 
-    def __init__(self, w, max_seqs=None):
+    def __init__(self, w, max_seqs=None, threads=None):
         import oracle
-        self.cores = len(os.sched_getaffinity(0))
+        self.cores = threads or len(os.sched_getaffinity(0))
         self.seqs = list(range(w.B if max_seqs is None else min(max_seqs, w.B)))
         o = oracle.OraclePool(1, w.Hkv, w.D, w.fmt, seed=w.hadamard_seed, group_size=w.group)
         o.reserve_rows(w.rows_used)
@@ -254,9 +276,9 @@ class OracleRun:
                 f"all {w.Hq} query heads; median of {runs} runs")
 
 
-def oracle_sample(w, budget_s: float = 10.0, max_seqs=None):
+def oracle_sample(w, budget_s: float = 10.0, max_seqs=None, threads=None):
     """Time the oracle until `budget_s` of CPU work (at least one run)."""
-    r = OracleRun(w, max_seqs)
+    r = OracleRun(w, max_seqs, threads)
     times = []
     t_end = time.perf_counter() + budget_s
     while True:
@@ -392,15 +414,9 @@ def run_gpu(args, rank, world, local):
         torch.cuda.synchronize()
         dist_barrier(world)
         torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(args.steps):
-            run()
-        t1.record(stream)
-        torch.cuda.synchronize()
+        total, per_step = timed_steps(run, args.steps, stream)
         dist_barrier(world)
-        ms_step = t0.elapsed_time(t1) / args.steps
+        ms_step = total / args.steps
         # end-to-end, through the public API with host buffers
         e2e_steps(max(2, args.warmup))
         torch.cuda.synchronize()
@@ -437,6 +453,7 @@ def run_gpu(args, rank, world, local):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
+        "step_ms": step_stats(per_step),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -623,6 +640,7 @@ def run_gpu_mixed(args, rank, world, local):
     wreps = max(1, math.ceil(args.warmup / STEPS_PER_REP))
     sampler = ClockSampler(local)
     t_dev, t_e2e, nbytes, launches, h2d, d2h = 0.0, 0.0, 0, 0, 0, 0
+    per_step = []
     with sampler:
         for r in range(wreps + reps):
             timed = r >= wreps
@@ -630,20 +648,15 @@ def run_gpu_mixed(args, rank, world, local):
                 mr.setup_rep()
                 dist_barrier(world)
                 torch.cuda.synchronize()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for i in range(STEPS_PER_REP):
-                    mr.run_step(i, e2e=e2e)
-                e1.record(stream)
-                torch.cuda.synchronize()
+                it = iter(range(STEPS_PER_REP))
+                ms, per = timed_steps(lambda: mr.run_step(next(it), e2e=e2e), STEPS_PER_REP, stream)
                 dist_barrier(world)
                 if timed:
-                    ms = e0.elapsed_time(e1)
                     if e2e:
                         t_e2e += ms
                     else:
                         t_dev += ms
+                        per_step += per
                         nbytes += sum(mr.step_bytes(i) for i in range(STEPS_PER_REP))
                         launches += sum(mr.launches(i) for i in range(STEPS_PER_REP))
                         io = [mr.h2d_d2h(i) for i in range(STEPS_PER_REP)]
@@ -668,6 +681,7 @@ def run_gpu_mixed(args, rank, world, local):
         "steps": nsteps,
         "warmup": wreps * STEPS_PER_REP,
         "ms_per_step": round(ms_step, 5),
+        "step_ms": step_stats(per_step),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -806,14 +820,9 @@ def run_gpu_blocks(args, rank, world, local):
             step()
         torch.cuda.synchronize()
         dist_barrier(world)
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(args.steps):
-            step()
-        t1.record(stream)
-        torch.cuda.synchronize()
+        total, per_step = timed_steps(step, args.steps, stream)
         dist_barrier(world)
-        ms_step = t0.elapsed_time(t1) / args.steps
+        ms_step = total / args.steps
         for _ in range(max(1, args.warmup)):
             e2e_step()
         torch.cuda.synchronize()
@@ -833,6 +842,7 @@ def run_gpu_blocks(args, rank, world, local):
     peak, peak_src = measured_peak()
     res = {"metric": "block export: achieved HBM GB/s (read + write bytes)", "value": round(value, 1), "unit": "GB/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+           "step_ms": step_stats(per_step),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
            "data": "synthetic (seeded N(0,1) bf16 K/V; no model weights)",
            "config": {"workload": f"block export: {blocks.size} blocks x {pool.block_record_bytes()} B records "
@@ -948,14 +958,9 @@ def run_gpu_prefill(args, rank, world, local):
             graph.replay()
         torch.cuda.synchronize()
         dist_barrier(world)
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        t1.record(stream)
-        torch.cuda.synchronize()
+        total, per_step = timed_steps(graph.replay, args.steps, stream)
         dist_barrier(world)
-        ms_step = t0.elapsed_time(t1) / args.steps
+        ms_step = total / args.steps
         for _ in range(max(1, args.warmup)):
             e2e_step()
         torch.cuda.synchronize()
@@ -979,7 +984,8 @@ def run_gpu_prefill(args, rank, world, local):
     launch_us = ms_step * 1e3 / w.n_layers
     res = {"metric": "chunked prefill attention: achieved HBM GB/s (K/V of the visible context once), query tokens/s",
            "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-           "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "ms_per_step": round(ms_step, 5), "step_ms": step_stats(per_step), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None,
            "dtype": "f32", "data": "synthetic (seeded N(0,1) bf16 K/V and q; no model weights)",
            "config": {"workload": f"chunked prefill: {describe(w)}; the last {n_q} tokens of each sequence are the chunk",
                       "global_batch": w.B * world, "seq_len": max(w.lens), "layers": w.n_layers,
@@ -997,13 +1003,52 @@ def run_gpu_prefill(args, rank, world, local):
     return res
 
 
+DEFAULT_WORKLOAD = "qwen3-0.6b"
+# Sub-records of the default line: every other configuration measured in the same
+# process (same box, same clock sampler conventions), each with its own steps.
+EXTRA_WORKLOADS = ["qwen3-1.7b-k4v4", "qwen3-1.7b-k4v4-g64", "llama-3.2-1b-k8v4", "llama-3.2-1b-k8v8",
+                   "d256-mixed", "prefill-qwen3-0.6b", "prefill-qwen3-1.7b-k4v4"]
+EXTRA_KEYS = ("metric", "value", "unit", "ms_per_step", "step_ms", "steps", "warmup", "pct_of_nominal_8tbs",
+              "kv_tokens_per_s", "query_tokens_per_s", "roofline", "e2e", "gpu_launches", "clocks")
+
+
+def run_extras(args, rank, world, local):
+    """Measure EXTRA_WORKLOADS one after another (pools freed in between) with the
+    default line's warm-up and at most 100 timed steps each (32 for the mixed
+    workload, whose repetitions start from a fresh setup)."""
+    import gc
+    import torch
+    out = []
+    for name in EXTRA_WORKLOADS:
+        a = argparse.Namespace(**vars(args))
+        a.workload = name
+        a.layers = 0
+        a.steps = min(args.steps, 32 if name == MIXED else 100)
+        if name == MIXED:
+            r, _ = run_gpu_mixed(a, rank, world, local)
+        elif name in (PREFILL, PREFILL_PACKED):
+            r = run_gpu_prefill(a, rank, world, local)
+        else:
+            r, _ = run_gpu(a, rank, world, local)
+        rec = {"workload": name, "config": r["config"]["workload"]}
+        rec.update({k: r[k] for k in EXTRA_KEYS if k in r})
+        out.append(rec)
+        del r
+        gc.collect()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
-    ap.add_argument("--workload", default="qwen3-0.6b")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="with the default workload, skip the other workloads' sub-records")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
@@ -1135,10 +1180,16 @@ def main():
         return
 
     res, w = run_gpu(args, rank, world, local)
+    if args.workload == DEFAULT_WORKLOAD and not args.no_extra:
+        res["extra"] = run_extras(args, rank, world, local)
     if rank == 0:
         if not args.no_cpu_baseline:
             cb = oracle_sample(w, budget_s=10.0, max_seqs=w.B)
             res["cpu_baseline"] = {k: (round(v, 5) if isinstance(v, float) else v) for k, v in cb.items()}
+            one = oracle_sample(w, budget_s=6.0, max_seqs=w.B, threads=1)
+            res["cpu_baseline"]["single_thread"] = {
+                "value": round(one["value"], 5), "unit": one["unit"], "cores": 1,
+                "kv_tokens_per_s": round(one["kv_tokens_per_s"], 1), "sample": one["sample"]}
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
