@@ -199,12 +199,13 @@ pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int Hq, int m
  * Limits: 1 <= B <= 4096 (the batch's unit prefix is staged in shared memory);
  * n_kv_heads <= 8 (one consumer warp per kv head, fixed at pool creation);
  * G = Hq / n_kv_heads in {1, 2, 4, 8}.
- * Range: any finite q, K and V whose magnitudes stay within about 2^-60..2^40 (and
- * whose logits scale * q.k are finite) are handled at the same accuracy as values
- * near 1: the packed kernels keep their two fp16 operands (the rotated q, and the
- * probability times the V scale) in range with power-of-two exponents that are
- * removed exactly in fp32.  Slots of a block past a sequence's context are never
- * read into the result, whatever bytes they hold.
+ * Range: q and K of any magnitude whose logits (scale * q.k) are finite in fp32
+ * (|q| below 2^100), and V of magnitudes within about 2^-50..2^40, are handled at
+ * the same accuracy as values near 1: the packed kernels keep their 16-bit tensor
+ * operands in range with powers of two that are removed exactly in fp32 (the
+ * rotated q per tile row, in fp16; the probabilities times the V scales with a fixed
+ * 2^64, in bf16).  Slots of a block past a sequence's context are never read into
+ * the result, whatever bytes they hold.
  * B = 0 returns PKV_OK with no device work.  PKV_ERR_INVALID, before any work,
  * when B > 4096, Hq is not n_kv_heads x G with G in {1, 2, 4, 8}, scale is not
  * finite, the workspace is smaller than pkv_decode_workspace_bytes or not 256-byte

@@ -46,10 +46,12 @@
 //    scale carries 2^-e.
 //  * p s uses an exponent f shared by all of a warp's groups: the softmax works
 //    with the reference max m - f, so every probability (and with it the running
-//    denominator and both accumulators) carries 2^f.  f is set from the first chunk
-//    with a nonzero V scale, so that its largest s 2^f lies in [2^4, 2^5), and is
-//    lowered (the state multiplied by the matching power of two) when a chunk's
-//    products would reach 2^15.  Partial records store the state with 2^f removed.
+//    denominator and both accumulators) carries 2^f.  Before the products of a
+//    chunk's groups are formed, their V scales are compared with 2^(15 - f) (p 2^f
+//    never exceeds 2^f): the first nonzero scale of a segment, or one at or above
+//    that bound, sets f from the chunk's largest scale s so that s 2^f lies in
+//    [2^4, 2^5), and the state is multiplied by the matching power of two.  Partial
+//    records store the state with 2^f removed.
 // A token past the context (in the last unit of a sequence) gets probability 0
 // and its V scale and offset are replaced by 0 before they meet it, so stale
 // non-finite bytes in unused slots of a block never reach the output.
@@ -191,16 +193,6 @@ __device__ __forceinline__ int v_exponent_for(float smax) {
   return f < -40 ? -40 : (f > 80 ? 80 : f);
 }
 
-__device__ __forceinline__ uint32_t hmax2u(uint32_t a, uint32_t b) {
-  const __half2 r = __hmax2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-// Either half of a packed non-negative fp16 pair at or above 2^15 (or NaN).
-__device__ __forceinline__ bool f16x2_reaches_2p15(uint32_t a) {
-  const __half2 h = *reinterpret_cast<const __half2*>(&a);
-  return !__hblt2(h, __float2half2_rn(32768.0f));
-}
 
 // Register split (RS): the block is laid out in warpgroups, ceil(Hkv / 4) of consumer
 // warps and one whose first two warps are the producers.  At the role branch the producer warpgroup
@@ -346,7 +338,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   float m_run = -INFINITY, l_run = 0.f;
   float m_eff = -INFINITY;  // m_run - vf: the reference of the probabilities (which carry 2^vf)
   int vf = 0;               // p s exponent of this warp's groups (warp-uniform)
-  bool vset = false;        // vf chosen for this segment
+  float vlim = 0.f;         // V scales at or above this take p s 2^vf to 2^15 (below 2^-100: vf not chosen yet)
   float s24 = 0.f;          // this row's logit scale: scale * log2(e) * 2^24 * 2^-(q~ exponent)
   // dim split: every lane of both warps of the pair arrives, then waits (bounded) for
   // the other warp.  False when the wait gave up: the warp then stops (returns), so
@@ -568,6 +560,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     }
     vf += d;
     m_eff = m_run - (float)vf;
+    vlim = pow2i(15 - vf);
   };
   // O^T += V^T (P S)^T over the 16 tokens of chunk kc (tiles p[jp], p[jp + 1]); offsets into corr.
   // MASK: only the chunk's first nvc tokens hold data (the last unit of a sequence);
@@ -594,27 +587,6 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
         }
     }
     auto tok_ok = [&](int pp, int e) { return !MASK || 8 * pp + 2 * t + e < nvc; };
-    if (!vset) {
-      // the segment's first chunk with a nonzero V scale sets the exponent (lanes of
-      // one t hold the same tokens, so two shuffles give the warp's maximum)
-      float sm = 0.f;
-#pragma unroll
-      for (int cm = 0; cm < NMC; ++cm)
-#pragma unroll
-        for (int pp = 0; pp < 2; ++pp)
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-            if (tok_ok(pp, e)) {
-              const float4 mv = lds128(m_addr(sb, 3, kc, pp, e, cm));
-              sm = fmaxf(sm, fmaxf(mv.x, mv.z));
-            }
-      sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 1));
-      sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 2));
-      if (sm > 0.f) {
-        v_rescale(v_exponent_for(sm) - vf, p);
-        vset = true;
-      }
-    }
 #pragma unroll
     for (int cm = 0; cm < NMC; ++cm) {
       float4 mv[2][2];  // token 8pp + 2t + e
@@ -625,43 +597,25 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
           mv[pp][e] = lds128(m_addr(sb, 3, kc, pp, e, cm));
           if (!tok_ok(pp, e)) mv[pp][e] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-      const float* p0 = p[jp];
-      const float* p1 = p[jp + 1];
-      uint32_t pbs[Tr::SPC][2];
-      auto make_pb = [&]() {
-#pragma unroll
-        for (int q = 0; q < Tr::SPC; ++q) {
-          const bool q2 = q >= Tr::SPP;  // second pair of the chunk
-          pbs[q][0] = pack_f16x2(p0[0] * (q2 ? mv[0][0].z : mv[0][0].x), p0[1] * (q2 ? mv[0][1].z : mv[0][1].x));
-          pbs[q][1] = pack_f16x2(p1[0] * (q2 ? mv[1][0].z : mv[1][0].x), p1[1] * (q2 ? mv[1][1].z : mv[1][1].x));
-        }
-      };
-      make_pb();
       {
-        uint32_t hm = hmax2u(pbs[0][0], pbs[0][1]);
-#pragma unroll
-        for (int q = 1; q < Tr::SPC; ++q) hm = hmax2u(hm, hmax2u(pbs[q][0], pbs[q][1]));
-        if (__any_sync(0xffffffffu, f16x2_reaches_2p15(hm))) {
-          // this chunk's scales outgrew the exponent: lower it to fit them
-          float sm = 0.f;
-#pragma unroll
-          for (int pp = 0; pp < 2; ++pp)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) sm = fmaxf(sm, fmaxf(mv[pp][e].x, mv[pp][e].z));
-          sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 1));
+        // the chunk's largest V scale of these groups against the exponent's bound
+        const float sm4 = fmaxf(fmaxf(fmaxf(mv[0][0].x, mv[0][0].z), fmaxf(mv[0][1].x, mv[0][1].z)),
+                                fmaxf(fmaxf(mv[1][0].x, mv[1][0].z), fmaxf(mv[1][1].x, mv[1][1].z)));
+        if (__any_sync(0xffffffffu, sm4 >= vlim && sm4 > 0.f)) {
+          float sm = fmaxf(sm4, __shfl_xor_sync(0xffffffffu, sm4, 1));
           sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 2));
-          const int nf = sm > 0.f ? v_exponent_for(sm) : vf;
-          if (nf < vf) {
-            v_rescale(nf - vf, p);
-            make_pb();
-          }
+          const int nf = v_exponent_for(sm);
+          if (vlim < 1e-30f || nf < vf) v_rescale(nf - vf, p);
         }
       }
+      const float* p0 = p[jp];
+      const float* p1 = p[jp + 1];
 #pragma unroll
       for (int q = 0; q < Tr::SPC; ++q) {
         const int grp = Tr::SPC * cm + q;
         const bool q2 = q >= Tr::SPP;  // second pair of the chunk
-        const uint32_t pb0 = pbs[q][0], pb1 = pbs[q][1];
+        const uint32_t pb0 = pack_f16x2(p0[0] * (q2 ? mv[0][0].z : mv[0][0].x), p0[1] * (q2 ? mv[0][1].z : mv[0][1].x));
+        const uint32_t pb1 = pack_f16x2(p1[0] * (q2 ? mv[1][0].z : mv[1][0].x), p1[1] * (q2 ? mv[1][1].z : mv[1][1].x));
         const float ov00 = q2 ? mv[0][0].w : mv[0][0].y, ov01 = q2 ? mv[0][1].w : mv[0][1].y;
         const float ov10 = q2 ? mv[1][0].w : mv[1][0].y, ov11 = q2 ? mv[1][1].w : mv[1][1].y;
         corr[grp] = fmaf(p0[0], ov00, fmaf(p0[1], ov01, fmaf(p1[0], ov10, fmaf(p1[1], ov11, corr[grp]))));
@@ -705,7 +659,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     m_eff = -INFINITY;
     l_run = 0.f;
     vf = 0;
-    vset = false;
+    vlim = 0.f;
     for (int32_t u = ua; u < ue; ++u) {
       {
         const bool ok = mbar_wait_bounded(&full[s], phase, err);

@@ -3,9 +3,12 @@
 Each case builds the full pool (every sequence, every layer, the full context
 lengths, the same block tables) and decodes every sequence with the same calls the
 benchmark makes; the oracle then recomputes a sample of sequences (and layers) one
-by one.  Sequences outside the sample keep whatever their rows hold (zeros of fresh
-slabs, or device-generated data) since only the sample is compared.  Bit-exact
-checks (gather bytes, codes, scale/offset bit patterns) run on the sample too."""
+by one.  In the compared layers every sequence holds its seeded data (so every CTA
+of the launch streams real packed groups, not zeros); the oracle is given only the
+sample.  Layers that are not compared hold device-generated N(0,1) data.  The sample
+spreads over the CTA range (first, last, shortest, longest and sequences between,
+whose segments start and end inside CTAs).  Bit-exact checks (gather bytes, codes,
+scale/offset bit patterns) run on the sample too."""
 import numpy as np
 import pytest
 
@@ -48,16 +51,36 @@ def _gather_equal(w, g, o, layer, olayer, seqs):
             assert np.array_equal(x, y), f"{w.name}: gather mismatch, seq {b} kind {kind}"
 
 
+def _device_fill(w, g, layer):
+    """Device-generated N(0,1) bf16 K/V for every sequence of `layer`."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(7000 + layer)
+    r = np.concatenate([w.token_placement(b)[0] for b in range(w.B)])
+    s = np.concatenate([w.token_placement(b)[1] for b in range(w.B)])
+    k = torch.randn((r.size, w.Hkv, w.D), generator=gen, device="cuda").to(torch.bfloat16)
+    v = torch.randn((r.size, w.Hkv, w.D), generator=gen, device="cuda").to(torch.bfloat16)
+    g.write_block(layer, to_dev_i32(r), to_dev_i32(s), k, v)
+
+
 def _full_case(w, sample, layers):
-    """Full pool of `w`; host data for `sample` in `layers`; all layers decoded with one
-    shared workspace in layer order (the benchmark's step); sample compared."""
+    """Full pool of `w`: seeded host data for every sequence of `layers` (the oracle
+    gets `sample`), device data elsewhere; all layers decoded with one shared
+    workspace in layer order (the benchmark's step); sample compared."""
     g = pkv.Pool(w.n_layers, w.Hkv, w.D, FMT[w.fmt], hadamard_seed=w.hadamard_seed,
                  max_slabs=(w.rows_used + 31) // 32 + 8, group_size=w.group)
     g.reserve_rows(w.rows_used)
     o = oracle.OraclePool(len(layers), w.Hkv, w.D, w.fmt, seed=w.hadamard_seed, group_size=w.group)
     o.reserve_rows(w.rows_used)
-    for i, layer in enumerate(layers):
-        _write_seqs(w, g, o, layer, i, sample)
+    rest = [b for b in range(w.B) if b not in sample]
+    for layer in range(w.n_layers):
+        if layer in layers:
+            i = layers.index(layer)
+            _write_seqs(w, g, o, layer, i, sample)
+            for c in range(0, len(rest), 4):
+                _write_seqs(w, g, None, layer, i, rest[c:c + 4])
+        else:
+            _device_fill(w, g, layer)
+    torch.cuda.synchronize()
     dev = torch.device("cuda")
     bt = to_dev_i32(w.block_table())
     ctx = to_dev_i32(w.ctx())
@@ -86,29 +109,43 @@ def test_qwen3_0_6b_full_size():
 
 
 def test_qwen3_1_7b_k4v4_full_size_sampled():
-    """16 x 16384 K4/V4 with outliers: three sequences compared."""
+    """16 x 16384 K4/V4 with outliers, every sequence holding data: eight sequences
+    spread over the launch compared (each spans about nine CTAs)."""
     w = wl.qwen3_1_7b_k4v4()
-    _full_case(w, sample=[0, 7, w.B - 1], layers=[0])
+    _full_case(w, sample=[0, 2, 5, 7, 9, 11, 13, w.B - 1], layers=[0])
 
 
 def test_qwen3_1_7b_k4v4_groups_of_64_full_size_sampled():
-    """16 x 16384 in the five-bit K4/V4 layout: two sequences compared."""
+    """16 x 16384 in the five-bit K4/V4 layout: eight sequences compared."""
     w = wl.qwen3_1_7b_k4v4_g64()
-    _full_case(w, sample=[0, w.B - 1], layers=[0])
+    _full_case(w, sample=[0, 3, 4, 6, 8, 10, 12, w.B - 1], layers=[0])
+
+
+def _spread_sample(lens, n=8):
+    """First, last, shortest and longest sequence, plus others evenly spaced."""
+    lens = np.asarray(lens)
+    pick = {0, len(lens) - 1, int(lens.argmin()), int(lens.argmax())}
+    for x in np.linspace(0, len(lens) - 1, n + 2)[1:-1]:
+        if len(pick) >= n:
+            break
+        pick.add(int(round(x)))
+    return sorted(pick)
 
 
 @pytest.mark.parametrize("fmt", [wl.FMT_K8V4, wl.FMT_K8V8])
 def test_llama_1b_full_size_sampled(fmt):
-    """64 ragged sequences in [512, 8192]: the shortest, the longest and two others."""
+    """64 ragged sequences in [512, 8192], every one holding data: the shortest, the
+    longest, the first, the last and four between compared."""
     w = wl.llama_1b(fmt)
-    lens = np.asarray(w.lens)
-    sample = sorted({int(lens.argmin()), int(lens.argmax()), 0, w.B - 1})
+    sample = _spread_sample(w.lens)
+    assert len(sample) >= 8
     _full_case(w, sample=sample, layers=[0])
 
 
 def test_mixed_d256_full_size_sampled():
-    """B=32 up to 32768 tokens, two pools; three steps of per-sequence writes and
-    copy-on-write; per pool a group leader and a sharer compared after each step."""
+    """B=32 up to 32768 tokens, two pools, every sequence holding data; three steps of
+    per-sequence writes and copy-on-write; per pool a group leader and a sharer
+    compared after each step."""
     m = wl.MixedWorkload()
     gp, op, samples = [], [], []
     for pi, P in enumerate(m.pools):
@@ -119,30 +156,22 @@ def test_mixed_d256_full_size_sampled():
         g.reserve_rows(P.next_row)
         o.reserve_rows(P.next_row)
         sample = [0, 3 * m.group_size + 1]
-        # every group's shared prefix (from its leader's stream), then the sample's own tokens
-        for gi in range(len(P.prefix_rows)):
-            lead = gi * m.group_size
-            k, v = m.initial_kv(pi, lead)
-            t = np.arange(m.prefix)
-            r = np.asarray(P.rows[lead], np.int32)[t // 32]
-            s = (t % 32).astype(np.int32)
-            if lead in sample:
-                t = np.arange(P.lens[lead])
-                r = np.asarray(P.rows[lead], np.int32)[t // 32]
-                s = (t % 32).astype(np.int32)
-            else:
-                k, v = k[: m.prefix], v[: m.prefix]
-            g.write_block(0, to_dev_i32(r), to_dev_i32(s), to_dev_bf16(k), to_dev_bf16(v))
-            o.write_block(0, r, s, k, v)
-        for i in sample:
-            if i % m.group_size == 0:
-                continue
+        # Every sequence's tokens go to the GPU pool: each group's leader writes the
+        # shared prefix and its own suffix, the other members their suffixes.  The
+        # oracle gets every group's prefix and the sample's suffixes.
+        for i in range(len(P.seqs)):
+            lead = i % m.group_size == 0
             k, v = m.initial_kv(pi, i)
-            t = np.arange(m.prefix, P.lens[i])
+            t = np.arange(0 if lead else m.prefix, P.lens[i])
             r = np.asarray(P.rows[i], np.int32)[t // 32]
             s = (t % 32).astype(np.int32)
-            g.write_block(0, to_dev_i32(r), to_dev_i32(s), to_dev_bf16(k[m.prefix:]), to_dev_bf16(v[m.prefix:]))
-            o.write_block(0, r, s, k[m.prefix:], v[m.prefix:])
+            kk, vv = k[t], v[t]
+            g.write_block(0, to_dev_i32(r), to_dev_i32(s), to_dev_bf16(kk), to_dev_bf16(vv))
+            if i in sample:
+                o.write_block(0, r, s, kk, vv)
+            elif lead:
+                n = m.prefix
+                o.write_block(0, r[:n], s[:n], kk[:n], vv[:n])
         gp.append(g)
         op.append(o)
         samples.append(sample)
