@@ -587,27 +587,27 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
         }
     }
     auto tok_ok = [&](int pp, int e) { return !MASK || 8 * pp + 2 * t + e < nvc; };
+    float4 mva[NMC][2][2];
+    float sm4 = 0.f;
 #pragma unroll
-    for (int cm = 0; cm < NMC; ++cm) {
-      float4 mv[2][2];  // token 8pp + 2t + e
+    for (int cm = 0; cm < NMC; ++cm)
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          mv[pp][e] = lds128(m_addr(sb, 3, kc, pp, e, cm));
-          if (!tok_ok(pp, e)) mv[pp][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+          mva[cm][pp][e] = lds128(m_addr(sb, 3, kc, pp, e, cm));
+          if (!tok_ok(pp, e)) mva[cm][pp][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+          sm4 = fmaxf(sm4, fmaxf(mva[cm][pp][e].x, mva[cm][pp][e].z));
         }
-      {
-        // the chunk's largest V scale of these groups against the exponent's bound
-        const float sm4 = fmaxf(fmaxf(fmaxf(mv[0][0].x, mv[0][0].z), fmaxf(mv[0][1].x, mv[0][1].z)),
-                                fmaxf(fmaxf(mv[1][0].x, mv[1][0].z), fmaxf(mv[1][1].x, mv[1][1].z)));
-        if (__any_sync(0xffffffffu, sm4 >= vlim && sm4 > 0.f)) {
-          float sm = fmaxf(sm4, __shfl_xor_sync(0xffffffffu, sm4, 1));
-          sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 2));
-          const int nf = v_exponent_for(sm);
-          if (vlim < 1e-30f || nf < vf) v_rescale(nf - vf, p);
-        }
-      }
+    if (__any_sync(0xffffffffu, sm4 >= vlim && sm4 > 0.f)) {
+      float sm = fmaxf(sm4, __shfl_xor_sync(0xffffffffu, sm4, 1));
+      sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 2));
+      const int nf = v_exponent_for(sm);
+      if (vlim < 1e-30f || nf < vf) v_rescale(nf - vf, p);
+    }
+#pragma unroll
+    for (int cm = 0; cm < NMC; ++cm) {
+      float4 (&mv)[2][2] = mva[cm];
       const float* p0 = p[jp];
       const float* p1 = p[jp + 1];
 #pragma unroll
