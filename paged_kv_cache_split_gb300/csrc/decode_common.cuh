@@ -95,8 +95,9 @@ struct FirstGuess {
   const uint8_t* map = nullptr;   // tensor maps of the unit's slab, acquired by this lane
   const uint8_t* qsrc = nullptr;  // q copied with the unit (it starts the CTA's segment)
   int32_t u = -1, row = -1;       // unit index and its pool row
-  int b = -1, y0 = 0;             // sequence; first slab row of the unit
+  int b = -1, y0 = 0, j = -1;     // sequence; first slab row of the unit; block-table column
   bool spec = false;              // its copies were issued right after the wait
+  int32_t row_now = -1;           // the same block-table entry read after the wait (spec lanes)
 };
 
 template <int D>
@@ -164,6 +165,7 @@ __device__ __forceinline__ FirstGuess guess_first_units(const DecodeParams& P, i
   g.u = u;
   g.row = row;
   g.b = bsel;
+  g.j = j;
   g.y0 = r * kBlockTokens + slot0;
   if (u == u0) g.qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)bsel * P.Hq * D);
   return g;
@@ -215,6 +217,9 @@ __device__ __forceinline__ FirstGuess decode_prologue(const DecodeParams& P, uin
   if (SPEC && warp == PW && g.map && lane < kSpecUnits && lane < P.NS) {
     issue(&spec[lane], stages + (size_t)lane * P.stage_bytes, g.map, g.y0, 1, g.qsrc);
     g.spec = true;
+    // the guessed entry as it is after the wait, read while warp 0 reads the context
+    // lengths, so that validating the guess costs one round trip instead of two
+    g.row_now = P.bt[(size_t)g.b * P.max_blocks + g.j];
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.NS; ++s) {
@@ -291,7 +296,11 @@ __device__ __forceinline__ void run_producer(const DecodeParams& P, const int pw
       if (u == u0 || u == UP[bb]) qsrc = reinterpret_cast<const uint8_t*>(P.q + (size_t)bb * P.Hq * D);
       const int32_t t0 = (u - UP[bb]) * T;
       const int j = t0 / kBlockTokens, slot0 = t0 % kBlockTokens;
-      const int32_t row = P.bt[(size_t)bb * P.max_blocks + j];
+      int32_t row;
+      if (k == 0 && g.spec && g.u == u && g.b == bb && g.j == j)
+        row = g.row_now;  // already read after the wait
+      else
+        row = P.bt[(size_t)bb * P.max_blocks + j];
       if (row >= 0 && (int64_t)row < P.lv.rows_capacity) {
         const int32_t slab = row / P.lv.slab_blocks;
         const int32_t r = row - slab * P.lv.slab_blocks;
@@ -478,7 +487,7 @@ __device__ __forceinline__ void merge_chunk(const float* base, size_t pstride, i
 // L2 prefetches there; its own wait still covers this kernel's completion, and
 // this kernel completes only after the attention grid has.
 template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const DecodeParams P, int main_grid) {
+__global__ void __launch_bounds__(32) combine_kernel(const DecodeParams P, int main_grid) {
   extern __shared__ int32_t cup[];  // unit prefix UP[0..B]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
@@ -596,11 +605,15 @@ inline cudaError_t launch_with_pdl(Kern kern, int grid, int threads, size_t smem
 template <int D>
 inline cudaError_t launch_combine(const DecodeParams& P, int main_grid, cudaStream_t stream) {
   const int pairs = P.B * P.Hq;
-  int grid = (pairs + 7) / 8;
-  if (grid > 1024) grid = 1024;
+  // One warp per CTA: such a CTA fits on an SM beside an attention CTA (whose
+  // registers and shared memory leave room for 32 threads, not for 256), so the
+  // combine CTAs become resident early and never hold an SM that the next
+  // attention launch needs.
+  int grid = pairs;
+  if (grid > 8192) grid = 8192;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(32);
   cfg.dynamicSmemBytes = (size_t)(P.B + 1) * sizeof(int32_t);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
