@@ -404,6 +404,10 @@ __device__ __forceinline__ float* partial_ptr(const DecodeParams& P, int D, size
 template <int V>
 struct VecF;
 template <>
+struct VecF<1> {
+  using T = float;
+};
+template <>
 struct VecF<2> {
   using T = float2;
 };
@@ -412,31 +416,41 @@ struct VecF<4> {
   using T = float4;
 };
 
-// Merge of up to N parts of one (sequence, query head), parts i0 .. i0+cnt-1 of
-// the records at `base` (one every `pstride` floats), into the running (M, den,
-// num): lane k holds part k's (m, l) for the max and the denominator, every lane
-// its V = D/32 dims of each part for the numerator.  All loads are issued before
-// any is used.  `first` (no earlier chunk) skips the rescale of an empty state,
-// which would multiply zeros by zero.
-template <int D, int N>
-__device__ __forceinline__ void merge_chunk(const float* base, size_t pstride, int i0, int cnt, int lane, bool first,
-                                            float& M, float& den, float (&num)[D / 32]) {
-  constexpr int V = D / 32;
-  constexpr int NV = V / 2 > 2 ? 2 : 1;  // vector loads per lane per part
-  constexpr int VW = V / NV;             // floats per vector load: 2 or 4
-  using Vec = typename VecF<VW>::T;
+// The combine gives each (sequence, query head) to S warps, one per slice of the
+// head's dims (S = 1: the whole head); a lane holds V = D / (32 S) consecutive dims.
+// Decode uses S = 1; chunked prefill, with many more (virtual sequence, head) pairs
+// each spread over as many CTAs, uses S = 4, which shortens each warp's chain.
+template <int D, int S>
+struct CombineShape {
+  static constexpr int V = D / (32 * S);                   // dims per lane: 1..8
+  static constexpr int NV = V > 4 ? 2 : 1;                 // vector loads per part
+  static constexpr int VW = V / NV;                        // floats per load
+  static constexpr int N = S == 1 ? (D <= 128 ? 10 : 5) : 12;  // parts per load round
+};
+
+// Merge of up to N parts of one (sequence, query head, slice), parts i0 .. i0+cnt-1
+// of the records at `base` (one every `pstride` floats; `dofs` the slice's first
+// dim), into the running (M, den, num): lane k holds part k's (m, l) for the max
+// and the denominator, every lane its V dims of each part for the numerator.  All
+// loads are issued before any is used.  `first` (no earlier round) skips the
+// rescale of an empty state, which would multiply zeros by zero.
+template <int D, int S>
+__device__ __forceinline__ void merge_chunk(const float* base, size_t pstride, int dofs, int i0, int cnt, int lane,
+                                            bool first, float& M, float& den, float (&num)[CombineShape<D, S>::V]) {
+  using Sh = CombineShape<D, S>;
+  constexpr int V = Sh::V, NV = Sh::NV, N = Sh::N;
+  using Vec = typename VecF<Sh::VW>::T;
   float2 ml = make_float2(-INFINITY, 0.f);
   if (lane < cnt) ml = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(i0 + lane) * pstride));
   Vec v[N][NV];
 #pragma unroll
-  for (int k = 0; k < N; ++k) {
-    if (k < cnt) {
+  for (int k = 0; k < N; ++k)
+    if (k < cnt)
 #pragma unroll
       for (int x = 0; x < NV; ++x)
-        v[k][x] = __ldcg(reinterpret_cast<const Vec*>(base + (size_t)(i0 + k) * pstride + kPartialHeader + lane * V) + x);
-    }
-  }
-  // Lanes = parts: chunk max, weights, denominator.
+        v[k][x] = __ldcg(reinterpret_cast<const Vec*>(base + (size_t)(i0 + k) * pstride + kPartialHeader + dofs +
+                                                      lane * V) + x);
+  // Lanes = parts: the round's max, weights, denominator.
   float Mc = ml.x;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, off));
@@ -448,13 +462,13 @@ __device__ __forceinline__ void merge_chunk(const float* base, size_t pstride, i
   if (first) {
     den = dc;
   } else {
-    const float a = exp2f(M - Mc);  // rescales earlier chunks
+    const float a = exp2f(M - Mc);  // rescales earlier rounds
     den = fmaf(den, a, dc);
 #pragma unroll
     for (int j = 0; j < V; ++j) num[j] *= a;
   }
   M = Mc;
-  // Lanes = dims: add the chunk's parts in order.
+  // Lanes = dims: add the round's parts in order.
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     if (k < cnt) {
@@ -466,13 +480,13 @@ __device__ __forceinline__ void merge_chunk(const float* base, size_t pstride, i
   }
 }
 
-// Split-K merge, a separate kernel chained after the attention kernel: one warp
-// per (sequence, query head) of every sequence that more than one CTA worked on.
-// Parts are merged one after another in CTA order with the online-softmax rule
-// (running max, rescaled denominator and numerator), so the result does not
-// depend on which CTA finished first.  Each lane owns D/32 consecutive dims.  A
-// sequence split into at most 32 parts is merged from one round of loads, with
-// the code specialised on 8, 16 or 32 parts (at D = 256: 8 or 16 parts per round).
+// Split-K merge, a separate kernel chained after the attention kernel: for every
+// (sequence, query head) of a sequence that more than one CTA worked on, S warps
+// (one per slice of the head's dims, CombineShape) merge the parts one after
+// another in CTA order with the online-softmax rule (running max, rescaled
+// denominator and numerator), so the result does not depend on which CTA finished
+// first.  Parts are loaded in rounds of CombineShape::N, all loads of a round issued
+// before any is used.
 //
 // The kernel is latency-bound (a few hundred dependent instructions per warp
 // around one L2 round trip), so everything that does not need the partials (the
@@ -486,8 +500,16 @@ __device__ __forceinline__ void merge_chunk(const float* base, size_t pstride, i
 // that the tail of this call's attention grid has left, and run its prologue and
 // L2 prefetches there; its own wait still covers this kernel's completion, and
 // this kernel completes only after the attention grid has.
-template <int D>
-__global__ void __launch_bounds__(32) combine_kernel(const DecodeParams P, int main_grid) {
+//
+// One warp per CTA, at most 80 registers a thread (launch bounds): the block
+// scheduler packs up to eight of these CTAs onto an SM that the attention grid has
+// left, and an attention CTA of the next call (about 44k registers, 219 KB of shared
+// memory) still fits beside eight of them (8 x 80 x 32 registers, 1 KB of shared
+// memory each), so the next call's CTAs are not held back until the merge ends.
+// With 256-thread CTAs of 176 registers a thread, such CTAs filled the SM's
+// registers and the next call's CTAs on about 16 SMs started 4-5 us late.
+template <int D, int S>
+__global__ void __launch_bounds__(32, 25) combine_kernel(const DecodeParams P, int main_grid) {
   extern __shared__ int32_t cup[];  // unit prefix UP[0..B]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
@@ -514,23 +536,26 @@ __global__ void __launch_bounds__(32) combine_kernel(const DecodeParams P, int m
   }
   __syncthreads();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  constexpr int V = D / 32;  // dims per lane: 2, 4 or 8
+  constexpr int V = CombineShape<D, S>::V;  // dims per lane of the warp's slice
+  constexpr int NC = CombineShape<D, S>::N;
   const int32_t U = cup[P.B];
   const int32_t C = (U + main_grid - 1) / main_grid;
   const size_t pstride = (size_t)P.Hq * partial_floats(D);
   const int nwarps = gridDim.x * (blockDim.x >> 5);
-  // this warp's first (sequence, head) and its part range, before the wait
-  int pair = blockIdx.x * (blockDim.x >> 5) + warp;
-  int b = pair / P.Hq;
+  const int items = S * P.B * P.Hq;  // (sequence, head, slice)
+  // this warp's first item and its part range, before the wait
+  int item = blockIdx.x * (blockDim.x >> 5) + warp;
+  int b = (item / S) / P.Hq;
   int32_t c_lo = 0, c_hi = 0;
-  if (C > 0 && pair < P.B * P.Hq && cup[b + 1] > cup[b]) {
+  if (C > 0 && item < items && cup[b + 1] > cup[b]) {
     c_lo = cup[b] / C;
     c_hi = (cup[b + 1] - 1) / C;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (C == 0) return;
-  while (pair < P.B * P.Hq) {
-    const size_t head = (size_t)(pair - b * P.Hq);
+  while (item < items) {
+    const size_t head = (size_t)(item / S - b * P.Hq);
+    const int dofs = S > 1 ? (item % S) * (D / S) : 0;
     const int nparts = c_hi - c_lo + 1;
     // empty sequences (zeros written by the attention kernel) and sequences of one
     // CTA (output written directly) have c_hi == c_lo
@@ -539,30 +564,30 @@ __global__ void __launch_bounds__(32) combine_kernel(const DecodeParams P, int m
       float M = -INFINITY, den = 0.f, num[V];
 #pragma unroll
       for (int j = 0; j < V; ++j) num[j] = 0.f;
-      {
-        // chunks of 32 parts (16 at D = 256, whose lanes hold 8 dims per part)
-        constexpr int NC = D <= 128 ? 32 : 16;
 #pragma unroll 1
-        for (int i0 = 0; i0 < nparts; i0 += NC)
-          merge_chunk<D, NC>(base, pstride, i0, min(NC, nparts - i0), lane, i0 == 0, M, den, num);
-      }
+      for (int i0 = 0; i0 < nparts; i0 += NC)
+        merge_chunk<D, S>(base, pstride, dofs, i0, min(NC, nparts - i0), lane, i0 == 0, M, den, num);
       const float inv = 1.0f / den;
-      uint32_t w[V / 2];
-#pragma unroll
-      for (int j = 0; j < V / 2; ++j)
-        w[j] = (uint32_t)f2bf(num[2 * j] * inv) | ((uint32_t)f2bf(num[2 * j + 1] * inv) << 16);
-      uint16_t* o = P.out + ((size_t)b * P.Hq + head) * D + lane * V;
-      if constexpr (V == 2) {
-        *reinterpret_cast<uint32_t*>(o) = w[0];
-      } else if constexpr (V == 4) {
-        *reinterpret_cast<uint2*>(o) = make_uint2(w[0], w[1]);
+      uint16_t* o = P.out + ((size_t)b * P.Hq + head) * D + dofs + lane * V;
+      if constexpr (V == 1) {
+        *o = f2bf(num[0] * inv);
       } else {
-        *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
+        uint32_t w[V / 2];
+#pragma unroll
+        for (int j = 0; j < V / 2; ++j)
+          w[j] = (uint32_t)f2bf(num[2 * j] * inv) | ((uint32_t)f2bf(num[2 * j + 1] * inv) << 16);
+        if constexpr (V == 2) {
+          *reinterpret_cast<uint32_t*>(o) = w[0];
+        } else if constexpr (V == 4) {
+          *reinterpret_cast<uint2*>(o) = make_uint2(w[0], w[1]);
+        } else {
+          *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
     }
-    pair += nwarps;
-    if (pair >= P.B * P.Hq) break;
-    b = pair / P.Hq;
+    item += nwarps;
+    if (item >= items) break;
+    b = (item / S) / P.Hq;
     c_lo = c_hi = 0;
     if (cup[b + 1] > cup[b]) {
       c_lo = cup[b] / C;
@@ -602,14 +627,11 @@ inline cudaError_t launch_with_pdl(Kern kern, int grid, int threads, size_t smem
   return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
-template <int D>
-inline cudaError_t launch_combine(const DecodeParams& P, int main_grid, cudaStream_t stream) {
+template <int D, int S>
+inline cudaError_t launch_combine_s(const DecodeParams& P, int main_grid, cudaStream_t stream) {
   const int pairs = P.B * P.Hq;
-  // One warp per CTA: such a CTA fits on an SM beside an attention CTA (whose
-  // registers and shared memory leave room for 32 threads, not for 256), so the
-  // combine CTAs become resident early and never hold an SM that the next
-  // attention launch needs.
-  int grid = pairs;
+  // one one-warp CTA per (sequence, head, slice); see combine_kernel
+  int grid = S * pairs;
   if (grid > 8192) grid = 8192;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -621,7 +643,15 @@ inline cudaError_t launch_combine(const DecodeParams& P, int main_grid, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<D>, P, main_grid);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<D, S>, P, main_grid);
+}
+
+// Decode: one warp per (sequence, head); chunked prefill (nq > 1 queries per virtual
+// sequence): four warps per head (two at head_dim 64; see CombineShape).
+template <int D>
+inline cudaError_t launch_combine(const DecodeParams& P, int main_grid, int nq, cudaStream_t stream) {
+  constexpr int SP = D >= 128 ? 4 : 2;  // a lane holds at least one dim
+  return nq > 1 ? launch_combine_s<D, SP>(P, main_grid, stream) : launch_combine_s<D, 1>(P, main_grid, stream);
 }
 
 }  // namespace pkv

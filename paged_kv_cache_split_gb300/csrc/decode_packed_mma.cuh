@@ -896,7 +896,7 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   const int threads = RS ? 128 * (((ncons + 3) >> 2) + 1) : (ncons + kProducerWarps) * 32;
   cudaError_t e = launch_with_pdl(kern, a.grid, threads, a.smem_bytes, a.stream, P);
   if (e != cudaSuccess) return e;
-  return launch_combine<D>(P, a.grid, a.stream);
+  return launch_combine<D>(P, a.grid, NQ, a.stream);
 }
 
 // The register split needs the launch allocation to cover the split: per scheduler
