@@ -226,7 +226,14 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   const int hkv = P.lv.hkv;
   const int NC = DS ? 2 * hkv : hkv;  // consumer warps
   constexpr int RW = NQ * G;          // tile rows in use
-  static_assert(RW <= 8, "query rows of one kv head fit the tile's first 8 rows");
+  constexpr bool TWO = RW > 8;        // rows 8..15 in use
+  // QG: the consumers read q from global memory at each segment start (the producer
+  // prefetches it into L2 with the segment's first unit) and rotate it into a per-head
+  // scratch, so the stages carry no q region: used with 16 rows, whose q (16 rows x D
+  // per kv head) would otherwise take a large share of every stage.
+  constexpr bool QG = TWO;
+  constexpr int QS = D + 8;  // QG scratch row stride (halves): rows 16 bytes apart in banks
+  static_assert(RW <= 16 && (!TWO || (D <= 128 && !DS)), "query rows of one kv head fit the tile");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NCW = (NC + 3) >> 2;                // consumer warpgroups (register split)
   const int PW = RS ? 4 * NCW : NC;             // the first of the two producer warps
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 #pragma unroll
   for (int k = 0; k < 4; ++k) off[k + 1] = off[k] + ((T * rows_b[k] + 1023) & ~1023);
   const int offQ = off[4];
-  const int QB = P.Hq * D * 2;
+  const int QB = QG ? 0 : P.Hq * D * 2;  // q bytes a stage receives
   SwzRegion zr[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -256,10 +263,13 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   const uint8_t** tab = reinterpret_cast<const uint8_t**>(empty + NS);
   int32_t* UP = reinterpret_cast<int32_t*>(tab + kSmemTableEntries);
   int32_t* LS = UP + (B + 1);
-  float* qscr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(LS + B) + 15) & ~uintptr_t(15));
+  // the q~ exponent of each tile row, per kv head
+  int32_t* qes = reinterpret_cast<int32_t*>((reinterpret_cast<uintptr_t>(LS + B) + 15) & ~uintptr_t(15));
+  // QG: q~ of each kv head's RW rows (fp16, row stride QS)
+  uint16_t* qg_scr = reinterpret_cast<uint16_t*>(qes + (size_t)hkv * 16);
   // dim split: per kv head, each half's partial logits (up to 32 tokens) of the last two exchanges, and
   // one mbarrier per kv head that pairs the two warps (bounded waits)
-  float4* xbuf = reinterpret_cast<float4*>(qscr + (size_t)hkv * RW * D);
+  float4* xbuf = reinterpret_cast<float4*>(qg_scr + (QG ? (size_t)hkv * RW * QS : 0));
   uint64_t* pbar = reinterpret_cast<uint64_t*>(xbuf + (size_t)hkv * 2 * 2 * 2 * 32);
   // the producers' issue token, one barrier per batch parity (after the dim-split
   // buffers, or where they would start)
@@ -272,7 +282,10 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   auto issue = [&](uint64_t* bar, uint8_t* st, const uint8_t* map, int y0, int ok, const uint8_t* qsrc) {
     const uint64_t kv_policy = P.kv_reuse ? l2_policy_evict_normal() : l2_policy_evict_first();
     mbar_arrive_expect_tx(bar, (ok ? (uint32_t)(T * (KR + VR + 2 * MR)) : 0u) + (qsrc ? (uint32_t)QB : 0u));
-    if (qsrc) bulk_g2s(st + offQ, qsrc, (uint32_t)QB, bar);
+    if (qsrc) {
+      if constexpr (QG) bulk_prefetch_l2(qsrc, (uint32_t)(P.Hq * D * 2));
+      else bulk_g2s(st + offQ, qsrc, (uint32_t)QB, bar);
+    }
     if (ok) {
       for (int cy = 0; cy < T / 16; ++cy)
 #pragma unroll
@@ -319,27 +332,29 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   // the warp's share of the head: NGL groups from group gofs; chunk counts per row
   constexpr int NGL = DS ? NG / 2 : NG;
   constexpr int NKC = Tr::NKC / (DS ? 2 : 1), NVC = Tr::NVC / (DS ? 2 : 1), NMC = Tr::NMC / (DS ? 2 : 1);
+  // row sets of the S tile: rows g (tile rows 0..7) and, with more than 8 rows in use,
+  // rows g + 8, each with its own softmax state and PV product
+  constexpr int NSET = TWO ? 2 : 1;
   const int h = DS ? warp % hkv : warp;
   const int half = DS ? warp / hkv : 0;
   const int gofs = half * NGL;
   const int g = lane >> 2, t = lane & 3;
-  float* qs = qscr + (size_t)h * RW * D;  // dim split: shared by the pair, written by half 0
   // q head (within the virtual sequence's P.Hq) of tile row r
   auto qhead = [&](int r) -> size_t {
     if constexpr (NQ == 1) return (size_t)h * G + r;
     else return (size_t)(r / G) * (size_t)(P.Hq / NQ) + (size_t)h * G + (size_t)(r % G);
   };
-  uint32_t qa[NGL][2][2];  // A fragments per group, k-step, register (rows g; rows g+8 zero)
-  float qsum[NGL];         // 2^-24 * sum over the group of the q~ values the MMA sees
-  float o[NGL][2][4];      // O^T accumulators, in units of 2^-24: group, M tile, fragment
-  float corr[NGL];         // sum_t p_t o_t for head g and each group, this lane's tokens
-  uint32_t pphase = 0;     // dim split: phase of the pair barrier
-  int xpar = 0;            // dim split: which partial-logit buffer this chunk uses
-  float m_run = -INFINITY, l_run = 0.f;
-  float m_eff = -INFINITY;  // m_run - vf: the reference of the probabilities (which carry 2^vf)
-  int vf = 0;               // p s exponent of this warp's groups (warp-uniform)
-  float vlim = 0.f;         // V scales at or above this take p s 2^vf to 2^15 (below 2^-100: vf not chosen yet)
-  float s24 = 0.f;          // this row's logit scale: scale * log2(e) * 2^24 * 2^-(q~ exponent)
+  uint32_t qa[NSET][NGL][2][2];  // A fragments per row set, group, k-step, register
+  float qsum[NSET][NGL];         // 2^-24 * sum over the group of the q~ values the MMA sees
+  float o[NSET][NGL][2][4];      // O^T accumulators, in units of 2^-24: set, group, M tile, fragment
+  float corr[NSET][NGL];         // sum_t p_t o_t for the lane's row and each group, this lane's tokens
+  uint32_t pphase = 0;           // dim split: phase of the pair barrier
+  int xpar = 0;                  // dim split: which partial-logit buffer this chunk uses
+  float m_run[NSET], l_run[NSET];
+  float m_eff[NSET];  // m_run - vf: the reference of the probabilities (which carry 2^vf)
+  float s24[NSET];    // the row's logit scale: scale * log2(e) * 2^24 * 2^-(q~ exponent)
+  int vf = 0;         // p s exponent of this warp's groups (warp-uniform)
+  float vlim = 0.f;   // V scales at or above this take p s 2^vf to 2^15 (below 2^-100: vf not chosen yet)
   // dim split: every lane of both warps of the pair arrives, then waits (bounded) for
   // the other warp.  False when the wait gave up: the warp then stops (returns), so
   // its partner gives up at its next wait and no wait is ever repeated.
@@ -423,9 +438,11 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 
   // ---- the CTA's units, one sequence segment at a time ----
   // Logits (unmasked, before the softmax scale) of NT n-tiles: tile jj holds tokens
-  // 16 kc0 + 8 jj + 2t + e of head g.  With the dim split both halves of every logit
-  // are added (in half order, by both warps).  False: a pair wait gave up.
-  auto logits = [&](auto nt_c, const uint32_t sb, const int kc0, float (&x)[4][2]) -> bool {
+  // 16 kc0 + 8 jj + 2t + e of row g (set 0) and row g + 8 (set 1).  One MMA serves both
+  // row sets (their q~ fill the A fragment's rows g and g + 8); the (scale, offset) fold
+  // is per row.  With the dim split both halves of every logit are added (in half
+  // order, by both warps).  False: a pair wait gave up.
+  auto logits = [&](auto nt_c, const uint32_t sb, const int kc0, auto& x) -> bool {
     constexpr int NT = decltype(nt_c)::value;
     uint32_t kw[4][NKC];  // word t of token 16kc + 8j + g, chunk c; tile jj = 2 (kc - kc0) + j
 #pragma unroll
@@ -452,7 +469,9 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 #pragma unroll
     for (int jj = 0; jj < NT; ++jj) {
       const int kc = kc0 + (jj >> 1), j = jj & 1;
-      float sa0 = 0.f, sa1 = 0.f;
+      float sa[NSET][2];
+#pragma unroll
+      for (int st2 = 0; st2 < NSET; ++st2) sa[st2][0] = sa[st2][1] = 0.f;
 #pragma unroll
       for (int cm = 0; cm < NMC; ++cm) {
         const float4 m0 = lds128(m_addr(sb, 2, kc, j, 0, cm));  // token 8j + 2t
@@ -468,26 +487,36 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
             k_group_frags8(kw[jj][2 * grp], kw[jj][2 * grp + 1], bfr);
           }
           float cacc[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_f16_16816(cacc, qa[grp][0][0], 0u, qa[grp][0][1], 0u, bfr[0][0], bfr[0][1]);
-          mma_f16_16816(cacc, qa[grp][1][0], 0u, qa[grp][1][1], 0u, bfr[1][0], bfr[1][1]);
-          sa0 = fmaf(q2 ? m0.z : m0.x, cacc[0], fmaf(q2 ? m0.w : m0.y, qsum[grp], sa0));
-          sa1 = fmaf(q2 ? m1.z : m1.x, cacc[1], fmaf(q2 ? m1.w : m1.y, qsum[grp], sa1));
+          mma_f16_16816(cacc, qa[0][grp][0][0], TWO ? qa[NSET - 1][grp][0][0] : 0u, qa[0][grp][0][1],
+                        TWO ? qa[NSET - 1][grp][0][1] : 0u, bfr[0][0], bfr[0][1]);
+          mma_f16_16816(cacc, qa[0][grp][1][0], TWO ? qa[NSET - 1][grp][1][0] : 0u, qa[0][grp][1][1],
+                        TWO ? qa[NSET - 1][grp][1][1] : 0u, bfr[1][0], bfr[1][1]);
+          const float sc0 = q2 ? m0.z : m0.x, of0 = q2 ? m0.w : m0.y;
+          const float sc1 = q2 ? m1.z : m1.x, of1 = q2 ? m1.w : m1.y;
+#pragma unroll
+          for (int st2 = 0; st2 < NSET; ++st2) {
+            sa[st2][0] = fmaf(sc0, cacc[2 * st2], fmaf(of0, qsum[st2][grp], sa[st2][0]));
+            sa[st2][1] = fmaf(sc1, cacc[2 * st2 + 1], fmaf(of1, qsum[st2][grp], sa[st2][1]));
+          }
         }
       }
-      x[jj][0] = sa0;
-      x[jj][1] = sa1;
+#pragma unroll
+      for (int st2 = 0; st2 < NSET; ++st2) {
+        x[st2][jj][0] = sa[st2][0];
+        x[st2][jj][1] = sa[st2][1];
+      }
     }
     if constexpr (DS) {
 #pragma unroll
       for (int q4 = 0; q4 < NT / 2; ++q4)
         xbuf[((((size_t)h * 2 + half) * 2 + xpar) * 2 + q4) * 32 + lane] =
-            make_float4(x[2 * q4][0], x[2 * q4][1], x[2 * q4 + 1][0], x[2 * q4 + 1][1]);
+            make_float4(x[0][2 * q4][0], x[0][2 * q4][1], x[0][2 * q4 + 1][0], x[0][2 * q4 + 1][1]);
       if (!pair_sync()) return false;
 #pragma unroll
       for (int q4 = 0; q4 < NT / 2; ++q4) {
         const float4 pr = xbuf[((((size_t)h * 2 + (half ^ 1)) * 2 + xpar) * 2 + q4) * 32 + lane];
-        float* x0 = x[2 * q4];
-        float* x1 = x[2 * q4 + 1];
+        float* x0 = x[0][2 * q4];
+        float* x1 = x[0][2 * q4 + 1];
         x0[0] = half ? pr.x + x0[0] : x0[0] + pr.x;
         x0[1] = half ? pr.y + x0[1] : x0[1] + pr.y;
         x1[0] = half ? pr.z + x1[0] : x1[0] + pr.z;
@@ -497,75 +526,82 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     }
     return true;
   };
-  // Online softmax of head g over NT tiles: x (scaled, masked) -> probabilities p.
-  auto softmax = [&](auto nt_c, float (&x)[4][2], float (&p)[4][2]) {
+  // Online softmax of each row set over NT tiles: x (scaled, masked) -> probabilities p.
+  auto softmax = [&](auto nt_c, auto& x, auto& p) {
     constexpr int NT = decltype(nt_c)::value;
-    float mx = fmaxf(x[0][0], x[0][1]);
 #pragma unroll
-    for (int jj = 1; jj < NT; ++jj) mx = fmaxf(mx, fmaxf(x[jj][0], x[jj][1]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const bool grow = mx > m_run;
-    if (__any_sync(0xffffffffu, grow)) {
-      const float alpha = grow ? ex2(m_run - mx) : 1.0f;
-      if (grow) m_run = mx;
-      m_eff = m_run - (float)vf;
-      l_run *= alpha;
+    for (int st2 = 0; st2 < NSET; ++st2) {
+      float mx = fmaxf(x[st2][0][0], x[st2][0][1]);
 #pragma unroll
-      for (int grp = 0; grp < NGL; ++grp) corr[grp] *= alpha;
-      const float ae = __shfl_sync(0xffffffffu, alpha, 8 * t);
-      const float ao = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+      for (int jj = 1; jj < NT; ++jj) mx = fmaxf(mx, fmaxf(x[st2][jj][0], x[st2][jj][1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const bool grow = mx > m_run[st2];
+      if (__any_sync(0xffffffffu, grow)) {
+        const float alpha = grow ? ex2(m_run[st2] - mx) : 1.0f;
+        if (grow) m_run[st2] = mx;
+        m_eff[st2] = m_run[st2] - (float)vf;
+        l_run[st2] *= alpha;
 #pragma unroll
-      for (int grp = 0; grp < NGL; ++grp)
+        for (int grp = 0; grp < NGL; ++grp) corr[st2][grp] *= alpha;
+        const float ae = __shfl_sync(0xffffffffu, alpha, 8 * t);
+        const float ao = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
 #pragma unroll
-        for (int mi = 0; mi < 2; ++mi) {
-          o[grp][mi][0] *= ae;
-          o[grp][mi][2] *= ae;
-          o[grp][mi][1] *= ao;
-          o[grp][mi][3] *= ao;
-        }
+        for (int grp = 0; grp < NGL; ++grp)
+#pragma unroll
+          for (int mi = 0; mi < 2; ++mi) {
+            o[st2][grp][mi][0] *= ae;
+            o[st2][grp][mi][2] *= ae;
+            o[st2][grp][mi][1] *= ao;
+            o[st2][grp][mi][3] *= ao;
+          }
+      }
+#pragma unroll
+      for (int jj = 0; jj < NT; ++jj)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) p[st2][jj][e] = ex2(x[st2][jj][e] - m_eff[st2]);
+      if constexpr (NQ > 1) {
+        // a row with no visible token yet in this segment keeps m_run = -inf
+        if (m_run[st2] == -INFINITY)
+#pragma unroll
+          for (int jj = 0; jj < NT; ++jj) p[st2][jj][0] = p[st2][jj][1] = 0.f;
+      }
+      float ls = p[st2][0][0] + p[st2][0][1];
+#pragma unroll
+      for (int jj = 1; jj < NT; ++jj) ls += p[st2][jj][0] + p[st2][jj][1];
+      l_run[st2] += ls;
     }
-#pragma unroll
-    for (int jj = 0; jj < NT; ++jj)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) p[jj][e] = ex2(x[jj][e] - m_eff);
-    if constexpr (NQ > 1) {
-      // a row with no visible token yet in this segment keeps m_run = -inf
-      if (m_run == -INFINITY)
-#pragma unroll
-        for (int jj = 0; jj < NT; ++jj) p[jj][0] = p[jj][1] = 0.f;
-    }
-    float ls = p[0][0] + p[0][1];
-#pragma unroll
-    for (int jj = 1; jj < NT; ++jj) ls += p[jj][0] + p[jj][1];
-    l_run += ls;
   };
   // The p s exponent moves by d: the state (both accumulators, the denominator and
-  // the probabilities in flight) is multiplied by 2^d, exactly.
-  auto v_rescale = [&](int d, float (&p)[4][2]) {
+  // the probabilities in flight) of every row set is multiplied by 2^d, exactly.
+  auto v_rescale = [&](int d, auto& p) {
     const float a = pow2i(d);
 #pragma unroll
-    for (int grp = 0; grp < NGL; ++grp) {
-      corr[grp] *= a;
+    for (int st2 = 0; st2 < NSET; ++st2) {
 #pragma unroll
-      for (int mi = 0; mi < 2; ++mi)
+      for (int grp = 0; grp < NGL; ++grp) {
+        corr[st2][grp] *= a;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[grp][mi][i] *= a;
-    }
-    l_run *= a;
+        for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      p[jj][0] *= a;
-      p[jj][1] *= a;
+          for (int i = 0; i < 4; ++i) o[st2][grp][mi][i] *= a;
+      }
+      l_run[st2] *= a;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        p[st2][jj][0] *= a;
+        p[st2][jj][1] *= a;
+      }
+      m_eff[st2] = m_run[st2] - (float)(vf + d);
     }
     vf += d;
-    m_eff = m_run - (float)vf;
     vlim = pow2i(15 - vf);
   };
-  // O^T += V^T (P S)^T over the 16 tokens of chunk kc (tiles p[jp], p[jp + 1]); offsets into corr.
+  // O^T += V^T (P S)^T over the 16 tokens of chunk kc (tiles p[.][jp], p[.][jp + 1]);
+  // offsets into corr.  The V fragment of each M tile serves every row set.
   // MASK: only the chunk's first nvc tokens hold data (the last unit of a sequence);
   // the others' scale and offset are taken as 0.
-  auto pv = [&](auto mask_c, const uint32_t sb, const int kc, float (&p)[4][2], const int jp, const int nvc) {
+  auto pv = [&](auto mask_c, const uint32_t sb, const int kc, auto& p, const int jp, const int nvc) {
     constexpr bool MASK = decltype(mask_c)::value;
     uint32_t vx[2][NVC];  // half-word g of tokens 16kc + 8pp + 2t, +1; chunk c
     if constexpr (NVC == 2) {
@@ -608,37 +644,49 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 #pragma unroll
     for (int cm = 0; cm < NMC; ++cm) {
       float4 (&mv)[2][2] = mva[cm];
-      const float* p0 = p[jp];
-      const float* p1 = p[jp + 1];
 #pragma unroll
       for (int q = 0; q < Tr::SPC; ++q) {
         const int grp = Tr::SPC * cm + q;
         const bool q2 = q >= Tr::SPP;  // second pair of the chunk
-        const uint32_t pb0 = pack_f16x2(p0[0] * (q2 ? mv[0][0].z : mv[0][0].x), p0[1] * (q2 ? mv[0][1].z : mv[0][1].x));
-        const uint32_t pb1 = pack_f16x2(p1[0] * (q2 ? mv[1][0].z : mv[1][0].x), p1[1] * (q2 ? mv[1][1].z : mv[1][1].x));
+        const float sv00 = q2 ? mv[0][0].z : mv[0][0].x, sv01 = q2 ? mv[0][1].z : mv[0][1].x;
+        const float sv10 = q2 ? mv[1][0].z : mv[1][0].x, sv11 = q2 ? mv[1][1].z : mv[1][1].x;
         const float ov00 = q2 ? mv[0][0].w : mv[0][0].y, ov01 = q2 ? mv[0][1].w : mv[0][1].y;
         const float ov10 = q2 ? mv[1][0].w : mv[1][0].y, ov11 = q2 ? mv[1][1].w : mv[1][1].y;
-        corr[grp] = fmaf(p0[0], ov00, fmaf(p0[1], ov01, fmaf(p1[0], ov10, fmaf(p1[1], ov11, corr[grp]))));
+        uint32_t pb[NSET][2];
+#pragma unroll
+        for (int st2 = 0; st2 < NSET; ++st2) {
+          const float* p0 = p[st2][jp];
+          const float* p1 = p[st2][jp + 1];
+          pb[st2][0] = pack_f16x2(p0[0] * sv00, p0[1] * sv01);
+          pb[st2][1] = pack_f16x2(p1[0] * sv10, p1[1] * sv11);
+          corr[st2][grp] =
+              fmaf(p0[0], ov00, fmaf(p0[1], ov01, fmaf(p1[0], ov10, fmaf(p1[1], ov11, corr[st2][grp]))));
+        }
         if constexpr (Tr::VBITS == 4) {
           const uint32_t x01 = vx[0][grp], x23 = vx[1][grp];
           const uint32_t y01 = x01 >> 8, y23 = x23 >> 8;
-          mma_f16_16816(o[grp][0], x01 & 0x000F000Fu, y01 & 0x000F000Fu, x23 & 0x000F000Fu, y23 & 0x000F000Fu, pb0,
-                        pb1);
-          mma_f16_16816(o[grp][1], x01 & 0x00F000F0u, y01 & 0x00F000F0u, x23 & 0x00F000F0u, y23 & 0x00F000F0u, pb0,
-                        pb1);
+#pragma unroll
+          for (int st2 = 0; st2 < NSET; ++st2) {
+            mma_f16_16816(o[st2][grp][0], x01 & 0x000F000Fu, y01 & 0x000F000Fu, x23 & 0x000F000Fu,
+                          y23 & 0x000F000Fu, pb[st2][0], pb[st2][1]);
+            mma_f16_16816(o[st2][grp][1], x01 & 0x00F000F0u, y01 & 0x00F000F0u, x23 & 0x00F000F0u,
+                          y23 & 0x00F000F0u, pb[st2][0], pb[st2][1]);
+          }
         } else {
 #pragma unroll
           for (int mi = 0; mi < 2; ++mi) {
             const uint32_t x01 = vx[0][2 * grp + mi], x23 = vx[1][2 * grp + mi];
-            mma_f16_16816(o[grp][mi], __byte_perm(x01, 0u, 0x4240), __byte_perm(x01, 0u, 0x4341),
-                          __byte_perm(x23, 0u, 0x4240), __byte_perm(x23, 0u, 0x4341), pb0, pb1);
+#pragma unroll
+            for (int st2 = 0; st2 < NSET; ++st2)
+              mma_f16_16816(o[st2][grp][mi], __byte_perm(x01, 0u, 0x4240), __byte_perm(x01, 0u, 0x4341),
+                            __byte_perm(x23, 0u, 0x4240), __byte_perm(x23, 0u, 0x4341), pb[st2][0], pb[st2][1]);
           }
         }
       }
     }
   };
   // A whole 32-token unit (both chunks, one softmax, no masks) where registers allow it.
-  constexpr bool kUnit32 = D <= 64 || (RS && D <= 128) || DS;
+  constexpr bool kUnit32 = !TWO && (D <= 64 || (RS && D <= 128) || DS);
 
   int b = find_seq(UP, B, u0);
   int s = 0;           // stage of the next unit
@@ -648,16 +696,19 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     const int32_t ue = min(u1, UP[b + 1]);  // this segment: units [ua, ue) of sequence b
     const int32_t Lb = LS[b];
 #pragma unroll
-    for (int grp = 0; grp < NGL; ++grp) {
-      corr[grp] = 0.f;
+    for (int st2 = 0; st2 < NSET; ++st2) {
 #pragma unroll
-      for (int mi = 0; mi < 2; ++mi)
+      for (int grp = 0; grp < NGL; ++grp) {
+        corr[st2][grp] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[grp][mi][i] = 0.f;
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[st2][grp][mi][i] = 0.f;
+      }
+      m_run[st2] = -INFINITY;
+      m_eff[st2] = -INFINITY;
+      l_run[st2] = 0.f;
     }
-    m_run = -INFINITY;
-    m_eff = -INFINITY;
-    l_run = 0.f;
     vf = 0;
     vlim = 0.f;
     for (int32_t u = ua; u < ue; ++u) {
@@ -668,117 +719,154 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
       const uint8_t* st = stages + (size_t)s * P.stage_bytes;
       const uint32_t sb = smem_u32(st);
       if (u == ua) {
+        // q~ rows of this kv head (fp16): without QG, q of the segment's sequence sits in
+        // the stage (bf16) and each row becomes q~ in place (same two bytes per element),
+        // read back below as the A fragments before the stage is released; with QG, q is
+        // read from global memory and q~ goes to the head's scratch
+        uint16_t* qst = reinterpret_cast<uint16_t*>(stages + (size_t)s * P.stage_bytes + offQ);
+        const uint16_t* qglob = P.q + (size_t)b * P.Hq * D;
+        auto qrow = [&](int r) -> uint16_t* { return QG ? qg_scr + ((size_t)h * RW + r) * QS : qst + qhead(r) * D; };
         if (half == 0) {
-          // q~ = H diag(s) q / sqrt(D) for this kv head's G query heads: a fast Walsh-
-          // Hadamard transform with lane l holding dims l + 32 r of one head (butterfly
-          // spans 1..16 across lanes, 32.. in registers), written to the head's scratch.
+          // q~ = H diag(s) q / sqrt(D) for the tile rows of this kv head, RB rows at a
+          // time: a fast Walsh-Hadamard transform with lane l holding dims l + 32 r of a
+          // row (butterfly spans 1..16 across lanes, 32.. in registers).  The row's q~
+          // exponent e puts its largest |q~| times 2^e in [2^14, 2^15); the stored fp16
+          // value is q~ 2^e, divided by 16 where the K code is read as 16c (odd dims of
+          // 4-bit K).
           constexpr int R = D / 32;
-          const uint16_t* qsm0 = reinterpret_cast<const uint16_t*>(st + offQ);
+          constexpr int RB = RW < 4 ? RW : 4;
           float sg[R];
 #pragma unroll
           for (int r = 0; r < R; ++r) sg[r] = P.signs[lane + 32 * r];
 #pragma unroll 1
-          for (int gg = 0; gg < RW; ++gg) {
-            const uint16_t* qsm = qsm0 + qhead(gg) * D;
-            float v[R];
+          for (int g0 = 0; g0 < RW; g0 += RB) {
+            float v[RB][R];
 #pragma unroll
-            for (int r = 0; r < R; ++r) v[r] = __uint_as_float((uint32_t)qsm[lane + 32 * r] << 16) * sg[r];
+            for (int i = 0; i < RB; ++i) {
+              const uint16_t* src = QG ? qglob + qhead(g0 + i) * D : qrow(g0 + i);
+#pragma unroll
+              for (int r = 0; r < R; ++r) v[i][r] = __uint_as_float((uint32_t)src[lane + 32 * r] << 16) * sg[r];
+            }
 #pragma unroll
             for (int hs = 1; hs < 32; hs <<= 1) {
               const float sgn = (lane & hs) ? -1.f : 1.f;  // upper element: x - y; lower: x + y
 #pragma unroll
-              for (int r = 0; r < R; ++r) v[r] = fmaf(sgn, v[r], __shfl_xor_sync(0xffffffffu, v[r], hs));
+              for (int i = 0; i < RB; ++i)
+#pragma unroll
+                for (int r = 0; r < R; ++r) v[i][r] = fmaf(sgn, v[i][r], __shfl_xor_sync(0xffffffffu, v[i][r], hs));
             }
 #pragma unroll
-            for (int hr = 1; hr < R; hr <<= 1)
+            for (int i = 0; i < RB; ++i) {
 #pragma unroll
-              for (int r = 0; r < R; ++r)
-                if ((r & hr) == 0) {
-                  const float x = v[r], y = v[r + hr];
-                  v[r] = x + y;
-                  v[r + hr] = x - y;
-                }
+              for (int hr = 1; hr < R; hr <<= 1)
 #pragma unroll
-            for (int r = 0; r < R; ++r) qs[gg * D + lane + 32 * r] = v[r];
+                for (int r = 0; r < R; ++r)
+                  if ((r & hr) == 0) {
+                    const float x = v[i][r], y = v[i][r + hr];
+                    v[i][r] = x + y;
+                    v[i][r + hr] = x - y;
+                  }
+            }
+            float qm[RB];
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+              qm[i] = fabsf(v[i][0]);
+#pragma unroll
+              for (int r = 1; r < R; ++r) qm[i] = fmaxf(qm[i], fabsf(v[i][r]));
+            }
+#pragma unroll
+            for (int hs = 16; hs >= 1; hs >>= 1)
+#pragma unroll
+              for (int i = 0; i < RB; ++i) qm[i] = fmaxf(qm[i], __shfl_xor_sync(0xffffffffu, qm[i], hs));
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+              const float qmi = qm[i] * P.inv_sqrt_d;
+              int qe = 0;
+              if (qmi > 0.f) {
+                qe = 14 - exponent_of(qmi);
+                qe = qe < -100 ? -100 : (qe > 126 ? 126 : qe);
+              }
+              const float qf = P.inv_sqrt_d * pow2i(qe);
+              uint16_t* dst = qrow(g0 + i);
+#pragma unroll
+              for (int r = 0; r < R; ++r) {
+                const float qv = v[i][r] * qf;
+                dst[lane + 32 * r] = __half_as_ushort(__float2half_rn(Tr::KBITS == 4 && (lane & 1) ? qv * 0.0625f : qv));
+              }
+              if (lane == 0) qes[h * 16 + g0 + i] = qe;
+            }
           }
         }
-        // q~ of this segment is in qs (dim split: written by the pair's first warp;
-        // the partner's reads of the previous segment's q~ preceded at least one
-        // exchange since)
+        // q~ of this segment is in place (dim split: written by the pair's first warp)
         if (!pair_sync()) return;
         __syncwarp();
-        // the row's q~ exponent: its largest |q~| times 2^e lands in [2^14, 2^15)
-        // (lanes 4g..4g+3 read a quarter of row g each; rows >= RW are zero)
-        float qm = 0.f;
-        if (g < RW) {
-          const float4* qr = reinterpret_cast<const float4*>(qs + g * D) + t * (D / 16);
 #pragma unroll
-          for (int i = 0; i < D / 16; ++i) {
-            const float4 v4 = qr[i];
-            qm = fmaxf(qm, fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w))));
-          }
-        }
-        qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 1));
-        qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 2));
-        qm *= P.inv_sqrt_d;
-        int qe = 0;
-        if (qm > 0.f) {
-          qe = 14 - exponent_of(qm);
-          qe = qe < -100 ? -100 : (qe > 126 ? 126 : qe);
-        }
-        const float qf = P.inv_sqrt_d * pow2i(qe);
-        s24 = P.scale_log2 * pow2i(-qe) * 16777216.0f;
+        for (int st2 = 0; st2 < NSET; ++st2) {
+          const int row = g + 8 * st2;
+          const bool live = row < RW;  // rows >= RW are zero
+          s24[st2] = P.scale_log2 * pow2i(live ? -qes[h * 16 + row] : 0) * 16777216.0f;
+          const uint16_t* qr = qrow(live ? row : 0);
 #pragma unroll
-        for (int grp = 0; grp < NGL; ++grp) {
-          float tsum = 0.f;
+          for (int grp = 0; grp < NGL; ++grp) {
+            float tsum = 0.f;
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks)
+            for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              float v[2];
-              bool d16 = false;
+              for (int r = 0; r < 2; ++r) {
+                uint32_t hv[2];
+                bool d16 = false;
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const int dd = 32 * (gofs + grp) + k_dim<Tr::KBITS>(t, ks, r, hh, d16);
-                const float qv = g < RW ? qs[g * D + dd] * qf : 0.f;
-                v[hh] = d16 ? qv * 0.0625f : qv;
+                for (int hh = 0; hh < 2; ++hh) {
+                  const int dd = 32 * (gofs + grp) + k_dim<Tr::KBITS>(t, ks, r, hh, d16);
+                  hv[hh] = live ? (uint32_t)qr[dd] : 0u;
+                }
+                qa[st2][grp][ks][r] = hv[0] | (hv[1] << 16);
+                const float2 back = unpack_f16x2(qa[st2][grp][ks][r]);  // the values the MMA sees
+                tsum += d16 ? 16.f * (back.x + back.y) : (back.x + back.y);
               }
-              qa[grp][ks][r] = pack_f16x2(v[0], v[1]);
-              const float2 back = unpack_f16x2(qa[grp][ks][r]);  // the values the MMA sees
-              tsum += d16 ? 16.f * (back.x + back.y) : (back.x + back.y);
-            }
-          tsum += __shfl_xor_sync(0xffffffffu, tsum, 1);
-          tsum += __shfl_xor_sync(0xffffffffu, tsum, 2);
-          qsum[grp] = tsum * 5.9604644775390625e-08f;  // 2^-24
+            tsum += __shfl_xor_sync(0xffffffffu, tsum, 1);
+            tsum += __shfl_xor_sync(0xffffffffu, tsum, 2);
+            qsum[st2][grp] = tsum * 5.9604644775390625e-08f;  // 2^-24
+          }
         }
         __syncwarp();
       }
       const int nv = min(T, Lb - (u - UP[b]) * T);
-      // tokens of this unit visible to the lane's row (its query's causal limit)
-      const int nvr = NQ == 1 ? nv : min(T, Lb - (u - UP[b]) * T - (NQ - 1 - (g < RW ? g / G : NQ - 1)));
-      if (kUnit32 && T == 32 && nv == 32 && (NQ == 1 || Lb - (u - UP[b]) * T - (NQ - 1) >= 32)) {
-        float x[4][2], p[4][2];
+      const int tleft = Lb - (u - UP[b]) * T;  // the sequence's tokens from this unit's first
+      if (kUnit32 && T == 32 && nv == 32 && (NQ == 1 || tleft - (NQ - 1) >= 32)) {
+        float x[NSET][4][2], p[NSET][4][2];
         if (!logits(std::integral_constant<int, 4>{}, sb, 0, x)) return;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          x[jj][0] *= s24;
-          x[jj][1] *= s24;
+          x[0][jj][0] *= s24[0];
+          x[0][jj][1] *= s24[0];
         }
         softmax(std::integral_constant<int, 4>{}, x, p);
         pv(std::false_type{}, sb, 0, p, 0, 16);
         pv(std::false_type{}, sb, 1, p, 2, 16);
       } else {
+        // tokens of this unit visible to each of the lane's rows (its query's causal limit)
+        int nvr[NSET];
+#pragma unroll
+        for (int st2 = 0; st2 < NSET; ++st2) {
+          const int row = g + 8 * st2;
+          nvr[st2] = NQ == 1 ? nv : min(T, tleft - (NQ - 1 - (row < RW ? row / G : NQ - 1)));
+        }
+        const bool whole = TWO && nv == T && tleft - (NQ - 1) >= T;  // every row sees every token
         for (int kc = 0; kc * 16 < nv; ++kc) {
-          float x[4][2], p[4][2] = {};
+          float x[NSET][4][2], p[NSET][4][2] = {};
           if (!logits(std::integral_constant<int, 2>{}, sb, kc, x)) return;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int tk = kc * 16 + 8 * j + 2 * t;
-            x[j][0] = tk < nvr ? x[j][0] * s24 : -INFINITY;
-            x[j][1] = tk + 1 < nvr ? x[j][1] * s24 : -INFINITY;
-          }
+          for (int st2 = 0; st2 < NSET; ++st2)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int tk = kc * 16 + 8 * j + 2 * t;
+              x[st2][j][0] = tk < nvr[st2] ? x[st2][j][0] * s24[st2] : -INFINITY;
+              x[st2][j][1] = tk + 1 < nvr[st2] ? x[st2][j][1] * s24[st2] : -INFINITY;
+            }
           softmax(std::integral_constant<int, 2>{}, x, p);
-          pv(std::true_type{}, sb, kc, p, 0, nv - 16 * kc);
+          if (whole) pv(std::false_type{}, sb, kc, p, 0, 16);
+          else pv(std::true_type{}, sb, kc, p, 0, nv - 16 * kc);
         }
       }
       mbar_arrive(&empty[s]);  // every lane: its reads of the stage are done
@@ -789,17 +877,20 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     }
 
     // ---- end of the segment: output rows, or a partial record for the combine ----
-    {
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-      const float me = __shfl_sync(0xffffffffu, m_run, 8 * t), mo = __shfl_sync(0xffffffffu, m_run, 8 * t + 4);
-      const float le = __shfl_sync(0xffffffffu, l_run, 8 * t), lo = __shfl_sync(0xffffffffu, l_run, 8 * t + 4);
-      // Offsets term of head g summed over the row's four lanes, then moved to the
-      // lanes that hold heads 2t and 2t+1 in the O^T fragments.
+    const int32_t c_lo = UP[b] / C, c_hi = (UP[b + 1] - 1) / C;
+#pragma unroll
+    for (int st2 = 0; st2 < NSET; ++st2) {
+      float lr2 = l_run[st2];
+      lr2 += __shfl_xor_sync(0xffffffffu, lr2, 1);
+      lr2 += __shfl_xor_sync(0xffffffffu, lr2, 2);
+      const float me = __shfl_sync(0xffffffffu, m_run[st2], 8 * t), mo = __shfl_sync(0xffffffffu, m_run[st2], 8 * t + 4);
+      const float le = __shfl_sync(0xffffffffu, lr2, 8 * t), lo = __shfl_sync(0xffffffffu, lr2, 8 * t + 4);
+      // Offsets term of the row summed over its four lanes, then moved to the lanes
+      // that hold rows 2t and 2t+1 (of the set) in the O^T fragments.
       float ce[NGL], co[NGL];
 #pragma unroll
       for (int grp = 0; grp < NGL; ++grp) {
-        float c = corr[grp];
+        float c = corr[st2][grp];
         c += __shfl_xor_sync(0xffffffffu, c, 1);
         c += __shfl_xor_sync(0xffffffffu, c, 2);
         ce[grp] = __shfl_sync(0xffffffffu, c, 8 * t);
@@ -807,8 +898,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
       }
       // 2^24 undoes the subnormal code scale; tile 1 of a 4-bit group read 16c.
       const float fs[2] = {16777216.0f, Tr::VBITS == 4 ? 1048576.0f : 16777216.0f};
-      const int he = 2 * t, ho = 2 * t + 1;
-      const int32_t c_lo = UP[b] / C, c_hi = (UP[b + 1] - 1) / C;
+      const int he = 2 * t + 8 * st2, ho = 2 * t + 1 + 8 * st2;
       if (c_lo == c_hi) {
         const float ie = 1.0f / le, io = 1.0f / lo;
         uint16_t* oe = P.out + ((size_t)b * P.Hq + qhead(he < RW ? he : 0)) * D;
@@ -819,12 +909,12 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
           for (int mi = 0; mi < 2; ++mi) {
             const int d0 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 0, g), d1 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 1, g);
             if (he < RW) {
-              oe[d0] = f2bf(fmaf(o[grp][mi][0], fs[mi], ce[grp]) * ie);
-              oe[d1] = f2bf(fmaf(o[grp][mi][2], fs[mi], ce[grp]) * ie);
+              oe[d0] = f2bf(fmaf(o[st2][grp][mi][0], fs[mi], ce[grp]) * ie);
+              oe[d1] = f2bf(fmaf(o[st2][grp][mi][2], fs[mi], ce[grp]) * ie);
             }
             if (ho < RW) {
-              oo[d0] = f2bf(fmaf(o[grp][mi][1], fs[mi], co[grp]) * io);
-              oo[d1] = f2bf(fmaf(o[grp][mi][3], fs[mi], co[grp]) * io);
+              oo[d0] = f2bf(fmaf(o[st2][grp][mi][1], fs[mi], co[grp]) * io);
+              oo[d1] = f2bf(fmaf(o[st2][grp][mi][3], fs[mi], co[grp]) * io);
             }
           }
       } else {
@@ -849,12 +939,12 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
           for (int mi = 0; mi < 2; ++mi) {
             const int d0 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 0, g), d1 = v_out_dim<Tr::VBITS>(gofs + grp, mi, 1, g);
             if (he < RW) {
-              pe[kPartialHeader + d0] = fmaf(o[grp][mi][0], fsv[mi], cev);
-              pe[kPartialHeader + d1] = fmaf(o[grp][mi][2], fsv[mi], cev);
+              pe[kPartialHeader + d0] = fmaf(o[st2][grp][mi][0], fsv[mi], cev);
+              pe[kPartialHeader + d1] = fmaf(o[st2][grp][mi][2], fsv[mi], cev);
             }
             if (ho < RW) {
-              po[kPartialHeader + d0] = fmaf(o[grp][mi][1], fsv[mi], cov);
-              po[kPartialHeader + d1] = fmaf(o[grp][mi][3], fsv[mi], cov);
+              po[kPartialHeader + d0] = fmaf(o[st2][grp][mi][1], fsv[mi], cov);
+              po[kPartialHeader + d1] = fmaf(o[st2][grp][mi][3], fsv[mi], cov);
             }
           }
         }
@@ -885,7 +975,7 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   P.T = a.tokens_per_stage;
   P.NS = a.n_stages;
   const int hkv = a.lv.hkv;
-  P.stage_bytes = packed_stage_bytes(P.T, hkv * Tr::KB, hkv * Tr::VB, hkv * Tr::MB, a.Hq * D * 2);
+  P.stage_bytes = packed_stage_bytes(P.T, hkv * Tr::KB, hkv * Tr::VB, hkv * Tr::MB, G * NQ > 8 ? 0 : a.Hq * D * 2);
   auto kern = decode_packed_mma_kernel<FMT, D, G, W128, RS, DS, GS, NQ>;
   {
     static unsigned long long smem_done = 0;  // this kernel (one per template instantiation)
@@ -902,12 +992,12 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
 // The register split needs the launch allocation to cover the split: per scheduler
 // 2 x kConsRegs + kProdRegs <= 3 x (registers per thread at launch); otherwise
 // setmaxnreg.inc could never be satisfied.  Checked once per kernel.
-template <typename Kern>
-bool register_split_fits(Kern kern) {
-  static int verdict = -1;
+template <auto Kern>
+bool register_split_fits() {
+  static int verdict = -1;  // one per kernel
   if (verdict < 0) {
     cudaFuncAttributes fa;
-    verdict = cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.maxThreadsPerBlock >= kRsThreads &&
+    verdict = cudaFuncGetAttributes(&fa, Kern) == cudaSuccess && fa.maxThreadsPerBlock >= kRsThreads &&
               2 * kConsRegs + kProdRegs <= 3 * fa.numRegs;
   }
   return verdict == 1;
@@ -920,11 +1010,11 @@ cudaError_t launch_decode_packed_mma(const DecodeArgs& a) {
 #define PKV_CASE(DD, GG)                                                                                      \
   if (a.D == DD && a.G == GG) {                                                                               \
     if (DD == 256 && a.dim_split) {                                                                           \
-      if (register_split_fits(decode_packed_mma_kernel<FMT, 256, GG, true, true, true, GS>))                 \
+      if (register_split_fits<decode_packed_mma_kernel<FMT, 256, GG, true, true, true, GS>>())                 \
         return launch_decode_packed_mma_t<FMT, 256, GG, true, true, true, GS>(a);                             \
       return launch_decode_packed_mma_t<FMT, 256, GG, true, false, true, GS>(a);                              \
     }                                                                                                         \
-    if (w128 && DD >= 128 && register_split_fits(decode_packed_mma_kernel<FMT, DD, GG, true, true, false, GS>)) \
+    if (w128 && DD >= 128 && register_split_fits<decode_packed_mma_kernel<FMT, DD, GG, true, true, false, GS>>()) \
       return launch_decode_packed_mma_t<FMT, DD, GG, true, true, false, GS>(a);                               \
     return w128 ? launch_decode_packed_mma_t<FMT, DD, GG, true, false, false, GS>(a)                          \
                 : launch_decode_packed_mma_t<FMT, DD, GG, false, false, false, GS>(a);                        \
@@ -942,22 +1032,36 @@ cudaError_t launch_decode_packed_mma(const DecodeArgs& a) {
 
 namespace pkv {
 
-// Chunked prefill in the packed formats: NQ = 8 / G queries per tile (the plain
-// variants: no register split, no dim split).
-template <int FMT, int GS = kGroup>
+// Chunked prefill in the packed formats: NQ queries per tile, NQ x G = 8 rows
+// (ROWS16 false) or 16 rows (true; head dims up to 128).  Head dim 128 with
+// 128-byte rows takes the register split; other geometries the plain variants.
+template <int FMT, int GS, bool ROWS16>
 cudaError_t launch_decode_packed_mma_mq(const DecodeArgs& a) {
   const bool w128 = a.lv.box_bytes[0] == 128 && a.lv.box_bytes[1] == 128 && a.lv.box_bytes[2] == 128 &&
                     a.lv.box_bytes[3] == 128;
   const int G = a.G / a.nq;
-#define PKV_MQ(DD, GG)                                                                           \
-  if (a.D == DD && G == GG && a.nq == 8 / GG)                                                    \
-    return w128 ? launch_decode_packed_mma_t<FMT, DD, GG, true, false, false, GS, 8 / GG>(a)      \
-                : launch_decode_packed_mma_t<FMT, DD, GG, false, false, false, GS, 8 / GG>(a);
-  if constexpr (GS == kGroup) {
-    PKV_MQ(64, 1) PKV_MQ(64, 2) PKV_MQ(64, 4)
+#define PKV_MQ(DD, GG, NN)                                                                                    \
+  if (a.D == DD && G == GG && a.nq == NN) {                                                                   \
+    if constexpr (DD == 128) {                                                                                \
+      if (w128 && register_split_fits<decode_packed_mma_kernel<FMT, DD, GG, true, true, false, GS, NN>>())      \
+        return launch_decode_packed_mma_t<FMT, DD, GG, true, true, false, GS, NN>(a);                         \
+    } else {                                                                                                  \
+      if (w128) return launch_decode_packed_mma_t<FMT, DD, GG, true, false, false, GS, NN>(a);                \
+    }                                                                                                         \
+    return launch_decode_packed_mma_t<FMT, DD, GG, false, false, false, GS, NN>(a);                           \
   }
-  PKV_MQ(128, 1) PKV_MQ(128, 2) PKV_MQ(128, 4)
-  PKV_MQ(256, 1) PKV_MQ(256, 2) PKV_MQ(256, 4)
+  if constexpr (ROWS16) {
+    if constexpr (GS == kGroup) {
+      PKV_MQ(64, 1, 16) PKV_MQ(64, 2, 8) PKV_MQ(64, 4, 4) PKV_MQ(64, 8, 2)
+    }
+    PKV_MQ(128, 1, 16) PKV_MQ(128, 2, 8) PKV_MQ(128, 4, 4) PKV_MQ(128, 8, 2)
+  } else {
+    if constexpr (GS == kGroup) {
+      PKV_MQ(64, 1, 8) PKV_MQ(64, 2, 4) PKV_MQ(64, 4, 2)
+    }
+    PKV_MQ(128, 1, 8) PKV_MQ(128, 2, 4) PKV_MQ(128, 4, 2)
+    PKV_MQ(256, 1, 8) PKV_MQ(256, 2, 4) PKV_MQ(256, 4, 2)
+  }
 #undef PKV_MQ
   return cudaErrorInvalidValue;
 }

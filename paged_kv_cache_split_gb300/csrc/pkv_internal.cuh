@@ -247,7 +247,7 @@ struct DecodeArgs {
   int dim_split;        // see DecodePlan
   int group;            // values per affine group of the packed formats: 32 or 64 (K4/V4)
   int kv_reuse;         // 1: K/V blocks are read again soon (chunked prefill): keep them in L2
-  int nq;               // queries per (virtual) sequence: 1 for decode; > 1 only for bf16 prefill,
+  int nq;               // queries per (virtual) sequence: 1 for decode; > 1 for chunked prefill,
                         // where Hq and G count the nq queries' heads (G = nq x heads per kv head)
 };
 
@@ -256,11 +256,16 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a);
 cudaError_t launch_decode_bf16_mq(const DecodeArgs& a);  // nq > 1 (decode_bf16_mq.cu)
 cudaError_t launch_decode_k4v4(const DecodeArgs& a);
 cudaError_t launch_decode_k4v4_g64(const DecodeArgs& a);  // groups of 64 (decode_k4v4g64.cu)
-// nq > 1 (chunked prefill), per format: decode_*_mq.cu
+// nq > 1 (chunked prefill), per format: 8 tile rows in decode_*_mq.cu, 16 in
+// decode_*_mq16.cu
 cudaError_t launch_decode_k4v4_mq(const DecodeArgs& a);
 cudaError_t launch_decode_k4v4_g64_mq(const DecodeArgs& a);
 cudaError_t launch_decode_k8v4_mq(const DecodeArgs& a);
 cudaError_t launch_decode_k8v8_mq(const DecodeArgs& a);
+cudaError_t launch_decode_k4v4_mq16(const DecodeArgs& a);
+cudaError_t launch_decode_k4v4_g64_mq16(const DecodeArgs& a);
+cudaError_t launch_decode_k8v4_mq16(const DecodeArgs& a);
+cudaError_t launch_decode_k8v8_mq16(const DecodeArgs& a);
 cudaError_t launch_decode_k8v4(const DecodeArgs& a);
 cudaError_t launch_decode_k8v8(const DecodeArgs& a);
 

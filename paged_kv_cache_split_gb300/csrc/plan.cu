@@ -5,8 +5,8 @@ namespace pkv {
 
 // The kernels keep NS stages of T tokens x all kv heads in shared memory (T = 32
 // or 16, NS <= 8), leaving room for the barriers, the staged slab table, the
-// per-sequence unit prefix and, for packed formats, the per-warp q scratch used by
-// the Hadamard rotation.
+// per-sequence unit prefix and, for packed formats, the q~ exponent of each tile row
+// (the rotated q~ itself replaces q in its stage).
 bool plan_decode(int fmt, int D, int G, int hkv, int B, int group, DecodePlan* plan) {
   const FormatBits fb = format_bits(fmt);
   if (fb.k == 0 || hkv < 1 || hkv > 8 || B < 1 || B > 4096) return false;
@@ -16,7 +16,11 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, int group, DecodePlan* p
   const size_t budget = 232448;  // 227 KB opt-in shared memory per block on sm_100-class parts
   // + staged slab table (kSmemTableEntries) + the producers' two token barriers
   size_t fixed = (size_t)(2 * B + 1 + 4) * 4 + 16 + 128 + 1024 * sizeof(void*) + 32;
-  if (packed) fixed += (size_t)hkv * G * D * 4;
+  if (packed) fixed += (size_t)hkv * 16 * 4 + 16;  // the q~ exponent of each tile row
+  // packed with more than 8 tile rows: q is read by the consumers (no q region in the
+  // stages) and rotated into a per-kv-head scratch of G rows, D + 8 halves apart
+  const bool q_global = packed && G > 8;
+  if (q_global) fixed += (size_t)hkv * G * (D + 8) * 2;
   // packed D = 256 with at most 4 kv heads and 128-byte rows: the dim split's partial
   // logit buffers and pair barriers
   const bool dim_split = packed && D == 256 && hkv <= 4 && (hkv * D * fb.k / 8) % 128 == 0 &&
@@ -60,7 +64,7 @@ bool plan_decode(int fmt, int D, int G, int hkv, int B, int group, DecodePlan* p
     for (int pass = 0; pass < 2; ++pass) {
       for (int T : cand_p) {
         // + 1024: the kernel aligns the first stage to a 1024-byte boundary
-        const size_t stage = (size_t)packed_stage_bytes(T, kr, vr, mr, hkv * G * D * 2);
+        const size_t stage = (size_t)packed_stage_bytes(T, kr, vr, mr, q_global ? 0 : hkv * G * D * 2);
         if (fixed + 1024 >= budget) return false;
         size_t ns = (budget - fixed - 1024) / (stage + 16);
         if (ns > 8) ns = 8;

@@ -594,19 +594,21 @@ pkv_status pkv_paged_decode_attention(pkv_pool* p, int layer, int B, int Hq, con
   return decode_impl(p, layer, B, Hq, q, bt, max_blocks, ctx, scale, out, ws, ws_bytes, stream, 0, 1);
 }
 
-// Chunked prefill: queries per virtual sequence.  The bf16 kernel serves nq
-// queries of one sequence per tile when nq x (query heads per kv head) fits the
-// tile's 16 rows (8 at head_dim 256) and nq divides the chunk; the packed kernels
-// serve 8 / (query heads per kv head) when that divides the chunk.
+// Chunked prefill: queries per virtual sequence.  The kernels serve nq queries of
+// one sequence per tile when nq x (query heads per kv head) fits the tile's 16 rows
+// (8 at head_dim 256) and nq divides the chunk: the bf16 kernel for any such power
+// of two, the packed kernels for the tile's full 16 rows or 8 rows.
 static int prefill_nq(const pkv_pool* p, int n_q, int Hq) {
   if (Hq % p->cfg.n_kv_heads) return 1;
   const int G = Hq / p->cfg.n_kv_heads;
-  if (p->cfg.format != PKV_FMT_BF16) {
-    // packed kernels: 8 / G queries per tile (8 rows)
-    const int nq = 8 / G;
-    return (nq > 1 && n_q % nq == 0) ? nq : 1;
-  }
   const int rows = p->cfg.head_dim <= 128 ? 16 : 8;
+  if (p->cfg.format != PKV_FMT_BF16) {
+    for (int r = rows; r >= 8; r >>= 1) {
+      const int nq = r / G;
+      if (nq > 1 && n_q % nq == 0) return nq;
+    }
+    return 1;
+  }
   for (int nq = 16; nq > 1; nq >>= 1)
     if (nq * G <= rows && n_q % nq == 0) return nq;
   return 1;

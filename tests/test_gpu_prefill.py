@@ -91,16 +91,20 @@ def test_prefill_several_queries_per_tile_bf16(D, G, n_q):
 
 
 @pytest.mark.parametrize("fmt,D,group", [(wl.FMT_K4V4, 128, 32), (wl.FMT_K8V4, 64, 32), (wl.FMT_K8V8, 128, 32),
-                                         (wl.FMT_K4V4, 256, 64)])
-@pytest.mark.parametrize("G,n_q", [(1, 8), (2, 8), (4, 2)])
-def test_prefill_several_queries_per_tile_packed(fmt, D, group, G, n_q):
-    """Packed chunks served 8 / G queries per tile, with CTA counts that start split-K
-    segments inside the chunk."""
+                                         (wl.FMT_K4V4, 256, 64), (wl.FMT_K4V4, 128, 64)])
+@pytest.mark.parametrize("hkv", [2, 4])
+@pytest.mark.parametrize("G,n_q", [(1, 8), (2, 8), (4, 2), (1, 16), (4, 4), (8, 2)])
+def test_prefill_several_queries_per_tile_packed(fmt, D, group, hkv, G, n_q):
+    """Packed chunks served several queries per tile: 16 rows of (query, head) pairs
+    when 16 / G queries divide the chunk (head dims up to 128; rows 8..15 with their
+    own softmax state), else 8 rows; with CTA counts that start split-K segments
+    inside the chunk.  Four kv heads give 128-byte rows at head_dim 128 (the
+    register-split variant); two give narrower boxes at 64 (the plain variant)."""
     lens = [n_q, n_q + 1, 33, 64, 500, 1031]
-    w = _case(fmt, D, 2, G, lens, 101 + G + n_q, group)
+    w = _case(fmt, D, hkv, G, lens, 101 + G + n_q + hkv, group)
     g, o, ol = make_pools(w)
     fill(w, g, o, ol)
-    q = wl.bf16_normal(wl.rng_for(102, n_q), (w.B, n_q, w.Hq, D))
+    q = wl.bf16_normal(wl.rng_for(102, n_q, hkv), (w.B, n_q, w.Hq, D))
     bt = w.block_table()
     ref = o.prefill_attention(0, q, bt, w.ctx(), w.scale)
     for ctas in [5, 97, 0]:
@@ -108,5 +112,5 @@ def test_prefill_several_queries_per_tile_packed(fmt, D, group, G, n_q):
         out = g.paged_prefill_attention(0, to_dev_bf16(q), to_dev_i32(bt), to_dev_i32(w.ctx()), w.scale)
         got = bf16_dev_to_f64(out)
         assert np.isfinite(got).all()
-        compare(got.reshape(-1, D), ref.reshape(-1, D), f"prefill {w.name} n_q={n_q} ctas={ctas}")
+        compare(got.reshape(-1, D), ref.reshape(-1, D), f"prefill {w.name} hkv={hkv} n_q={n_q} ctas={ctas}")
     assert g.check_errors() == 0

@@ -169,18 +169,19 @@ def test_stale_tail_slots_are_ignored(fmt, D, gs, pattern):
     assert g.check_errors() == 0
 
 
+@pytest.mark.parametrize("n_q", [5, 8])
 @pytest.mark.parametrize("fmt", [wl.FMT_BF16, wl.FMT_K4V4, wl.FMT_K8V8])
-def test_stale_tail_slots_are_ignored_by_prefill(fmt):
+def test_stale_tail_slots_are_ignored_by_prefill(fmt, n_q):
+    """n_q = 5: one query per tile; 8: the chunk in one 16-row tile."""
     lens = [40, 95, 401, 1000]
-    n_q = 5
     D = 128
     rows, used = wl.fragmented_rows([wl.nblocks(L) for L in lens], wl.rng_for(35, fmt))
     w = wl.Workload(f"stale-prefill-{wl.FMT_NAMES[fmt]}", 1, 8, 4, D, fmt, lens, rows, used, 1 / math.sqrt(D),
-                    0x57A2, 91 + fmt)
+                    0x57A2, 91 + fmt + n_q)
     g, o, ol = make_pools(w)
     fill(w, g, o, ol)
     _poison_tails(w, g, "nan")
-    q = wl.bf16_normal(wl.rng_for(36, fmt), (w.B, n_q, w.Hq, D))
+    q = wl.bf16_normal(wl.rng_for(36, fmt, n_q), (w.B, n_q, w.Hq, D))
     ref = o.prefill_attention(0, q, w.block_table(), w.ctx(), w.scale)
     out = g.paged_prefill_attention(0, to_dev_bf16(q), to_dev_i32(w.block_table()), to_dev_i32(w.ctx()), w.scale,
                                     max_ctx=max(lens))
@@ -188,3 +189,49 @@ def test_stale_tail_slots_are_ignored_by_prefill(fmt):
     assert np.isfinite(got).all()
     compare(got, ref, "prefill")
     assert g.check_errors() == 0
+
+
+# ---------------------------------------------------------------------------
+# Prefill tiles: every row of a 16-row tile picks its own q~ exponent
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", [wl.FMT_K4V4, wl.FMT_K8V4, wl.FMT_K8V8])
+def test_prefill_operand_ranges(fmt):
+    """Chunks of 8 queries at 2 heads per kv head (one 16-row tile at head_dim 128;
+    queries 4..7 in rows 8..15) with q scaled per query by powers of two from 2^-20
+    to 2^16, so the rows of one tile need exponents 36 apart.  The attention scale
+    carries 2^-16: the 2^16 queries see the logits of unscaled ones, the others a
+    flatter softmax (well conditioned), and a row that took another row's exponent
+    would see its logits off by up to 2^36.  K or V is also scaled as in the decode
+    cases."""
+    D, hkv, G, n_q = 128, 4, 2, 8
+    lens = [9, 40, 700, 2100]
+    qexp = np.array([-20, -8, 16, 0, 6, 16, -14, 10])[None, :, None, None]
+    base = 2.0 ** -16
+    cases = [("q per query", {}, base, 1.0), ("K*2^-14", dict(k_exp=-14), base * 2.0 ** 14, 1.0),
+             ("K*2^16", dict(k_exp=16), base * 2.0 ** -16, 1.0), ("V*2^-20", dict(v_exp=-20), base, 2.0 ** 20),
+             ("V*2^16", dict(v_exp=16), base, 2.0 ** -16), ("1/64 of V *2^12", dict(v_boost=12), base, 2.0 ** -8)]
+    fails = []
+    import dataclasses
+    for ci, (label, chg, sfac, ofac) in enumerate(cases):
+        rows, used = wl.fragmented_rows([wl.nblocks(L) for L in lens], wl.rng_for(37, fmt, ci))
+        w = wl.Workload(f"range-prefill-{wl.FMT_NAMES[fmt]}", 1, hkv * G, hkv, D, fmt, lens, rows, used,
+                        1 / math.sqrt(D), 0x3A9F, 120 + ci)
+        w = dataclasses.replace(w, **chg)
+        g, o, ol = make_pools(w)
+        fill(w, g, o, ol)
+        q = wl.scale_pow2(wl.bf16_normal(wl.rng_for(38, fmt, ci), (w.B, n_q, w.Hq, D)), qexp)
+        ref = o.prefill_attention(0, q, w.block_table(), w.ctx(), w.scale * sfac) * ofac
+        for ctas in (0, 3):
+            g.decode_set_ctas(ctas)
+            out = g.paged_prefill_attention(0, to_dev_bf16(q), to_dev_i32(w.block_table()), to_dev_i32(w.ctx()),
+                                            w.scale * sfac, max_ctx=max(lens))
+            got = bf16_dev_to_f64(out) * ofac
+            try:
+                assert np.isfinite(got).all(), f"{label} ctas={ctas}: non-finite output"
+                compare(got.reshape(-1, D), ref.reshape(-1, D), f"{label} ctas={ctas}")
+            except AssertionError as ex:
+                fails.append(str(ex))
+        assert g.check_errors() == 0
+        g.close()
+    assert not fails, "\n".join(fails)
