@@ -726,13 +726,86 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
         uint16_t* qst = reinterpret_cast<uint16_t*>(stages + (size_t)s * P.stage_bytes + offQ);
         const uint16_t* qglob = P.q + (size_t)b * P.Hq * D;
         auto qrow = [&](int r) -> uint16_t* { return QG ? qg_scr + ((size_t)h * RW + r) * QS : qst + qhead(r) * D; };
-        if (half == 0) {
-          // q~ = H diag(s) q / sqrt(D) for the tile rows of this kv head, RB rows at a
-          // time: a fast Walsh-Hadamard transform with lane l holding dims l + 32 r of a
-          // row (butterfly spans 1..16 across lanes, 32.. in registers).  The row's q~
-          // exponent e puts its largest |q~| times 2^e in [2^14, 2^15); the stored fp16
-          // value is q~ 2^e, divided by 16 where the K code is read as 16c (odd dims of
-          // 4-bit K).
+        // Rotation layout: with at least 16 lanes' worth of rows (rows x lanes per row)
+        // the rows are spread over the lanes (short chains, two or three exchange
+        // steps); with fewer the whole warp works on each row in turn.
+        constexpr bool kRowLanes = RW * (D <= 128 ? 4 : 8) >= 16;
+        if (half == 0 && kRowLanes) {
+          // q~ = H diag(s) q / sqrt(D) for the tile rows of this kv head by a fast Walsh-
+          // Hadamard transform, RPP rows at a time: LPR lanes per row, lane k of a row
+          // holding its VPL consecutive dims from k VPL (butterfly spans below VPL in
+          // registers, the longer ones across the row's lanes).  The row's q~ exponent e
+          // puts its largest |q~| times 2^e in [2^14, 2^15); the stored fp16 value is
+          // q~ 2^e, divided by 16 where the K code is read as 16c (odd dims of 4-bit K).
+          constexpr int LPR = D <= 128 ? 4 : 8;  // lanes per row
+          constexpr int VPL = D / LPR;            // dims per lane
+          constexpr int RPP = 32 / LPR;           // rows per pass
+          const int k = lane % LPR;
+          const int d0 = k * VPL;
+#pragma unroll 1
+          for (int g0 = 0; g0 < RW; g0 += RPP) {
+            const int row = g0 + lane / LPR;
+            const bool live = row < RW;
+            const uint16_t* src = (QG ? qglob + qhead(live ? row : 0) * D : qrow(live ? row : 0)) + d0;
+            float v[VPL];
+#pragma unroll
+            for (int i = 0; i < VPL; i += 8) {
+              const uint4 w = live ? *reinterpret_cast<const uint4*>(src + i) : make_uint4(0u, 0u, 0u, 0u);
+              const float4 s0 = *reinterpret_cast<const float4*>(P.signs + d0 + i);
+              const float4 s1 = *reinterpret_cast<const float4*>(P.signs + d0 + i + 4);
+              v[i + 0] = __uint_as_float(w.x << 16) * s0.x;
+              v[i + 1] = __uint_as_float(w.x & 0xffff0000u) * s0.y;
+              v[i + 2] = __uint_as_float(w.y << 16) * s0.z;
+              v[i + 3] = __uint_as_float(w.y & 0xffff0000u) * s0.w;
+              v[i + 4] = __uint_as_float(w.z << 16) * s1.x;
+              v[i + 5] = __uint_as_float(w.z & 0xffff0000u) * s1.y;
+              v[i + 6] = __uint_as_float(w.w << 16) * s1.z;
+              v[i + 7] = __uint_as_float(w.w & 0xffff0000u) * s1.w;
+            }
+#pragma unroll
+            for (int hs = 1; hs < VPL; hs <<= 1)
+#pragma unroll
+              for (int i = 0; i < VPL; ++i)
+                if ((i & hs) == 0) {
+                  const float x = v[i], y = v[i + hs];
+                  v[i] = x + y;
+                  v[i + hs] = x - y;
+                }
+#pragma unroll
+            for (int lb = 1; lb < LPR; lb <<= 1) {
+              const float sgn = (k & lb) ? -1.f : 1.f;  // upper element: x - y; lower: x + y
+#pragma unroll
+              for (int i = 0; i < VPL; ++i) v[i] = fmaf(sgn, v[i], __shfl_xor_sync(0xffffffffu, v[i], lb));
+            }
+            float qm = fabsf(v[0]);
+#pragma unroll
+            for (int i = 1; i < VPL; ++i) qm = fmaxf(qm, fabsf(v[i]));
+#pragma unroll
+            for (int lb = 1; lb < LPR; lb <<= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, lb));
+            qm *= P.inv_sqrt_d;
+            int qe = 0;
+            if (qm > 0.f) {
+              qe = 14 - exponent_of(qm);
+              qe = qe < -100 ? -100 : (qe > 126 ? 126 : qe);
+            }
+            const float qf = P.inv_sqrt_d * pow2i(qe);
+            if (live) {
+              uint16_t* dst = qrow(row) + d0;
+              constexpr float kOdd = Tr::KBITS == 4 ? 0.0625f : 1.0f;  // odd dims of 4-bit K
+#pragma unroll
+              for (int i = 0; i < VPL; i += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) w[j] = pack_f16x2(v[i + 2 * j] * qf, v[i + 2 * j + 1] * qf * kOdd);
+                *reinterpret_cast<uint4*>(dst + i) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+              if (k == 0) qes[h * 16 + row] = qe;
+            }
+          }
+        } else if (half == 0) {
+          // The same transform for few rows (RB at a time), lane l holding dims l + 32 r of
+          // a row (butterfly spans 1..16 across lanes, 32.. in registers), so every lane
+          // works on every row.
           constexpr int R = D / 32;
           constexpr int RB = RW < 4 ? RW : 4;
           float sg[R];
