@@ -934,8 +934,8 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const int tk = kc * 16 + 8 * j + 2 * t;
-              x[st2][j][0] = tk < nvr[st2] ? x[st2][j][0] * s24[st2] : -INFINITY;
-              x[st2][j][1] = tk + 1 < nvr[st2] ? x[st2][j][1] * s24[st2] : -INFINITY;
+              x[st2][j][0] = whole || tk < nvr[st2] ? x[st2][j][0] * s24[st2] : -INFINITY;
+              x[st2][j][1] = whole || tk + 1 < nvr[st2] ? x[st2][j][1] * s24[st2] : -INFINITY;
             }
           softmax(std::integral_constant<int, 2>{}, x, p);
           if (whole) pv(std::false_type{}, sb, kc, p, 0, 16);
