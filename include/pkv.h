@@ -149,8 +149,8 @@ int pkv_slab_runs(const int32_t* rows_host, int n, int slab_blocks, int32_t* run
  * Packed formats quantise here, once: K is rotated into the Hadamard basis,
  * then every group of group_size values gets scale = (max-min)/(2^bits-1),
  * offset = min, code = round-half-even((x-min)/scale) (0 when scale is 0).
- *   [mlxcel #235, touch point 1; mlx-swift-lm #142, After: "quantize fresh K/V
- *    once"] */
+ *   [mlxcel #235, touch point 1; mlx-swift-lm #142, After flowchart: new K/V are
+ *    quantised a single time, when written] */
 pkv_status pkv_write_block(pkv_pool* pool, int layer, int n_tokens, const int32_t* rows_dev,
                            const int32_t* slots_dev, const void* k_bf16_dev, const void* v_bf16_dev,
                            void* stream);

@@ -13,8 +13,8 @@
  *  [SLAB]  mlxcel issue #235, "chunked slab storage for the paged pool":
  *          Proposed solution (bullets 1-3) and touch points 1-3, 5.
  *  [PACK]  mlx-swift-lm PR #142, "packed paged KV formats with bounded workspace
- *          admission": Summary; After flowchart ("quantize fresh K/V once",
- *          "direct packed attention").
+ *          admission": Summary; After flowchart (new K/V quantised a single
+ *          time on write; attention reads the packed pages directly).
  *  [ATTN]  mlxcel issue #2171, "one KV storage abstraction with dense and paged
  *          backends": Proposed Solution (attend = update storage, then attention)
  *          and Implementation Notes / Edge cases (single token, no mask).
@@ -347,7 +347,7 @@ static int row_ok(const oracle_pool* p, int32_t row) {
   return row >= 0 && (int64_t)row < oracle_pool_rows(p);
 }
 
-/* write_block [SLAB, touch point 1] with "quantize fresh K/V once" [PACK, After]:
+/* write_block [SLAB, touch point 1], new K/V quantised a single time [PACK, After]:
  * token i of k/v ([n, Hkv, D] bf16) goes to (rows[i], slots[i]). */
 int oracle_write_block(oracle_pool* p, int layer, int n, const int32_t* rows, const int32_t* slots,
                        const uint16_t* k, const uint16_t* v) {

@@ -4,7 +4,7 @@
 //  write_block: mlxcel #235 touch point 1 (the row's slab is the target);
 //    packed formats follow mlx-swift-lm #142 (Summary: token-local affine groups
 //    with FP32 scale/offset, fixed signed Hadamard basis on K; After flowchart:
-//    "quantize fresh K/V once").
+//    new K/V quantised a single time, when written).
 //  copy_on_write_block: mlxcel #235 touch point 2.
 //  gather_visible: mlxcel #235 touch point 3.  The page splits the row list into
 //    maximal same-slab runs because one gather op cannot span tensors; here every

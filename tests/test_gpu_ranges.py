@@ -16,8 +16,8 @@ multiplies V by 2^e compares out * 2^-e with ref * 2^-e (attention is linear in 
 and bf16 rounding commutes with powers of two), so the tolerance keeps its meaning.
 
 Stale slots: the slots of a sequence's last block past its context length hold
-whatever an earlier owner of the row, or an imported record, left there ("slots >= L
-in the last block are zero or stale, and must be ignored").  The tests fill them
+whatever an earlier owner of the row, or an imported record, left there; they are not
+part of the sequence, so nothing in them may reach an output.  The tests fill them
 with NaN or infinity bit patterns (through import_blocks, which writes raw bytes)
 and expect the same output as with clean slots."""
 import math
