@@ -864,6 +864,28 @@ PREFILL_PACKED = "prefill-qwen3-1.7b-k4v4"
 PREFILL_NQ = 8  # new tokens per sequence in the chunk
 
 
+def prefill_launches_per_call(fmt: int, D: int, G: int, n_q: int) -> int:
+    """Kernels one prefill call launches: attention and combine, plus the expansion of
+    the block table unless the chunk's queries fit one tile (the library's choice of
+    queries per tile, restated: up to 16 (query, head) rows at head_dim <= 128, 8 at
+    256; bf16 takes the largest power of two dividing the chunk, the packed formats
+    the count filling 16 rows, else 8)."""
+    rows = 16 if D <= 128 else 8
+    nq = 1
+    if fmt == wl.FMT_BF16:
+        for c in (16, 8, 4, 2):
+            if c * G <= rows and n_q % c == 0:
+                nq = c
+                break
+    else:
+        for r in (rows, 8) if rows == 16 else (8,):
+            c = r // G
+            if c > 1 and n_q % c == 0:
+                nq = c
+                break
+    return 2 if (nq == n_q and nq > 1) else 3
+
+
 def prefill_oracle_sample(budget_s: float = 10.0, n_seqs: int = 2):
     """The oracle's chunked prefill on one layer of the Qwen3-0.6B-shaped workload,
     sequences 0..n_seqs-1, all host cores it may use."""
@@ -982,6 +1004,7 @@ def run_gpu_prefill(args, rank, world, local):
     value = bytes_step * world / (ms_step * 1e-3) / 1e9
     peak, peak_src = measured_peak()
     launch_us = ms_step * 1e3 / w.n_layers
+    per_call = prefill_launches_per_call(w.fmt, w.D, w.Hq // w.Hkv, n_q)
     res = {"metric": "chunked prefill attention: achieved HBM GB/s (K/V of the visible context once), query tokens/s",
            "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(ms_step, 5), "step_ms": step_stats(per_step), "higher_is_better": True,
@@ -995,11 +1018,12 @@ def run_gpu_prefill(args, rank, world, local):
            "roofline": {"bound": "hbm", "achieved": round(bytes_layer / (launch_us * 1e-6) / 1e9, 1), "peak": peak,
                         "unit": "GB/s", "frac": round(bytes_layer / (launch_us * 1e-6) / 1e9 / peak, 4), "traffic": ncu_traffic(args.workload),
                         "per_launch_bytes": bytes_layer, "avg_launch_us": round(launch_us, 3), "peak_source": peak_src,
-                        "kernel": "expansion + attention + combine kernels per layer"},
+                        "kernel": ("attention + combine kernels per layer" if per_call == 2 else
+                                   "expansion + attention + combine kernels per layer")},
            "e2e": {"value": round(bytes_step * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
                    "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": int(q.numel() * 2),
                    "d2h_bytes_per_step": int(out.numel() * 2)},
-           "gpu_launches": 3 * w.n_layers * args.steps, "clocks": sampler.summary()}
+           "gpu_launches": per_call * w.n_layers * args.steps, "clocks": sampler.summary()}
     return res
 
 

@@ -340,10 +340,12 @@ pkv_status pkv_prefill_workspace_bytes(const pkv_pool* pool, int B, int n_q, int
  * mapping as for pkv_paged_decode_attention.  The workspace (caller-owned, 256-byte
  * aligned, pkv_prefill_workspace_bytes) holds, for each run of NQ consecutive
  * queries of a sequence, a view of the sequence (the same block-table row, the
- * last of those queries' causal length) and the split-K partials.  The attention
- * kernels serve the NQ queries in one tensor-core tile, each masked at its own
- * causal limit: bf16 up to 16 (query, head) rows per kv head at head_dim <= 128 and
- * 8 at 256, the packed formats 8; NQ is the largest such count dividing n_q, else 1.
+ * last of those queries' causal length; when NQ = n_q > 1 the caller's block table
+ * and lengths serve directly) and the split-K partials.  The attention kernels
+ * serve the NQ queries in one tensor-core tile, each masked at its own causal
+ * limit: up to 16 (query, head) rows per kv head at head_dim <= 128 and 8 at 256;
+ * NQ is the largest such count dividing n_q (bf16), or the one filling 16 rows, else
+ * 8 rows (packed formats), else 1.
  * A sequence with fewer than n_q tokens sets the device error word (bit 2) and its
  * rows are zero.
  * Errors as for pkv_paged_decode_attention; PKV_ERR_INVALID when B * n_q > 4096.

@@ -27,6 +27,7 @@ struct DecodeParams {
   int NS;           // stages in the ring
   int stage_bytes;  // bytes of one stage
   int kv_reuse;     // 1: K/V are read again soon (chunked prefill): normal L2 priority, else evict-first
+  int nq;           // queries per (virtual) sequence: 1 for decode
 };
 
 constexpr int kMaxConsumerWarps = 8;
@@ -100,14 +101,22 @@ struct FirstGuess {
   int32_t row_now = -1;           // the same block-table entry read after the wait (spec lanes)
 };
 
+// The context length the kernels work with: clamped into [0, max_blocks x block
+// size]; with nq > 1 queries per (virtual) sequence a length in (0, nq) is too short
+// for the chunk (its first query would see no token) and counts as empty.  The
+// caller flags both cases as context errors where it reads the lengths first.
+__device__ __forceinline__ int32_t usable_ctx(int32_t L, int32_t lim, int nq) {
+  L = L < 0 ? 0 : (L > lim ? lim : L);
+  return (nq > 1 && L < nq) ? 0 : L;
+}
+
 template <int D>
 __device__ __forceinline__ FirstGuess guess_first_units(const DecodeParams& P, int nprefetch) {
   FirstGuess g;
   const int lane = threadIdx.x & 31;
   const int lim = P.max_blocks * kBlockTokens;
   auto units_of = [&](int b) -> int32_t {
-    int32_t L = b < P.B ? P.ctx[b] : 0;
-    L = L < 0 ? 0 : (L > lim ? lim : L);
+    const int32_t L = usable_ctx(b < P.B ? P.ctx[b] : 0, lim, P.nq);
     return (L + P.T - 1) / P.T;
   };
   int32_t tot = 0;
@@ -237,11 +246,9 @@ __device__ __forceinline__ FirstGuess decode_prologue(const DecodeParams& P, uin
       const int b = base + lane;
       int32_t n = 0;
       if (b < P.B) {
-        int32_t L = P.ctx[b];
-        if (L < 0 || L > lim) {
-          atomicOr(P.lv.err, ERR_CTX);
-          L = L < 0 ? 0 : lim;
-        }
+        const int32_t L0 = P.ctx[b];
+        const int32_t L = usable_ctx(L0, lim, P.nq);
+        if (L != L0) atomicOr(P.lv.err, ERR_CTX);
         LS[b] = L;
         n = (L + P.T - 1) / P.T;
       }
@@ -519,8 +526,7 @@ __global__ void __launch_bounds__(32, 25) combine_kernel(const DecodeParams P, i
       const int b = base + lane;
       int32_t n = 0;
       if (b < P.B) {
-        int32_t L = P.ctx[b];
-        L = L < 0 ? 0 : (L > lim ? lim : L);
+        const int32_t L = usable_ctx(P.ctx[b], lim, P.nq);
         n = (L + P.T - 1) / P.T;
       }
       int32_t inc = n;

@@ -403,6 +403,7 @@ cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
   P.counters = a.counters;
   P.partials = a.partials;
   P.kv_reuse = a.kv_reuse;
+  P.nq = a.nq;
   P.T = a.tokens_per_stage;
   P.NS = a.n_stages;
   P.stage_bytes = 2 * P.T * (a.lv.hkv * D * 2) + ((a.Hq * D * 2 + 1023) & ~1023);

@@ -1045,6 +1045,7 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   P.counters = a.counters;
   P.partials = a.partials;
   P.kv_reuse = a.kv_reuse;
+  P.nq = a.nq;
   P.T = a.tokens_per_stage;
   P.NS = a.n_stages;
   const int hkv = a.lv.hkv;

@@ -657,14 +657,24 @@ pkv_status pkv_paged_prefill_attention(pkv_pool* p, int layer, int B, int n_q, i
   if (!plan_decode(p->cfg.format, p->cfg.head_dim, G * nq, p->cfg.n_kv_heads, Bv, p->cfg.group_size, &plan) ||
       plan.smem_bytes > p->smem_optin)
     return PKV_ERR_INVALID;
-  int32_t* bt2 = (int32_t*)((uint8_t*)ws + bt_off);
-  int32_t* ctx2 = (int32_t*)((uint8_t*)ws + ctx_off);
-  PKV_CUDA(launch_expand_prefill(B, n_q, nq, max_blocks, bt, ctx, bt2, ctx2, p->err_dev, (cudaStream_t)stream),
-           "prefill expansion launch");
   // q [B, n_q, Hq, D] and out [B, n_q, Hq, D] are [Bv, nq * Hq, D]: virtual sequence v
   // holds queries nq * (v mod (n_q / nq)) .. + nq - 1 of its sequence.  The K/V blocks
-  // of a sequence are read by all of its virtual sequences: normal L2 priority.
-  return decode_impl(p, layer, Bv, Hq * nq, q, bt2, max_blocks, ctx2, scale, out, (uint8_t*)ws + dec_off,
+  // of a sequence are read by all of its virtual sequences: normal L2 priority.  A
+  // chunk of several queries that fits one tile (nq = n_q > 1) is its own virtual
+  // sequence: the caller's block table and context lengths serve as they are (the
+  // kernels treat a length below nq as a context error and the sequence as empty, as
+  // the expansion does).
+  const int32_t* bt_v = bt;
+  const int32_t* ctx_v = ctx;
+  if (nq != n_q || nq == 1) {
+    int32_t* bt2 = (int32_t*)((uint8_t*)ws + bt_off);
+    int32_t* ctx2 = (int32_t*)((uint8_t*)ws + ctx_off);
+    PKV_CUDA(launch_expand_prefill(B, n_q, nq, max_blocks, bt, ctx, bt2, ctx2, p->err_dev, (cudaStream_t)stream),
+             "prefill expansion launch");
+    bt_v = bt2;
+    ctx_v = ctx2;
+  }
+  return decode_impl(p, layer, Bv, Hq * nq, q, bt_v, max_blocks, ctx_v, scale, out, (uint8_t*)ws + dec_off,
                      ws_bytes - dec_off, stream, 1, nq);
 }
 
