@@ -28,6 +28,7 @@ struct DecodeParams {
   int stage_bytes;  // bytes of one stage
   int kv_reuse;     // 1: K/V are read again soon (chunked prefill): normal L2 priority, else evict-first
   int nq;           // queries per (virtual) sequence: 1 for decode
+  int seg_cost;     // cost of a sequence start in quarter units (see Split)
 };
 
 constexpr int kMaxConsumerWarps = 8;
@@ -52,6 +53,54 @@ __device__ __forceinline__ int find_seq(const int32_t* UP, int B, int32_t u) {
     if (UP[mid] <= u) lo = mid; else hi = mid - 1;
   }
   return lo;
+}
+
+// Split of the units over the CTAs.  A CTA pays for each sequence segment it starts
+// (q staging or rotation at the start, the output or partial record at the end),
+// about seg_cost / kCostScale units, so the split is even in cost, not in units:
+// unit u of sequence b sits at position kCostScale u + seg_cost (b + 1), and CTA c
+// holds the units whose positions lie in [c VC, (c + 1) VC), VC = ceil((kCostScale
+// U + seg_cost B) / grid) but at least kCostScale.  seg_cost 0 gives the plain even
+// split.  The attention
+// kernels (each CTA's unit range, and whether a sequence needs a split-K merge) and
+// the combine (the CTAs holding a sequence's parts) use the same positions.
+constexpr int kCostScale = 4;
+
+struct Split {
+  int64_t VC = 0;   // positions per CTA (0: no units)
+  int32_t a = 0;    // seg_cost
+  __device__ __forceinline__ int32_t cta_of(int32_t u, int b) const {
+    return (int32_t)(((int64_t)kCostScale * u + (int64_t)a * (b + 1)) / VC);
+  }
+  // first and last CTA holding units of a non-empty sequence b
+  __device__ __forceinline__ int32_t c_lo(const int32_t* UP, int b) const { return cta_of(UP[b], b); }
+  __device__ __forceinline__ int32_t c_hi(const int32_t* UP, int b) const { return cta_of(UP[b + 1] - 1, b); }
+  // first unit of CTA c, UP[B] when it has none: the first sequence whose last unit
+  // reaches position c VC, from the first of its units that does
+  __device__ __forceinline__ int32_t first_unit(const int32_t* UP, int B, int64_t c) const {
+    const int64_t pos = c * VC;
+    int lo = 0, hi = B;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if ((int64_t)kCostScale * (UP[mid + 1] - 1) + (int64_t)a * (mid + 1) >= pos) hi = mid;
+      else lo = mid + 1;
+    }
+    if (lo == B) return UP[B];
+    const int64_t x = pos - (int64_t)a * (lo + 1);
+    const int64_t u = x <= 0 ? 0 : (x + kCostScale - 1) / kCostScale;
+    return (int32_t)(u > UP[lo] ? u : UP[lo]);
+  }
+};
+
+__device__ __forceinline__ Split make_split(int32_t U, int B, int grid, int seg_cost) {
+  Split sp;
+  sp.a = seg_cost;
+  const int64_t tot = (int64_t)kCostScale * U + (int64_t)seg_cost * B;
+  // at least one unit's step per CTA, so the CTAs holding a sequence's units are
+  // consecutive (no CTA in between is left without a unit of it)
+  const int64_t vc = (tot + grid - 1) / grid;
+  sp.VC = U == 0 ? 0 : (vc > kCostScale ? vc : kCostScale);
+  return sp;
 }
 
 // Prologue of every decode kernel: thread 0 initialises the stage barriers (full:
@@ -126,10 +175,12 @@ __device__ __forceinline__ FirstGuess guess_first_units(const DecodeParams& P, i
     for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
     tot += n;
   }
-  const int32_t C = (tot + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
-  const int32_t u0 = (int32_t)blockIdx.x * C;
-  if (C == 0 || u0 >= tot) return g;
-  // the sequence holding unit u0, and its first unit
+  if (tot == 0) return g;
+  const Split sp = make_split(tot, P.B, (int)gridDim.x, P.seg_cost);
+  // the first sequence whose units reach this CTA's first position, and the CTA's
+  // first unit (Split::first_unit over the guessed lengths, one lane per sequence)
+  const int64_t pos = (int64_t)blockIdx.x * sp.VC;
+  const int64_t pos1 = pos + sp.VC;
   int32_t carry = 0;
   int bsel = -1, nsel = 0;
   int32_t ubase = 0;
@@ -141,7 +192,9 @@ __device__ __forceinline__ FirstGuess guess_first_units(const DecodeParams& P, i
       const int32_t y = __shfl_up_sync(0xffffffffu, inc, off);
       if (lane >= off) inc += y;
     }
-    const unsigned hit = __ballot_sync(0xffffffffu, base + lane < P.B && carry + inc > u0);
+    const int bb = base + lane;
+    const unsigned hit = __ballot_sync(
+        0xffffffffu, bb < P.B && (int64_t)kCostScale * (carry + inc - 1) + (int64_t)sp.a * (bb + 1) >= pos);
     if (hit) {
       const int l = __ffs(hit) - 1;
       bsel = base + l;
@@ -151,8 +204,12 @@ __device__ __forceinline__ FirstGuess guess_first_units(const DecodeParams& P, i
     carry += __shfl_sync(0xffffffffu, inc, 31);
   }
   if (bsel < 0) return g;
+  const int64_t x0 = pos - (int64_t)sp.a * (bsel + 1);
+  const int64_t uf = x0 <= 0 ? 0 : (x0 + kCostScale - 1) / kCostScale;
+  const int32_t u0 = (int32_t)(uf > ubase ? uf : ubase);
   const int32_t u = u0 + lane;
-  if (u >= ubase + nsel || u >= u0 + C) return g;
+  // inside the first sequence and inside this CTA (position below the next CTA's first)
+  if (u >= ubase + nsel || (int64_t)kCostScale * u + (int64_t)sp.a * (bsel + 1) >= pos1) return g;
   const int32_t tok0 = (u - ubase) * P.T;
   const int j = tok0 / kBlockTokens, slot0 = tok0 % kBlockTokens;
   if (j >= P.max_blocks) return g;
@@ -545,7 +602,7 @@ __global__ void __launch_bounds__(32, 25) combine_kernel(const DecodeParams P, i
   constexpr int V = CombineShape<D, S>::V;  // dims per lane of the warp's slice
   constexpr int NC = CombineShape<D, S>::N;
   const int32_t U = cup[P.B];
-  const int32_t C = (U + main_grid - 1) / main_grid;
+  const Split sp = make_split(U, P.B, main_grid, P.seg_cost);
   const size_t pstride = (size_t)P.Hq * partial_floats(D);
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   const int items = S * P.B * P.Hq;  // (sequence, head, slice)
@@ -553,12 +610,12 @@ __global__ void __launch_bounds__(32, 25) combine_kernel(const DecodeParams P, i
   int item = blockIdx.x * (blockDim.x >> 5) + warp;
   int b = (item / S) / P.Hq;
   int32_t c_lo = 0, c_hi = 0;
-  if (C > 0 && item < items && cup[b + 1] > cup[b]) {
-    c_lo = cup[b] / C;
-    c_hi = (cup[b + 1] - 1) / C;
+  if (U > 0 && item < items && cup[b + 1] > cup[b]) {
+    c_lo = sp.c_lo(cup, b);
+    c_hi = sp.c_hi(cup, b);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (C == 0) return;
+  if (U == 0) return;
   while (item < items) {
     const size_t head = (size_t)(item / S - b * P.Hq);
     const int dofs = S > 1 ? (item % S) * (D / S) : 0;
@@ -596,8 +653,8 @@ __global__ void __launch_bounds__(32, 25) combine_kernel(const DecodeParams P, i
     b = (item / S) / P.Hq;
     c_lo = c_hi = 0;
     if (cup[b + 1] > cup[b]) {
-      c_lo = cup[b] / C;
-      c_hi = (cup[b + 1] - 1) / C;
+      c_lo = sp.c_lo(cup, b);
+      c_hi = sp.c_hi(cup, b);
     }
   }
 }
@@ -653,11 +710,12 @@ inline cudaError_t launch_combine_s(const DecodeParams& P, int main_grid, cudaSt
 }
 
 // Decode: one warp per (sequence, head); chunked prefill (nq > 1 queries per virtual
-// sequence): four warps per head (two at head_dim 64; see CombineShape).
+// sequence, so nq times the heads): two warps per head, each merging half of its dims
+// (at head_dim 128, four warps per head merged the bf16 chunk of 8 as fast and the
+// K4/V4 one 2% slower; one warp per head was 8% slower on bf16).
 template <int D>
 inline cudaError_t launch_combine(const DecodeParams& P, int main_grid, int nq, cudaStream_t stream) {
-  constexpr int SP = D >= 128 ? 4 : 2;  // a lane holds at least one dim
-  return nq > 1 ? launch_combine_s<D, SP>(P, main_grid, stream) : launch_combine_s<D, 1>(P, main_grid, stream);
+  return nq > 1 ? launch_combine_s<D, 2>(P, main_grid, stream) : launch_combine_s<D, 1>(P, main_grid, stream);
 }
 
 }  // namespace pkv

@@ -111,11 +111,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
   const FirstGuess fg = decode_prologue<D, true>(P, full, empty, NC, NC, UP, LS, tab, tok, spec, stages, issue);
   __syncthreads();
   const int32_t U = UP[B];
-  const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
+  const Split sp = make_split(U, B, (int)gridDim.x, P.seg_cost);  // this CTA's units: [u0, u1)
   zero_empty_sequences<D>(P, LS);
-  const int32_t u0 = (int32_t)blockIdx.x * C;
-  const int32_t u1 = min(U, u0 + C);
-  if (C == 0 || u0 >= u1) {
+  const int32_t u0 = U == 0 ? 0 : sp.first_unit(UP, B, blockIdx.x);
+  const int32_t u1 = U == 0 ? 0 : sp.first_unit(UP, B, (int64_t)blockIdx.x + 1);
+  if (U == 0 || u0 >= u1) {
     if (warp == NC) finish_spec(fg, spec, err);
     return;
   }
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_bf16_mma_kernel(const D
         const float me = __shfl_sync(0xffffffffu, mv, 8 * t), mo = __shfl_sync(0xffffffffu, mv, 8 * t + 4);
         const float le = __shfl_sync(0xffffffffu, lv, 8 * t), lo = __shfl_sync(0xffffffffu, lv, 8 * t + 4);
         const int he = rb + 2 * t, ho = rb + 2 * t + 1;
-        const int32_t c_lo = UP[b] / C, c_hi = (UP[b + 1] - 1) / C;
+        const int32_t c_lo = sp.c_lo(UP, b), c_hi = sp.c_hi(UP, b);
         if (c_lo == c_hi) {
           const float ie = 1.0f / le, io = 1.0f / lo;
           uint16_t* oe = P.out + ((size_t)b * P.Hq + qhead(he < R ? he : 0)) * D;
@@ -404,6 +404,7 @@ cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
   P.partials = a.partials;
   P.kv_reuse = a.kv_reuse;
   P.nq = a.nq;
+  P.seg_cost = a.seg_cost;
   P.T = a.tokens_per_stage;
   P.NS = a.n_stages;
   P.stage_bytes = 2 * P.T * (a.lv.hkv * D * 2) + ((a.Hq * D * 2 + 1023) & ~1023);

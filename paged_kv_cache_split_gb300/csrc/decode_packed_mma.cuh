@@ -303,11 +303,11 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
   }
   __syncthreads();
   const int32_t U = UP[B];
-  const int32_t C = (U + (int32_t)gridDim.x - 1) / (int32_t)gridDim.x;
+  const Split sp = make_split(U, B, (int)gridDim.x, P.seg_cost);  // this CTA's units: [u0, u1)
   zero_empty_sequences<D>(P, LS);
-  const int32_t u0 = (int32_t)blockIdx.x * C;
-  const int32_t u1 = min(U, u0 + C);
-  if (C == 0 || u0 >= u1) {
+  const int32_t u0 = U == 0 ? 0 : sp.first_unit(UP, B, blockIdx.x);
+  const int32_t u1 = U == 0 ? 0 : sp.first_unit(UP, B, (int64_t)blockIdx.x + 1);
+  if (U == 0 || u0 >= u1) {
     if (warp == PW) finish_spec(fg, spec, err);
     return;
   }
@@ -950,7 +950,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
     }
 
     // ---- end of the segment: output rows, or a partial record for the combine ----
-    const int32_t c_lo = UP[b] / C, c_hi = (UP[b + 1] - 1) / C;
+    const int32_t c_lo = sp.c_lo(UP, b), c_hi = sp.c_hi(UP, b);
 #pragma unroll
     for (int st2 = 0; st2 < NSET; ++st2) {
       float lr2 = l_run[st2];
@@ -1046,6 +1046,7 @@ cudaError_t launch_decode_packed_mma_t(const DecodeArgs& a) {
   P.partials = a.partials;
   P.kv_reuse = a.kv_reuse;
   P.nq = a.nq;
+  P.seg_cost = a.seg_cost;
   P.T = a.tokens_per_stage;
   P.NS = a.n_stages;
   const int hkv = a.lv.hkv;

@@ -247,6 +247,7 @@ struct DecodeArgs {
   int dim_split;        // see DecodePlan
   int group;            // values per affine group of the packed formats: 32 or 64 (K4/V4)
   int kv_reuse;         // 1: K/V blocks are read again soon (chunked prefill): keep them in L2
+  int seg_cost;         // cost of a sequence start for the CTA split, in quarter units (Split)
   int nq;               // queries per (virtual) sequence: 1 for decode; > 1 for chunked prefill,
                         // where Hq and G count the nq queries' heads (G = nq x heads per kv head)
 };

@@ -573,6 +573,12 @@ static pkv_status decode_impl(pkv_pool* p, int layer, int B, int Hq, const void*
   a.group = p->cfg.group_size;
   a.kv_reuse = kv_reuse;
   a.nq = nq;
+  // what a sequence start costs a CTA, in quarter units (the CTA split weighs it; the
+  // values measured best on the bench workloads): bf16 only reads q's fragments; the
+  // packed kernels rotate q at each start (worth more units where units are cheap, at
+  // head_dim 64), and with 16 tile rows rotate 16 rows and write two row sets
+  const int D = p->cfg.head_dim;
+  a.seg_cost = p->cfg.format == PKV_FMT_BF16 ? 2 : (G > 8 ? 16 : (D <= 64 ? 8 : 4));
   a.smem_bytes = plan.smem_bytes;
   a.stream = (cudaStream_t)stream;
   cudaError_t e;
