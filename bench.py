@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -215,13 +216,22 @@ def measured_peak():
         return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and blank-line or trailing-space differences."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash() -> str:
+    """Hash of the decode kernels' code (comments ignored): ncu figures taken on one
+    kernel source stay attached to it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_split_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.startswith("decode") or f in ("pkv_internal.cuh", "plan.cu"):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

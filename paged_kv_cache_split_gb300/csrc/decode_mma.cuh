@@ -1,7 +1,8 @@
 // decode_mma.cuh — native-bf16 paged decode attention on tensor-core tiles.
 //
-// Work partition: units of T tokens x all kv heads, split evenly over one CTA per
-// SM; a producer warp plus one consumer warp per kv head; split-K partials merged
+// Work partition: units of T tokens x all kv heads, split over one CTA per SM
+// evenly in cost (Split, decode_common.cuh: a sequence start counts as part of a
+// unit); a producer warp plus one consumer warp per kv head; split-K partials merged
 // by the chained combine kernel (decode_common.cuh).  For bf16 K/V two choices cut
 // the consumer's issue slots by several times against CUDA-core dot products:
 //

@@ -2,21 +2,25 @@
 // pages on tensor-core tiles (fp16 in, fp32 accumulate).
 //
 // Work partition and split-K epilogue are those of the bf16 kernel
-// (decode_mma.cuh): units of T tokens x all kv heads split evenly over one CTA per
-// SM, two producer warps and one consumer warp per kv head (two with the dim split).
+// (decode_mma.cuh): units of T tokens x all kv heads split over one CTA per SM,
+// evenly in cost (Split), two producer warps and one consumer warp per kv head (two
+// with the dim split).
 // Staging uses TMA tensor copies: each stored tensor of a slab (K codes, V codes, K
 // meta, V meta) has a tensor map over [tokens][all-heads row bytes]; a stage holds
 // T tokens of each tensor as boxes of 16 tokens x W bytes (W = 128, 64, 32 or 16,
 // the largest dividing the row), written with the W-byte shared-memory swizzle (16-byte chunk c of box row r
 // lands at chunk c ^ f(r)), so 16-byte chunks of 8 consecutive tokens sit in
 // distinct banks and are read with ldmatrix.  q comes with the first unit of a
-// sequence (one bulk copy).  The packed pages are consumed directly, never
+// sequence (one bulk copy; with 16 tile rows the consumers read it from global
+// memory instead, QG).  The packed pages are consumed directly, never
 // expanded in memory (mlx-swift-lm PR #142, Summary: direct attention on packed
 // pages):
 //
-//  * q is rotated into K's signed Hadamard basis (q~ = H diag(s) q / sqrt(D), FWHT
-//    in per-warp shared scratch) when a sequence starts and kept as fp16 A
-//    fragments (rows = query heads, rows >= G zero).
+//  * q is rotated into K's signed Hadamard basis (q~ = H diag(s) q / sqrt(D), a fast
+//    Walsh-Hadamard transform at each segment start, stored as fp16 in place of q in
+//    the stage, or in a per-head scratch with QG) and kept as fp16 A fragments
+//    (rows = the tile's (query, head) rows, rows 8..15 in the fragment's upper half
+//    when more than 8 are in use; unused rows zero).
 //  * Codes enter the tensor cores as fp16 subnormals: the bit pattern of a code c
 //    (4 or 8 bits) in the low mantissa bits is the exact value c * 2^-24, so a code
 //    becomes an operand with one AND (4-bit) or one byte permute (8-bit).  A 4-bit
