@@ -91,3 +91,28 @@ def test_one_long_sequence_spans_every_cta(fmt):
                                                        to_dev_i32(w.ctx()), w.scale, max_ctx=lens[0]))
         compare(got, ref, f"{w.name} L={lens[0]} ctas={ctas}")
     assert g.check_errors() == 0
+
+
+@pytest.mark.parametrize("fmt,D,G", [(wl.FMT_BF16, 128, 2), (wl.FMT_K4V4, 128, 2), (wl.FMT_K8V4, 64, 4),
+                                     (wl.FMT_K8V8, 256, 2)])
+def test_many_short_and_empty_sequences_over_the_cost_split(fmt, D, G):
+    """Eighty sequences of 0 to 70 tokens (a quarter empty, many of one unit or less):
+    the CTA split weighs every sequence start, so a CTA holds many segments, several
+    CTAs hold none, and with few units the positions per CTA are clamped to one unit's
+    step.  Parity with the oracle and bit-identical repeats at 1, 5, 37 CTAs, the
+    default grid and 400 CTAs."""
+    rng = np.random.default_rng(4242)
+    lens = [int(x) if rng.random() > 0.25 else 0 for x in rng.integers(1, 71, size=80)]
+    w = _case(fmt, D, 4, G, lens, 97 + D + G)
+    g, o, ol = make_pools(w)
+    fill(w, g, o, ol)
+    ref = o.decode_attention(0, w.q(0), w.block_table(), w.ctx(), w.scale)
+    q, bt, ctx = to_dev_bf16(w.q(0)), to_dev_i32(w.block_table()), to_dev_i32(w.ctx())
+    for ctas in [1, 5, 37, 0, 400]:
+        g.decode_set_ctas(ctas)
+        a = bf16_dev_to_f64(g.paged_decode_attention(0, q, bt, ctx, w.scale, max_ctx=max(lens)))
+        b = bf16_dev_to_f64(g.paged_decode_attention(0, q, bt, ctx, w.scale, max_ctx=max(lens)))
+        assert np.array_equal(a, b), f"run-to-run difference with {ctas} CTAs"
+        assert not a[np.asarray(lens) == 0].any(), "empty sequences must give zero rows"
+        compare(a, ref, f"ctas={ctas}")
+    assert g.check_errors() == 0
