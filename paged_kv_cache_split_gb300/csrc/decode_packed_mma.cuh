@@ -689,8 +689,10 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
       }
     }
   };
-  // A whole 32-token unit (both chunks, one softmax, no masks) where registers allow it.
-  constexpr bool kUnit32 = !TWO && (D <= 64 || (RS && D <= 128) || DS);
+  // A whole 32-token unit (both chunks, one softmax, no masks) where registers allow it
+  // (with 16 rows, in the register-split variant: a few spilled registers, one softmax
+  // step per 32 tokens instead of two).
+  constexpr bool kUnit32 = (!TWO && (D <= 64 || (RS && D <= 128) || DS)) || (TWO && RS);
 
   int b = find_seq(UP, B, u0);
   int s = 0;           // stage of the next unit
@@ -914,10 +916,12 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
         float x[NSET][4][2], p[NSET][4][2];
         if (!logits(std::integral_constant<int, 4>{}, sb, 0, x)) return;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          x[0][jj][0] *= s24[0];
-          x[0][jj][1] *= s24[0];
-        }
+        for (int st2 = 0; st2 < NSET; ++st2)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            x[st2][jj][0] *= s24[st2];
+            x[st2][jj][1] *= s24[st2];
+          }
         softmax(std::integral_constant<int, 4>{}, x, p);
         pv(std::false_type{}, sb, 0, p, 0, 16);
         pv(std::false_type{}, sb, 1, p, 2, 16);
