@@ -61,9 +61,9 @@ __device__ __forceinline__ int find_seq(const int32_t* UP, int B, int32_t u) {
 // unit u of sequence b sits at position kCostScale u + seg_cost (b + 1), and CTA c
 // holds the units whose positions lie in [c VC, (c + 1) VC), VC = ceil((kCostScale
 // U + seg_cost B) / grid) but at least kCostScale.  seg_cost 0 gives the plain even
-// split.  The attention
-// kernels (each CTA's unit range, and whether a sequence needs a split-K merge) and
-// the combine (the CTAs holding a sequence's parts) use the same positions.
+// split.  The attention kernels (each CTA's unit range, and whether a sequence needs
+// a split-K merge) and the combine (the CTAs holding a sequence's parts) use the
+// same positions.
 constexpr int kCostScale = 4;
 
 struct Split {
