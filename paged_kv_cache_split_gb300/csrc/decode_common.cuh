@@ -565,15 +565,16 @@ __device__ __forceinline__ void merge_chunk(const float* base, size_t pstride, i
 // L2 prefetches there; its own wait still covers this kernel's completion, and
 // this kernel completes only after the attention grid has.
 //
-// One warp per CTA, at most 80 registers a thread (launch bounds): the block
-// scheduler packs up to eight of these CTAs onto an SM that the attention grid has
-// left, and an attention CTA of the next call (about 44k registers, 219 KB of shared
-// memory) still fits beside eight of them (8 x 80 x 32 registers, 1 KB of shared
-// memory each), so the next call's CTAs are not held back until the merge ends.
+// One warp per CTA (W warps for bf16 prefill), at most 80 registers a thread (launch
+// bounds): the block scheduler packs up to eight of these CTAs onto an SM that the
+// attention grid has left, and an attention CTA of the next call (about 44k
+// registers, 219 KB of shared memory) still fits beside eight one-warp CTAs (8 x 80 x
+// 32 registers, 1 KB of shared memory each), so the next call's CTAs are not held
+// back until the merge ends.
 // With 256-thread CTAs of 176 registers a thread, such CTAs filled the SM's
 // registers and the next call's CTAs on about 16 SMs started 4-5 us late.
-template <int D, int S>
-__global__ void __launch_bounds__(32, 25) combine_kernel(const DecodeParams P, int main_grid) {
+template <int D, int S, int W = 1>
+__global__ void __launch_bounds__(32 * W, 25 / W) combine_kernel(const DecodeParams P, int main_grid) {
   extern __shared__ int32_t cup[];  // unit prefix UP[0..B]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
@@ -690,15 +691,16 @@ inline cudaError_t launch_with_pdl(Kern kern, int grid, int threads, size_t smem
   return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
-template <int D, int S>
+template <int D, int S, int W = 1>
 inline cudaError_t launch_combine_s(const DecodeParams& P, int main_grid, cudaStream_t stream) {
   const int pairs = P.B * P.Hq;
-  // one one-warp CTA per (sequence, head, slice); see combine_kernel
-  int grid = S * pairs;
+  // one warp per (sequence, head, slice), W warps (consecutive items) per CTA; see
+  // combine_kernel
+  int grid = (S * pairs + W - 1) / W;
   if (grid > 8192) grid = 8192;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(32);
+  cfg.blockDim = dim3(32 * W);
   cfg.dynamicSmemBytes = (size_t)(P.B + 1) * sizeof(int32_t);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -706,16 +708,17 @@ inline cudaError_t launch_combine_s(const DecodeParams& P, int main_grid, cudaSt
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<D, S>, P, main_grid);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<D, S, W>, P, main_grid);
 }
 
 // Decode: one warp per (sequence, head); chunked prefill (nq > 1 queries per virtual
 // sequence, so nq times the heads): two warps per head, each merging half of its dims
 // (at head_dim 128, four warps per head merged the bf16 chunk of 8 as fast and the
-// K4/V4 one 2% slower; one warp per head was 8% slower on bf16).
-template <int D>
+// K4/V4 one 2% slower; one warp per head was 8% slower on bf16).  WP: warps per CTA
+// for prefill (the two warps of a head in one CTA: bf16 prefill +4%, K4/V4 -1%).
+template <int D, int WP = 1>
 inline cudaError_t launch_combine(const DecodeParams& P, int main_grid, int nq, cudaStream_t stream) {
-  return nq > 1 ? launch_combine_s<D, 2>(P, main_grid, stream) : launch_combine_s<D, 1>(P, main_grid, stream);
+  return nq > 1 ? launch_combine_s<D, 2, WP>(P, main_grid, stream) : launch_combine_s<D, 1>(P, main_grid, stream);
 }
 
 }  // namespace pkv

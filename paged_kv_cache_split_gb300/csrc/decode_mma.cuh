@@ -417,7 +417,7 @@ cudaError_t launch_decode_bf16_mma_t(const DecodeArgs& a) {
   }
   cudaError_t e = launch_with_pdl(kern, a.grid, (a.lv.hkv + 1) * 32, a.smem_bytes, a.stream, P);
   if (e != cudaSuccess) return e;
-  return launch_combine<D>(P, a.grid, a.nq, a.stream);
+  return launch_combine<D, 2>(P, a.grid, a.nq, a.stream);
 }
 
 
