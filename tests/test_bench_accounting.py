@@ -54,3 +54,26 @@ def test_mixed_row_bytes_is_one_block_of_every_stored_tensor():
     # one 32-token block of one layer: bf16 K and V, or codes plus (scale, offset) pairs
     assert bench.mixed_row_bytes(wl.FMT_BF16, 4, 256) == 32 * 4 * 2 * 256 * 2
     assert bench.mixed_row_bytes(wl.FMT_K4V4, 4, 256) == 32 * 4 * (128 + 128 + 2 * 8 * 8)
+
+
+@pytest.mark.parametrize("fmt,D,G,n_q,launches", [
+    (wl.FMT_BF16, 128, 2, 8, 2),    # 16 rows: the chunk is one tile, no expansion kernel
+    (wl.FMT_BF16, 128, 2, 5, 3),    # one query per tile: expansion + attention + combine
+    (wl.FMT_BF16, 256, 2, 8, 3),    # 8 rows at head_dim 256: two tiles of 4 queries
+    (wl.FMT_K4V4, 128, 2, 8, 2),    # packed, 16 rows
+    (wl.FMT_K4V4, 128, 2, 4, 2),    # packed, 8 rows hold the chunk
+    (wl.FMT_K8V4, 64, 4, 16, 3),    # packed, 16 rows = 4 queries: four tiles
+    (wl.FMT_K4V4, 128, 1, 1, 3),    # a single query keeps the expansion (short sequences flagged)
+])
+def test_prefill_launches_per_call(fmt, D, G, n_q, launches):
+    """The launches the prefill bench line counts per call follow the library's choice
+    of queries per tile (documented with pkv_paged_prefill_attention)."""
+    assert bench.prefill_launches_per_call(fmt, D, G, n_q) == launches
+
+
+def test_kernel_hash_ignores_comments():
+    a = "int f(int x) {  // twice\n  return 2 * x; /* doubled */\n}\n"
+    b = "/* header */\nint f(int x) {\n\n  return 2 * x;   \n}\n"
+    c = "int f(int x) {\n  return 3 * x;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
