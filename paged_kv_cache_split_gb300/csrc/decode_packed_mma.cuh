@@ -480,27 +480,33 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
       for (int cm = 0; cm < NMC; ++cm) {
         const float4 m0 = lds128(m_addr(sb, 2, kc, j, 0, cm));  // token 8j + 2t
         const float4 m1 = lds128(m_addr(sb, 2, kc, j, 1, cm));  // token 8j + 2t + 1
+        // per (scale, offset) pair of the chunk: the products of the groups sharing it
+        // (one group, or two with groups of 64) accumulate in one fragment, folded once
+        // (qsum of the pair's first group holds the pair's sum)
 #pragma unroll
-        for (int q = 0; q < Tr::SPC; ++q) {
-          const int grp = Tr::SPC * cm + q;
-          const bool q2 = q >= Tr::SPP;  // second pair of the chunk
-          uint32_t bfr[2][2];
-          if constexpr (Tr::KBITS == 4) {
-            k_group_frags4(kw[jj][grp], bfr);
-          } else {
-            k_group_frags8(kw[jj][2 * grp], kw[jj][2 * grp + 1], bfr);
-          }
+        for (int pr = 0; pr < 2; ++pr) {
           float cacc[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_f16_16816(cacc, qa[0][grp][0][0], TWO ? qa[NSET - 1][grp][0][0] : 0u, qa[0][grp][0][1],
-                        TWO ? qa[NSET - 1][grp][0][1] : 0u, bfr[0][0], bfr[0][1]);
-          mma_f16_16816(cacc, qa[0][grp][1][0], TWO ? qa[NSET - 1][grp][1][0] : 0u, qa[0][grp][1][1],
-                        TWO ? qa[NSET - 1][grp][1][1] : 0u, bfr[1][0], bfr[1][1]);
-          const float sc0 = q2 ? m0.z : m0.x, of0 = q2 ? m0.w : m0.y;
-          const float sc1 = q2 ? m1.z : m1.x, of1 = q2 ? m1.w : m1.y;
+#pragma unroll
+          for (int gi = 0; gi < Tr::SPP; ++gi) {
+            const int grp = Tr::SPC * cm + Tr::SPP * pr + gi;
+            uint32_t bfr[2][2];
+            if constexpr (Tr::KBITS == 4) {
+              k_group_frags4(kw[jj][grp], bfr);
+            } else {
+              k_group_frags8(kw[jj][2 * grp], kw[jj][2 * grp + 1], bfr);
+            }
+            mma_f16_16816(cacc, qa[0][grp][0][0], TWO ? qa[NSET - 1][grp][0][0] : 0u, qa[0][grp][0][1],
+                          TWO ? qa[NSET - 1][grp][0][1] : 0u, bfr[0][0], bfr[0][1]);
+            mma_f16_16816(cacc, qa[0][grp][1][0], TWO ? qa[NSET - 1][grp][1][0] : 0u, qa[0][grp][1][1],
+                          TWO ? qa[NSET - 1][grp][1][1] : 0u, bfr[1][0], bfr[1][1]);
+          }
+          const int lead = Tr::SPC * cm + Tr::SPP * pr;
+          const float sc0 = pr ? m0.z : m0.x, of0 = pr ? m0.w : m0.y;
+          const float sc1 = pr ? m1.z : m1.x, of1 = pr ? m1.w : m1.y;
 #pragma unroll
           for (int st2 = 0; st2 < NSET; ++st2) {
-            sa[st2][0] = fmaf(sc0, cacc[2 * st2], fmaf(of0, qsum[st2][grp], sa[st2][0]));
-            sa[st2][1] = fmaf(sc1, cacc[2 * st2 + 1], fmaf(of1, qsum[st2][grp], sa[st2][1]));
+            sa[st2][0] = fmaf(sc0, cacc[2 * st2], fmaf(of0, qsum[st2][lead], sa[st2][0]));
+            sa[st2][1] = fmaf(sc1, cacc[2 * st2 + 1], fmaf(of1, qsum[st2][lead], sa[st2][1]));
           }
         }
       }
@@ -663,8 +669,10 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
           const float* p1 = p[st2][jp + 1];
           pb[st2][0] = pack_f16x2(p0[0] * sv00, p0[1] * sv01);
           pb[st2][1] = pack_f16x2(p1[0] * sv10, p1[1] * sv11);
-          corr[st2][grp] =
-              fmaf(p0[0], ov00, fmaf(p0[1], ov01, fmaf(p1[0], ov10, fmaf(p1[1], ov11, corr[st2][grp]))));
+          // the offsets term, once per (scale, offset) pair (in its first group's slot)
+          if (q % Tr::SPP == 0)
+            corr[st2][grp] =
+                fmaf(p0[0], ov00, fmaf(p0[1], ov01, fmaf(p1[0], ov10, fmaf(p1[1], ov11, corr[st2][grp]))));
         }
         if constexpr (Tr::VBITS == 4) {
           const uint32_t x01 = vx[0][grp], x23 = vx[1][grp];
@@ -907,6 +915,12 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
             tsum += __shfl_xor_sync(0xffffffffu, tsum, 2);
             qsum[st2][grp] = tsum * 5.9604644775390625e-08f;  // 2^-24
           }
+          if constexpr (Tr::SPP == 2) {
+            // groups sharing a (scale, offset) pair fold together: the pair's sum of q~
+            // in its first group's slot
+#pragma unroll
+            for (int grp = 0; grp < NGL; grp += 2) qsum[st2][grp] += qsum[st2][grp + 1];
+          }
         }
         __syncwarp();
       }
@@ -971,7 +985,7 @@ __global__ void __launch_bounds__(RS ? kRsThreads : kMaxThreads, 1) decode_packe
       float ce[NGL], co[NGL];
 #pragma unroll
       for (int grp = 0; grp < NGL; ++grp) {
-        float c = corr[st2][grp];
+        float c = corr[st2][grp - grp % Tr::SPP];  // a pair's offsets term sits in its first group
         c += __shfl_xor_sync(0xffffffffu, c, 1);
         c += __shfl_xor_sync(0xffffffffu, c, 2);
         ce[grp] = __shfl_sync(0xffffffffu, c, 8 * t);
